@@ -1,0 +1,232 @@
+"""Seeded synthetic inputs for top-k sparse attention and the top-k mask.
+
+This module only draws random numbers and lays out index patterns; it holds
+none of the method's arithmetic, so the CPU oracle (tests) and the CUDA
+library both consume exactly the same bits from it.  Everything is generated
+on the CPU with ``torch.Generator().manual_seed(seed)`` and may be moved to a
+device afterwards.
+
+Shapes and index structure follow the workloads the pages describe for
+DeepSeek V4 ("DeepSeek V4 源码剖析, 第5章", §5.1 and §5.14): q [B,S,128,512]
+bf16, a shared kv [B,T,512] bf16, a float32 sink per head, int32 top-k indices
+[B,S,K] with -1 for an invalid slot, K = 128 window rows + 1024 indexer picks
+on a ratio-4 layer, 128 window rows + every compressed row on a ratio-128
+layer.  The kv layout puts the window rows first and the compressed rows after
+them; indexer picks are random distinct compressed rows (unsorted, as a top-k
+selection returns them).  The mask workload follows the vLLM PR 52217/48770
+pages: per-request top-k rows scattered into a padded uint32 bitmask.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+SENTINEL_U32 = 0xA5A5A5A5
+
+
+@dataclass
+class AttnInputs:
+    q: torch.Tensor          # [B,S,H,D] bf16
+    kv: torch.Tensor         # [B,T,D]   bf16
+    attn_sink: torch.Tensor  # [H]       float32
+    topk_idxs: torch.Tensor  # [B,S,K]   int32, -1 = invalid slot
+    softmax_scale: float
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def shape(self):
+        B, S, H, D = self.q.shape
+        return dict(B=B, S=S, H=H, D=D, T=self.kv.shape[1], K=self.topk_idxs.shape[-1])
+
+    def to(self, device):
+        return AttnInputs(self.q.to(device), self.kv.to(device), self.attn_sink.to(device),
+                          self.topk_idxs.to(device), self.softmax_scale, self.name, dict(self.meta))
+
+
+@dataclass
+class MaskInputs:
+    topk: torch.Tensor       # [sum q_len, K] int32
+    cu_q_lens: torch.Tensor  # [B+1] int32
+    batch: int
+    max_q_len: int
+    max_key_len: int
+    key_starts: torch.Tensor | None  # [B] int32 or None
+    name: str = ""
+
+    def to(self, device):
+        return MaskInputs(self.topk.to(device), self.cu_q_lens.to(device), self.batch, self.max_q_len,
+                          self.max_key_len, None if self.key_starts is None else self.key_starts.to(device),
+                          self.name)
+
+
+def _gen(seed: int) -> torch.Generator:
+    return torch.Generator().manual_seed(int(seed))
+
+
+def _randn_bf16(shape, g) -> torch.Tensor:
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _distinct(n_pool: int, k: int, g) -> torch.Tensor:
+    """k distinct values of [0, n_pool) in random order."""
+    return torch.randperm(n_pool, generator=g)[:k].to(torch.int32)
+
+
+def random_attn(B, S, H, D, T, K, *, p_invalid=0.1, seed=0, distinct=True, scale=None) -> AttnInputs:
+    """Generic case: per token, K slots drawn from [0,T) (distinct when K<=T),
+    each set to -1 with probability p_invalid."""
+    g = _gen(seed)
+    q = _randn_bf16((B, S, H, D), g)
+    kv = _randn_bf16((B, T, D), g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.empty((B, S, K), dtype=torch.int32)
+    for b in range(B):
+        for s in range(S):
+            if distinct and K <= T:
+                idx[b, s] = _distinct(T, K, g)
+            else:
+                idx[b, s] = torch.randint(0, max(T, 1), (K,), generator=g, dtype=torch.int32)
+    if p_invalid > 0:
+        drop = torch.rand((B, S, K), generator=g) < p_invalid
+        idx[drop] = -1
+    return AttnInputs(q, kv, sink, idx, float(scale if scale is not None else D ** -0.5),
+                      name=f"random B={B} S={S} H={H} D={D} T={T} K={K}")
+
+
+def tiny(seed=1000) -> AttnInputs:
+    """B=1,S=4,H=8,D=64,T=256,K=64: the first 64 of a random permutation of
+    [0,256) per token, each slot -1 with probability 0.1, scale = 1/8."""
+    out = random_attn(1, 4, 8, 64, 256, 64, p_invalid=0.1, seed=seed)
+    out.name = "tiny B=1 S=4 H=8 D=64 T=256 K=64"
+    return out
+
+
+def v4_ratio4_decode(seed=1001, B=32, H=128, D=512, window=128, topk=1024, ratio=4,
+                     long_ctx=65536, short_lo=128, short_hi=4096) -> AttnInputs:
+    """Ratio-4 decode: T = window + long_ctx/ratio; K = window + topk.
+    Context L_b = long_ctx for the upper half of the batch and uniform in
+    [short_lo, short_hi) for the lower half.  Slots: the window rows
+    0..window-1 (valid for min(window, L_b)), then min(topk, L_b//ratio)
+    distinct random compressed rows from [window, window + L_b//ratio),
+    then -1."""
+    g = _gen(seed)
+    n_comp = long_ctx // ratio
+    T = window + n_comp
+    K = window + topk
+    q = _randn_bf16((B, 1, H, D), g)
+    kv = _randn_bf16((B, T, D), g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.full((B, 1, K), -1, dtype=torch.int32)
+    ctx = []
+    for b in range(B):
+        L = long_ctx if b >= B // 2 else int(torch.randint(short_lo, short_hi, (1,), generator=g))
+        ctx.append(L)
+        nw = min(window, L)
+        idx[b, 0, :nw] = torch.arange(nw, dtype=torch.int32)
+        pool = L // ratio
+        nc = min(topk, pool)
+        idx[b, 0, window:window + nc] = window + _distinct(pool, nc, g)
+    return AttnInputs(q, kv, sink, idx, D ** -0.5,
+                      name=f"V4 ratio-4 decode B={B} S=1 H={H} D={D} T={T} K={K}",
+                      meta=dict(context=ctx))
+
+
+def v4_prefill(seed=1002, S=4096, H=128, D=512, window=128, topk=1024, ratio=4) -> AttnInputs:
+    """Prefill of one S-token chunk: kv rows 0..S-1 are the chunk's own
+    tokens, rows S..S+S/ratio-1 the compressed rows.  Token s: window slots
+    s-window+1..s ascending (-1 when negative), then min(topk, (s+1)//ratio)
+    distinct random compressed rows from [S, S + (s+1)//ratio), then -1."""
+    g = _gen(seed)
+    n_comp = S // ratio
+    T = S + n_comp
+    K = window + topk
+    q = _randn_bf16((1, S, H, D), g)
+    kv = _randn_bf16((1, T, D), g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.full((1, S, K), -1, dtype=torch.int32)
+    win = torch.arange(-window + 1, 1, dtype=torch.int32)
+    for s in range(S):
+        w = win + s
+        idx[0, s, :window] = torch.where(w >= 0, w, torch.full_like(w, -1))
+        pool = (s + 1) // ratio
+        nc = min(topk, pool)
+        if nc > 0:
+            idx[0, s, window:window + nc] = S + _distinct(pool, nc, g)
+    return AttnInputs(q, kv, sink, idx, D ** -0.5, name=f"V4 prefill B=1 S={S} H={H} D={D} T={T} K={K}")
+
+
+def v4_ratio128_decode(seed=1003, B=64, H=128, D=512, window=128, end_pos=65536, ratio=128) -> AttnInputs:
+    """Ratio-128 decode: K = T = window + end_pos/ratio.  Even b: every slot
+    valid, idx = 0..K-1.  Odd b: end_b uniform in [1, end_pos); the first
+    min(window, end_b) window slots and the first end_b//ratio compressed
+    slots are valid, the rest -1."""
+    g = _gen(seed)
+    n_comp = end_pos // ratio
+    T = window + n_comp
+    K = T
+    q = _randn_bf16((B, 1, H, D), g)
+    kv = _randn_bf16((B, T, D), g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.full((B, 1, K), -1, dtype=torch.int32)
+    ends = []
+    for b in range(B):
+        if b % 2 == 0:
+            idx[b, 0] = torch.arange(K, dtype=torch.int32)
+            ends.append(end_pos)
+            continue
+        e = int(torch.randint(1, end_pos, (1,), generator=g))
+        ends.append(e)
+        nw = min(window, e)
+        idx[b, 0, :nw] = torch.arange(nw, dtype=torch.int32)
+        nc = e // ratio
+        idx[b, 0, window:window + nc] = window + torch.arange(nc, dtype=torch.int32)
+    return AttnInputs(q, kv, sink, idx, D ** -0.5,
+                      name=f"V4 ratio-128 decode B={B} S=1 H={H} D={D} T={T} K={K}", meta=dict(end=ends))
+
+
+def topk_mask(seed=1004, B=4, Q=2048, max_key_len=8193, K=2048, key_starts=(0, 1, 31, 8192),
+              q_lens=None) -> MaskInputs:
+    """Mask build: request b has q_lens[b] (default Q) query rows; row q sits at
+    absolute position p = max_key_len - Q + q and holds K distinct uniform
+    indices from [0, p] (fewer candidates than K: -1 fill)."""
+    g = _gen(seed)
+    q_lens = [Q] * B if q_lens is None else list(q_lens)
+    cu = [0]
+    rows = []
+    for b in range(B):
+        for qi in range(q_lens[b]):
+            p = max_key_len - Q + qi
+            n = min(K, p + 1)
+            r = torch.full((K,), -1, dtype=torch.int32)
+            if n > 0:
+                r[:n] = _distinct(p + 1, n, g)
+            rows.append(r)
+        cu.append(cu[-1] + q_lens[b])
+    topk = torch.stack(rows) if rows else torch.empty((0, K), dtype=torch.int32)
+    ks = None if key_starts is None else torch.tensor(list(key_starts)[:B], dtype=torch.int32)
+    return MaskInputs(topk, torch.tensor(cu, dtype=torch.int32), B, max(q_lens) if q_lens else 0,
+                      max_key_len, ks, name=f"topk mask B={B} Q={Q} keys={max_key_len} K={K}")
+
+
+CONFIGS = {
+    "tiny": tiny,
+    "v4_ratio4_decode": v4_ratio4_decode,
+    "v4_prefill": v4_prefill,
+    "v4_ratio128_decode": v4_ratio128_decode,
+}
+
+
+def count_valid(idx: torch.Tensor, T: int) -> int:
+    """Number of slots with 0 <= idx < T (the work a sparse kernel must do)."""
+    return int(((idx >= 0) & (idx < T)).sum())
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b) if b else 0
+
+
+def nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()

@@ -1,0 +1,163 @@
+"""CPU oracle for top-k sparse attention and the bit-packed top-k mask.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product library (``deepseek_top_sparse_gb300``) never imports it, and the two
+share no code: the arithmetic lives in ``oracle.c`` (plain C, float64), this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+
+What each routine follows (page title and section):
+
+* ``sparse_attn`` -- "DeepSeek V4 源码剖析, 第5章", §5.2 pseudocode (per query
+  token and head: gather the indexed kv rows, logits = scale * q.k, -inf on
+  invalid slots, append the per-head sink logit, softmax, weighted sum of the
+  gathered rows without the sink) and §5.5 (the sink only enters the
+  denominator; sink = +inf zeroes all real weights, -inf means no sink).
+* ``masked_dense_attn`` -- the consumer semantics of the bit mask from the
+  vLLM PR 48770 page (``dense_mask_mod`` / ``offset_dense_mask_mod``): key k
+  is admitted iff bit k&31 of word k>>5 of its query row is set.
+* ``topk_mask_shape`` / ``build_topk_mask`` -- vLLM PR 52217 page
+  (``_topk_mask_shape``, ``_build_topk_mask`` and the two alignment tests) and
+  the PR 48770 page (bit order, reserved key_start word).
+
+Pins against the pages and closed forms live in ``tests/test_oracle_pins.py``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, -O2, pthreads)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_sparse_attn.argtypes = [p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, ctypes.c_int]
+            lib.oracle_sparse_attn_tokens.argtypes = (
+                [p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
+            lib.oracle_masked_dense_attn.argtypes = [p, p, p, p, i64, i64, p, ctypes.c_double] + [i64] * 5 + [p]
+            lib.oracle_topk_mask_shape.argtypes = [i64, i64, i64, ctypes.c_int, p]
+            lib.oracle_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p]
+            for f in (lib.oracle_sparse_attn, lib.oracle_sparse_attn_tokens, lib.oracle_masked_dense_attn,
+                      lib.oracle_topk_mask_shape, lib.oracle_build_topk_mask):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """Accept a torch bf16 tensor or a uint16 array of bf16 bit patterns."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch  # local: numpy-only callers need no torch
+
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _np(x, dtype):
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=dtype)
+    return np.ascontiguousarray(x.detach().cpu().numpy(), dtype=dtype)
+
+
+def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0):
+    """float64 o[B,S,H,D] (or o[len(tokens),H,D] for flat token ids b*S+s)."""
+    qb, kvb = _bf16_bits(q), _bf16_bits(kv)
+    sink = _np(attn_sink, np.float32)
+    idx = _np(topk_idxs, np.int32)
+    B, S, H, D = qb.shape
+    T = kvb.shape[1]
+    K = idx.shape[-1]
+    assert kvb.shape == (B, T, D) and idx.shape == (B, S, K) and sink.shape == (H,)
+    lib = _load()
+    if tokens is None:
+        o = np.zeros((B, S, H, D), dtype=np.float64)
+        rc = lib.oracle_sparse_attn(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), float(softmax_scale),
+                                    B, S, H, D, T, K, _ptr(o), int(nthreads))
+    else:
+        tok = np.ascontiguousarray(tokens, dtype=np.int64)
+        o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
+        rc = lib.oracle_sparse_attn_tokens(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), float(softmax_scale),
+                                           B, S, H, D, T, K, _ptr(tok), tok.shape[0], _ptr(o), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_attn rejected its arguments (rc={rc})")
+    return o
+
+
+def masked_dense_attn(q, kv, attn_sink, mask, softmax_scale: float, key_offset=None):
+    """float64 o[B,S,H,D]: dense attention over the keys the bit mask admits."""
+    qb, kvb = _bf16_bits(q), _bf16_bits(kv)
+    sink = _np(attn_sink, np.float32)
+    m = _np(mask, np.int64).astype(np.uint32) if not isinstance(mask, np.ndarray) or mask.dtype != np.uint32 \
+        else np.ascontiguousarray(mask)
+    B, S, H, D = qb.shape
+    T = kvb.shape[1]
+    assert m.shape[0] == B and m.shape[1] >= S
+    off = None if key_offset is None else np.ascontiguousarray(key_offset, dtype=np.int64)
+    o = np.zeros((B, S, H, D), dtype=np.float64)
+    rc = _load().oracle_masked_dense_attn(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(m), m.shape[1], m.shape[2],
+                                          _ptr(off), float(softmax_scale), B, S, H, D, T, _ptr(o))
+    if rc != 0:
+        raise ValueError(f"oracle_masked_dense_attn rejected its arguments (rc={rc})")
+    return o
+
+
+def topk_mask_shape(batch: int, max_query_len: int, max_key_len: int,
+                    reserve_key_starts_word: bool = False) -> tuple[int, int, int]:
+    out = np.zeros(3, dtype=np.int64)
+    rc = _load().oracle_topk_mask_shape(batch, max_query_len, max_key_len, int(bool(reserve_key_starts_word)),
+                                        _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_topk_mask_shape: negative size")
+    return int(out[0]), int(out[1]), int(out[2])
+
+
+def build_topk_mask(topk, cu_q_lens, batch: int, max_q_len: int, max_key_len: int,
+                    key_starts=None, out: np.ndarray | None = None) -> np.ndarray:
+    """uint32 mask [B, padded_Q, W].  ``out`` (uint32, the right shape) keeps
+    whatever it holds outside the words the build writes."""
+    tk = _np(topk, np.int32)
+    if tk.ndim == 1:
+        tk = tk.reshape(-1, 1)
+    cu = _np(cu_q_lens, np.int32)
+    assert cu.shape == (batch + 1,)
+    ks = None if key_starts is None else _np(key_starts, np.int32)
+    shape = topk_mask_shape(batch, max_q_len, max_key_len, ks is not None)
+    if out is None:
+        out = np.zeros(shape, dtype=np.uint32)
+    assert out.dtype == np.uint32 and out.ndim == 3 and out.flags.c_contiguous
+    shp = np.asarray(out.shape, dtype=np.int64)  # the C routine rejects a wrong shape
+    rc = _load().oracle_build_topk_mask(_ptr(tk), tk.shape[0], _ptr(cu), batch, max_q_len, max_key_len,
+                                        tk.shape[1], _ptr(ks), _ptr(out), _ptr(shp))
+    if rc != 0:
+        raise ValueError(f"oracle_build_topk_mask rejected its arguments (rc={rc})")
+    return out

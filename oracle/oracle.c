@@ -1,0 +1,294 @@
+/*
+ * CPU ORACLE -- test infrastructure only.
+ *
+ * A plain, slow, double-precision restatement of what top-k sparse attention
+ * and the bit-packed top-k mask compute.  Only the test suite, the smoke check
+ * and the CPU-baseline leg of the benchmark may load this library; the product
+ * path (the CUDA library) never calls it and shares no code with it.
+ *
+ * Sources, cited by page title and section:
+ *   [V4-5.2]  "DeepSeek V4 源码剖析, 第5章 sparse_attn 与 FlashMLA", §5.2
+ *             (interface semantics, per-(b,s,h) pseudocode) and §5.1 (shapes,
+ *             -1 marks an invalid slot, softmax_scale = head_dim^-0.5).
+ *   [V4-5.5]  same chapter, §5.5: the sink enters the softmax denominator only;
+ *             sink = +inf zeroes every real weight, sink = -inf means no sink.
+ *   [MASK-SHAPE] vLLM PR 52217 page ("Sparse MLA mask 向量化 128-bit 加载"),
+ *             key source excerpt `_topk_mask_shape`, `_build_topk_mask`, and the
+ *             two tests (129 keys -> 8 words; bits 0 and 128 in words 0 and 4).
+ *   [MASK-BITS] vLLM PR 48770 page (masked MHA for sparse-MLA prefill), source
+ *             excerpt `dense_mask_mod` / `offset_dense_mask_mod`: word kv>>5,
+ *             bit kv&31, LSB first; the last word of row q=0 holds key_start.
+ *
+ * Readings taken where the pages are silent (each one is tested):
+ *   R1 a slot is valid iff 0 <= idx < T (the pages only define -1).
+ *   R3 all slots invalid, finite sink -> o = 0 (weights are [0..0, 1]).
+ *   R4 sink = +inf -> o = 0.      R6 sink = -inf and no valid slot -> o = 0.
+ *   R8 the scale multiplies q.k only; the sink is a raw logit.
+ *   R14 live mask words [0, ceil(max_key_len/32)) are cleared then OR-ed;
+ *   R15 padding words and rows q >= q_len are never written;
+ *   R16 the reserved word of row 0 holds the raw bits of key_starts[b].
+ *
+ * Inputs are bf16 bit patterns (uint16) as stored on the device; each value
+ * is widened exactly to double before any arithmetic.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* sparse_attn, [V4-5.2]                                                     */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *q, *kv;
+    const float *sink;
+    const int32_t *idx;
+    double scale;
+    double *o;
+    int64_t B, S, H, D, T, K;
+    const int64_t *tokens; /* flat b*S+s token ids to evaluate */
+    int64_t ntok;
+    int64_t next; /* work counter, guarded by mu */
+    pthread_mutex_t mu;
+} attn_job;
+
+/* One query token (b, s), every head h:
+ *   logits_j = scale * q[b,s,h,:] . kv[b, idx_j, :]   for valid slots j,
+ *   -inf for invalid ones; the sink logit attn_sink[h] is appended; softmax
+ *   over the K+1 values; o = sum_{j<K} w_j * kv[b, idx_j, :] (the sink's
+ *   weight is dropped).  [V4-5.2], [V4-5.5] */
+static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] */) {
+    const int64_t b = tok / J->S, s = tok % J->S;
+    const int64_t H = J->H, D = J->D, T = J->T, K = J->K;
+    const int32_t *idx = J->idx + (b * J->S + s) * K;
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int64_t h = 0; h < H; ++h) {
+        double *orow = out + h * D;
+        for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
+        const uint16_t *qh = J->q + ((b * J->S + s) * H + h) * D;
+        for (int64_t d = 0; d < D; ++d) qrow[d] = bf16_to_double(qh[d]);
+        /* logits of the K slots, -inf where the slot is invalid (R1) */
+        for (int64_t j = 0; j < K; ++j) {
+            int64_t t = idx[j];
+            if (t < 0 || t >= T) {
+                logit[j] = -INFINITY;
+                continue;
+            }
+            const uint16_t *kr = J->kv + (b * T + t) * D;
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += qrow[d] * bf16_to_double(kr[d]);
+            logit[j] = dot * J->scale; /* R8: scale on q.k only */
+        }
+        const double sink = (double)J->sink[h];
+        /* softmax over [logits..., sink] */
+        double m = sink;
+        for (int64_t j = 0; j < K; ++j)
+            if (logit[j] > m) m = logit[j];
+        if (isnan(sink)) { /* R7: NaN propagates */
+            for (int64_t d = 0; d < D; ++d) orow[d] = NAN;
+            continue;
+        }
+        if (m == INFINITY && sink == INFINITY) continue; /* R4: o = 0 */
+        if (m == -INFINITY) continue;                    /* R6: o = 0 */
+        double denom = exp(sink - m);
+        for (int64_t j = 0; j < K; ++j) denom += exp(logit[j] - m);
+        for (int64_t j = 0; j < K; ++j) {
+            if (logit[j] == -INFINITY) continue; /* weight exactly 0 */
+            const double w = exp(logit[j] - m) / denom;
+            const uint16_t *kr = J->kv + (b * T + idx[j]) * D;
+            for (int64_t d = 0; d < D; ++d) orow[d] += w * bf16_to_double(kr[d]);
+        }
+    }
+    free(logit);
+    free(qrow);
+}
+
+static void *attn_worker(void *arg) {
+    attn_job *J = (attn_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int64_t i = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (i >= J->ntok) break;
+        attn_one_token(J, J->tokens[i], J->o + i * J->H * J->D);
+    }
+    return NULL;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D]. */
+int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                              const int32_t *topk_idxs, double softmax_scale, int64_t B,
+                              int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
+                              const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
+    if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || K < 0 || ntok < 0) return ORACLE_EINVAL;
+    for (int64_t i = 0; i < ntok; ++i)
+        if (tokens[i] < 0 || tokens[i] >= B * S) return ORACLE_EINVAL;
+    attn_job J;
+    J.q = q; J.kv = kv; J.sink = attn_sink; J.idx = topk_idxs; J.scale = softmax_scale;
+    J.o = o; J.B = B; J.S = S; J.H = H; J.D = D; J.T = T; J.K = K;
+    J.tokens = tokens; J.ntok = ntok; J.next = 0;
+    pthread_mutex_init(&J.mu, NULL);
+    int nt = resolve_threads(nthreads);
+    if (nt > ntok) nt = ntok > 0 ? (int)ntok : 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, attn_worker, &J);
+    for (int i = 0; i < nt; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.mu);
+    return ORACLE_OK;
+}
+
+/* Every token; o is [B,S,H,D]. */
+int oracle_sparse_attn(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                       const int32_t *topk_idxs, double softmax_scale, int64_t B, int64_t S,
+                       int64_t H, int64_t D, int64_t T, int64_t K, double *o, int nthreads) {
+    int64_t n = B * S;
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    for (int64_t i = 0; i < n; ++i) tok[i] = i;
+    int rc = oracle_sparse_attn_tokens(q, kv, attn_sink, topk_idxs, softmax_scale, B, S, H, D,
+                                       T, K, tok, n, o, nthreads);
+    free(tok);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense attention under a bit-packed key mask (the consumer side of the     */
+/* mask, [MASK-BITS]): key t of kv[b] is admitted for query (b,s) iff bit    */
+/* ((t + key_offset[b]) & 31) of word ((t + key_offset[b]) >> 5) in row      */
+/* mask[b, s, :] is set.  Same softmax-with-sink as above over the admitted  */
+/* keys.  key_offset may be NULL (all zero, `dense_mask_mod`); a non-NULL    */
+/* offset is the chunked-context reading (`offset_dense_mask_mod`).          */
+/* ------------------------------------------------------------------------ */
+int oracle_masked_dense_attn(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                             const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                             const int64_t *key_offset, double softmax_scale, int64_t B,
+                             int64_t S, int64_t H, int64_t D, int64_t T, double *o) {
+    if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || mask_rows < S || mask_words < 0)
+        return ORACLE_EINVAL;
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t off = key_offset ? key_offset[b] : 0;
+        for (int64_t s = 0; s < S; ++s) {
+            const uint32_t *row = mask + (b * mask_rows + s) * mask_words;
+            for (int64_t h = 0; h < H; ++h) {
+                double *orow = o + ((b * S + s) * H + h) * D;
+                for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
+                const uint16_t *qh = q + ((b * S + s) * H + h) * D;
+                for (int64_t t = 0; t < T; ++t) {
+                    int64_t key = t + off;
+                    int on = key >= 0 && (key >> 5) < mask_words &&
+                             ((row[key >> 5] >> (key & 31)) & 1u);
+                    if (!on) {
+                        logit[t] = -INFINITY;
+                        continue;
+                    }
+                    const uint16_t *kr = kv + (b * T + t) * D;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += bf16_to_double(qh[d]) * bf16_to_double(kr[d]);
+                    logit[t] = dot * softmax_scale;
+                }
+                const double sink = (double)attn_sink[h];
+                if (isnan(sink)) {
+                    for (int64_t d = 0; d < D; ++d) orow[d] = NAN;
+                    continue;
+                }
+                double m = sink;
+                for (int64_t t = 0; t < T; ++t)
+                    if (logit[t] > m) m = logit[t];
+                if (m == INFINITY && sink == INFINITY) continue;
+                if (m == -INFINITY) continue;
+                double denom = exp(sink - m);
+                for (int64_t t = 0; t < T; ++t) denom += exp(logit[t] - m);
+                for (int64_t t = 0; t < T; ++t) {
+                    if (logit[t] == -INFINITY) continue;
+                    const double w = exp(logit[t] - m) / denom;
+                    const uint16_t *kr = kv + (b * T + t) * D;
+                    for (int64_t d = 0; d < D; ++d) orow[d] += w * bf16_to_double(kr[d]);
+                }
+            }
+        }
+    }
+    free(logit);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bit-packed top-k mask, [MASK-SHAPE], [MASK-BITS]                          */
+/* ------------------------------------------------------------------------ */
+
+static int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* (batch, padded query rows, words per row):
+ *   tile_m = 128 when max_query_len <= 128, else 256;
+ *   rows   = ceil(max_query_len / tile_m) * tile_m;
+ *   words  = ceil(max_key_len / 32) + reserve, rounded up to a multiple of 4
+ *            so every row starts on a 16-byte boundary. */
+int oracle_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key_len,
+                           int reserve_key_starts_word, int64_t out_shape[3]) {
+    if (batch < 0 || max_query_len < 0 || max_key_len < 0) return ORACLE_EINVAL;
+    const int64_t tile_m = max_query_len <= 128 ? 128 : 256;
+    const int64_t rows = cdiv64(max_query_len, tile_m) * tile_m;
+    int64_t words = cdiv64(max_key_len, 32) + (reserve_key_starts_word ? 1 : 0);
+    words = cdiv64(words, 4) * 4;
+    out_shape[0] = batch;
+    out_shape[1] = rows;
+    out_shape[2] = words;
+    return ORACLE_OK;
+}
+
+/* Writes, bit by bit, the mask of every live row (b, q < q_len_b): word
+ * k>>5 of row (b,q) gets bit k&31 for each index k of topk row
+ * cu_q_lens[b] + q with 0 <= k < max_key_len (R14).  Live words are cleared
+ * first.  When key_starts is non-NULL, word W-1 of row (b, 0) receives the
+ * raw bits of key_starts[b] (R16).  Nothing else is written (R15). */
+int oracle_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                           int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
+                           const int32_t *key_starts, uint32_t *mask,
+                           const int64_t mask_shape[3]) {
+    int64_t want[3];
+    if (oracle_topk_mask_shape(B, max_q_len, max_key_len, key_starts != NULL, want))
+        return ORACLE_EINVAL;
+    if (mask_shape[0] != want[0] || mask_shape[1] != want[1] || mask_shape[2] != want[2])
+        return ORACLE_EINVAL;
+    const int64_t R = want[1], W = want[2];
+    const int64_t live_words = cdiv64(max_key_len, 32);
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t q_len = (int64_t)cu_q_lens[b + 1] - (int64_t)cu_q_lens[b];
+        if (q_len > max_q_len) q_len = max_q_len;
+        for (int64_t qi = 0; qi < q_len; ++qi) {
+            const int64_t src = (int64_t)cu_q_lens[b] + qi;
+            if (src < 0 || src >= topk_rows) continue;
+            uint32_t *row = mask + (b * R + qi) * W;
+            for (int64_t w = 0; w < live_words; ++w) row[w] = 0u;
+            for (int64_t j = 0; j < K; ++j) {
+                const int64_t k = topk[src * K + j];
+                if (k < 0 || k >= max_key_len) continue;
+                row[k >> 5] |= 1u << (k & 31);
+            }
+        }
+        if (key_starts != NULL && R > 0 && W > 0)
+            mask[(b * R + 0) * W + (W - 1)] = (uint32_t)key_starts[b];
+    }
+    return ORACLE_OK;
+}

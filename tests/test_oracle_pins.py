@@ -1,0 +1,311 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped sink
+term, the scale applied to the sink, a wrong sign, the wrong batch's kv, a
+transposed operand, an off-by-one word or bit) fails at least one of them:
+
+* values printed by the pages (tests/golden/*.txt, each with its source);
+* closed forms: K = 1 (a logistic of logit - sink), identical kv rows,
+  q = 0 (uniform weights);
+* a library routine: torch's scaled_dot_product_attention in float64 with an
+  additive mask, where the sink is an extra key whose value row is zero;
+* invariants: slot permutation, moving invalid slots, sink limits;
+* brute force: the mask decoded bit by bit against Python sets.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_top_sparse_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- mask shape
+
+def _golden_shapes():
+    out = []
+    with open(os.path.join(GOLDEN, "mask_shape.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            lhs, rhs = line.split("->")
+            out.append((tuple(int(v) for v in lhs.split()), tuple(int(v) for v in rhs.split())))
+    return out
+
+
+@pytest.mark.parametrize("args,want", _golden_shapes())
+def test_mask_shape_golden(args, want):
+    b, q, k, r = args
+    assert oracle.topk_mask_shape(b, q, k, bool(r)) == want
+
+
+def test_mask_shape_rows_are_16_byte_aligned():
+    for q in (0, 1, 127, 128, 129, 255, 256, 257, 4097):
+        for k in (0, 1, 31, 32, 33, 127, 128, 129, 8193):
+            for r in (False, True):
+                _, rows, words = oracle.topk_mask_shape(3, q, k, r)
+                assert words % 4 == 0 and words * 32 >= k + 32 * r
+                assert words < (-(-k // 32) + r) + 4
+                assert rows >= q and rows % 128 == 0
+
+
+# ---------------------------------------------------------------- mask build
+
+def _golden_example():
+    kv = {}
+    with open(os.path.join(GOLDEN, "mask_build_example.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, *vals = line.split()
+                kv[key] = [int(v) for v in vals]
+    return kv
+
+
+def test_mask_build_worked_example():
+    ex = _golden_example()
+    B, Q, KEYS = ex["batch"][0], ex["max_q_len"][0], ex["max_key_len"][0]
+    shape = oracle.topk_mask_shape(B, Q, KEYS)
+    out = np.zeros(shape, dtype=np.uint32)
+    topk = np.array([ex["topk"]], dtype=np.int32)
+    m = oracle.build_topk_mask(topk, np.array([0, 1], np.int32), B, Q, KEYS, out=out)
+    assert m[:B, :Q].shape == (1, 1, 8)
+    assert m[0, 0].tolist() == ex["row"]
+
+
+def _decode_row(words, n_keys):
+    return {k for k in range(n_keys) if (int(words[k >> 5]) >> (k & 31)) & 1}
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mask_build_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    q_lens = [int(rng.integers(0, 6)) for _ in range(B)]
+    max_q = max(q_lens + [1]) + int(rng.integers(0, 2))
+    keys = int(rng.integers(1, 200))
+    K = int(rng.integers(1, 40))
+    reserve = bool(rng.integers(0, 2))
+    rows = sum(q_lens)
+    # indices include -1, out-of-range values and duplicates on purpose
+    topk = rng.integers(-3, keys + 5, size=(rows, K)).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    ks = rng.integers(-2**31, 2**31 - 1, size=B).astype(np.int32) if reserve else None
+    shape = oracle.topk_mask_shape(B, max_q, keys, reserve)
+    out = np.full(shape, workloads.SENTINEL_U32, dtype=np.uint32)
+    m = oracle.build_topk_mask(topk, cu, B, max_q, keys, key_starts=ks, out=out)
+    n_live = -(-keys // 32)
+    for b in range(B):
+        for q in range(shape[1]):
+            row = m[b, q]
+            if q < q_lens[b]:
+                want = {int(v) for v in topk[cu[b] + q] if 0 <= v < keys}
+                assert _decode_row(row, keys) == want
+                # bits beyond max_key_len inside the last live word stay clear
+                assert all(((int(row[k >> 5]) >> (k & 31)) & 1) == 0 for k in range(keys, n_live * 32))
+                tail = row[n_live:]
+            else:
+                tail = row  # rows past q_len are never written
+            for wi, w in enumerate(tail):
+                absolute = (n_live + wi) if q < q_lens[b] else wi
+                if reserve and q == 0 and absolute == shape[2] - 1:
+                    assert np.uint32(w) == np.uint32(ks[b]).astype(np.uint32)
+                else:
+                    assert w == workloads.SENTINEL_U32, (b, q, absolute)
+
+
+def test_mask_build_rejects_wrong_shape():
+    topk = np.zeros((1, 2), np.int32)
+    bad = np.zeros((1, 128, 4), dtype=np.uint32)  # 129 keys need 8 words
+    with pytest.raises(ValueError):
+        oracle.build_topk_mask(topk, np.array([0, 1], np.int32), 1, 1, 129, out=bad)
+
+
+# ---------------------------------------------------------------- attention
+
+def _sdpa_reference(inp):
+    """torch SDPA (float64, CPU) over the gathered rows of each token, the sink
+    realised as one more key with additive logit attn_sink[h] and a zero value
+    row, invalid slots masked with -inf."""
+    q = inp.q.double()
+    kv = inp.kv.double()
+    idx = inp.topk_idxs.long()
+    B, S, H, D = q.shape
+    T, K = kv.shape[1], idx.shape[-1]
+    out = torch.zeros(B, S, H, D, dtype=torch.float64)
+    for b in range(B):
+        for s in range(S):
+            sel = idx[b, s]
+            valid = (sel >= 0) & (sel < T)
+            rows = torch.zeros(K + 1, D, dtype=torch.float64)
+            rows[:K][valid] = kv[b, sel[valid]]
+            bias = torch.full((H, 1, K + 1), 0.0, dtype=torch.float64)
+            bias[:, 0, :K][:, ~valid] = -math.inf
+            bias[:, 0, K] = inp.attn_sink.double()
+            qh = q[b, s].unsqueeze(1)  # [H,1,D]
+            k = rows.unsqueeze(0).expand(H, K + 1, D)
+            v = k.clone()
+            v[:, K] = 0.0
+            out[b, s] = torch.nn.functional.scaled_dot_product_attention(
+                qh, k, v, attn_mask=bias, scale=inp.softmax_scale)[:, 0]
+    return out.numpy()
+
+
+def _run(inp, **kw):
+    return oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, **kw)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_attn_matches_library_sdpa_with_sink(seed):
+    inp = workloads.random_attn(2, 3, 4, 32, 40, 12, p_invalid=0.2, seed=seed, distinct=(seed != 2))
+    # seed 2 draws indices with repeats: a repeated slot counts once per occurrence
+    got = _run(inp)
+    want = _sdpa_reference(inp)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+
+
+def test_attn_uses_own_batch_kv_and_out_of_range_is_invalid():
+    inp = workloads.random_attn(3, 2, 2, 16, 20, 8, p_invalid=0.0, seed=5)
+    inp.topk_idxs[0, 0, 0] = 20      # == T: out of range, treated like -1
+    inp.topk_idxs[1, 1, 3] = 1 << 30
+    inp.topk_idxs[2, 0, 5] = -7
+    np.testing.assert_allclose(_run(inp), _sdpa_reference(inp), rtol=1e-10, atol=1e-12)
+
+
+def test_attn_k1_closed_form():
+    # one valid slot: weights are [sigmoid(x - sink), 1 - that]; o = w * row
+    D, H = 8, 3
+    q = _bf(torch.tensor([0.5, -1.0, 2.0, 0.25, 1.5, -0.75, 0.0, 1.0]).repeat(H, 1)).reshape(1, 1, H, D)
+    row = _bf(torch.tensor([1.0, 0.5, -0.5, 2.0, -1.0, 0.25, 3.0, -2.0]))
+    kv = row.reshape(1, 1, D)
+    sink = torch.tensor([-1.0, 0.0, 2.5], dtype=torch.float32)
+    idx = torch.zeros(1, 1, 1, dtype=torch.int32)
+    scale = 0.375
+    o = oracle.sparse_attn(q, kv, sink, idx, scale)
+    x = scale * float((q[0, 0, 0].double() * row.double()).sum())
+    for h in range(H):
+        w = 1.0 / (1.0 + math.exp(-(x - float(sink[h]))))
+        np.testing.assert_allclose(o[0, 0, h], w * row.double().numpy(), rtol=1e-14, atol=1e-15)
+
+
+def test_attn_identical_rows_closed_form():
+    # n valid copies of one row v: o = n e^x / (n e^x + e^sink) * v
+    D, H, K, n = 16, 2, 10, 7
+    g = torch.Generator().manual_seed(3)
+    v = _bf(torch.randn(D, generator=g))
+    q = _bf(torch.randn(1, 1, H, D, generator=g))
+    kv = v.reshape(1, 1, D).repeat(1, 5, 1)
+    idx = torch.full((1, 1, K), -1, dtype=torch.int32)
+    idx[0, 0, [0, 2, 3, 5, 6, 8, 9]] = torch.tensor([0, 1, 2, 3, 4, 0, 1], dtype=torch.int32)
+    sink = torch.tensor([0.3, -2.0], dtype=torch.float32)
+    scale = D ** -0.5
+    o = oracle.sparse_attn(q, kv, sink, idx, scale)
+    for h in range(H):
+        x = scale * float((q[0, 0, h].double() * v.double()).sum())
+        w = n * math.exp(x) / (n * math.exp(x) + math.exp(float(sink[h])))
+        np.testing.assert_allclose(o[0, 0, h], w * v.double().numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_attn_zero_query_gives_uniform_weights():
+    inp = workloads.random_attn(1, 1, 2, 8, 30, 9, p_invalid=0.3, seed=11)
+    inp.q.zero_()
+    sel = inp.topk_idxs[0, 0]
+    valid = sel[(sel >= 0)].long()
+    rows = inp.kv[0, valid].double().sum(0).numpy()
+    o = _run(inp)
+    for h in range(2):
+        want = rows / (len(valid) + math.exp(float(inp.attn_sink[h])))
+        np.testing.assert_allclose(o[0, 0, h], want, rtol=1e-13, atol=1e-15)
+
+
+def test_attn_all_invalid_gives_zero():
+    inp = workloads.random_attn(1, 2, 3, 8, 10, 5, p_invalid=0.0, seed=2)
+    inp.topk_idxs.fill_(-1)
+    assert np.all(_run(inp) == 0.0)
+    inp.attn_sink[:] = -math.inf  # no sink and no key: zero, not NaN
+    assert np.all(_run(inp) == 0.0)
+
+
+def test_attn_sink_limits():
+    inp = workloads.random_attn(1, 2, 3, 8, 10, 5, p_invalid=0.2, seed=4)
+    inp.attn_sink[:] = math.inf
+    assert np.all(_run(inp) == 0.0)
+    inp.attn_sink[:] = -math.inf
+    got = _run(inp)
+    # sink = -inf is plain softmax attention over the valid slots
+    want = _sdpa_reference(inp)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+    # and the sink lowers every weight when finite (sum w_j < 1)
+    inp.attn_sink[:] = 0.0
+    assert not np.allclose(_run(inp), got)
+
+
+def test_attn_invariant_to_slot_order_and_invalid_position():
+    inp = workloads.random_attn(1, 3, 4, 16, 64, 24, p_invalid=0.25, seed=9)
+    base = _run(inp)
+    perm = torch.randperm(24, generator=torch.Generator().manual_seed(1))
+    inp2 = workloads.AttnInputs(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs[..., perm].contiguous(),
+                                inp.softmax_scale)
+    np.testing.assert_allclose(_run(inp2), base, rtol=1e-12, atol=1e-14)
+    # padding with extra -1 slots changes nothing
+    pad = torch.full((1, 3, 40), -1, dtype=torch.int32)
+    inp3 = workloads.AttnInputs(inp.q, inp.kv, inp.attn_sink, torch.cat([pad, inp.topk_idxs], -1),
+                                inp.softmax_scale)
+    np.testing.assert_allclose(_run(inp3), base, rtol=1e-12, atol=1e-14)
+
+
+def test_attn_token_subset_matches_full():
+    inp = workloads.random_attn(2, 5, 2, 16, 32, 8, seed=12)
+    full = _run(inp)
+    tok = np.array([7, 0, 3], dtype=np.int64)
+    sub = _run(inp, tokens=tok)
+    for i, t in enumerate(tok):
+        np.testing.assert_array_equal(sub[i], full[t // 5, t % 5])
+
+
+# ---------------------------------------------------------------- mask <-> attention
+
+def test_masked_dense_equals_sparse_with_oracle_mask():
+    inp = workloads.random_attn(2, 4, 3, 16, 70, 20, p_invalid=0.15, seed=21)
+    B, S = 2, 4
+    cu = np.arange(0, B * S + 1, S, dtype=np.int32)
+    topk = inp.topk_idxs.reshape(B * S, -1).numpy()
+    m = oracle.build_topk_mask(topk, cu, B, S, 70)
+    dense = oracle.masked_dense_attn(inp.q, inp.kv, inp.attn_sink, m, inp.softmax_scale)
+    np.testing.assert_allclose(dense, _run(inp), rtol=1e-12, atol=1e-14)
+
+
+def test_masked_dense_key_offset_reads_absolute_positions():
+    # a context chunk kv[start:] with a mask over absolute key positions: the
+    # consumer adds key_start before the bit test
+    inp = workloads.random_attn(1, 2, 2, 8, 50, 12, p_invalid=0.0, seed=31)
+    start = 17
+    topk = inp.topk_idxs.reshape(2, -1).numpy()
+    m = oracle.build_topk_mask(topk, np.array([0, 2], np.int32), 1, 2, 50)
+    chunk = inp.kv[:, start:].contiguous()
+    got = oracle.masked_dense_attn(inp.q, chunk, inp.attn_sink, m, inp.softmax_scale, key_offset=[start])
+    shifted = torch.where(inp.topk_idxs >= start, inp.topk_idxs - start, torch.full_like(inp.topk_idxs, -1))
+    want = oracle.sparse_attn(inp.q, chunk, inp.attn_sink, shifted, inp.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_tiny_workload_shape_and_structure():
+    inp = workloads.tiny()
+    assert inp.shape == dict(B=1, S=4, H=8, D=64, T=256, K=64)
+    idx = inp.topk_idxs
+    for s in range(4):
+        v = idx[0, s][idx[0, s] >= 0]
+        assert len(set(v.tolist())) == len(v)
+    assert 0 < int((idx < 0).sum()) < 64
+    assert inp.softmax_scale == 0.125
