@@ -1,0 +1,373 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse_attn hot path on one or more GB300s (one process
+per GPU, weak scaling: every rank runs its own batch, no collective on the
+data path).
+
+A step is one sparse_attn forward over the V4 ratio-4 decode batch (B=32,
+S=1, H=128, D=512, T=16512, K=1152, ragged contexts), inputs resident in HBM,
+L2 flushed between steps (a 256 MB write outside the timed events).  Rank 0
+prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse_attn query-tokens/s & TFLOP/s (% roofline); mask-build GB/s; vs CPU oracle"
+UNIT = "query-tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 9 for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+def _source_hash(paths):
+    h = hashlib.sha1()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def _profile_traffic(kernel_tag: str, src_hash: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/*.md line
+    'traffic_bytes_per_launch: <n> source_hash: <h> kernel: <tag>'); None if
+    absent or if the kernel source changed since the capture."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            if line.startswith("traffic_bytes_per_launch:") and f"kernel: {kernel_tag}" in line:
+                parts = line.split()
+                try:
+                    n = float(parts[1])
+                    h = parts[parts.index("source_hash:") + 1]
+                except (ValueError, IndexError):
+                    continue
+                if h == src_hash:
+                    return n
+    return None
+
+
+KERNEL_SOURCES = ["deepseek_top_sparse_gb300/csrc/attn_tc.cu", "deepseek_top_sparse_gb300/csrc/attn_tc_kernel.cuh"]
+
+
+def _attn_kernel_sources():
+    return [p for p in KERNEL_SOURCES + ["deepseek_top_sparse_gb300/csrc/attn_simt.cu"]
+            if os.path.exists(os.path.join(ROOT, p))]
+
+
+def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None):
+    """Time the oracle (as it stands) on whole tokens of the workload until
+    about budget_s of wall time; returns (tokens/s, tokens, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+
+    B, S = inp.q.shape[:2]
+    ntok = B * S
+    threads = os.cpu_count() or 1
+    done, elapsed, start_tok = 0, 0.0, 0
+    chunk = max(1, min(ntok, threads, max_tokens or ntok))
+    while done == 0 or (elapsed < budget_s and (max_tokens is None or done < max_tokens)):
+        tok = np.arange(start_tok, start_tok + chunk, dtype=np.int64) % ntok
+        t0 = time.perf_counter()
+        oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, tokens=tok,
+                           nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        done += chunk
+        start_tok += chunk
+    return done / elapsed, done, elapsed, threads
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from deepseek_top_sparse_gb300 import workloads
+
+    inp = workloads.v4_ratio4_decode()
+    per_step_tokens = min(32, os.cpu_count() or 1)  # bounded sample per step: one token per host core
+    for _ in range(args.warmup):
+        cpu_oracle_time(inp, 0.0, max_tokens=per_step_tokens)
+    times = []
+    threads = os.cpu_count() or 1
+    for _ in range(args.steps):
+        _, n, sec, threads = cpu_oracle_time(inp, 0.0, max_tokens=per_step_tokens)
+        times.append((n, sec))
+    tot_tok = sum(n for n, _ in times)
+    tot_s = sum(s for _, s in times)
+    value = tot_tok / tot_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": inp.name, "sample": f"{per_step_tokens} query tokens per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{per_step_tokens} of the batch's 32 query tokens per step, all 128 heads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from deepseek_top_sparse_gb300 import binding, workloads
+
+    dev = torch.device("cuda", local)
+    inp_cpu = workloads.v4_ratio4_decode(seed=1001 + rank)
+    inp = inp_cpu.to(dev)
+    B, S, H, D = inp.q.shape
+    T, K = inp.kv.shape[1], inp.topk_idxs.shape[-1]
+    tokens = B * S
+    valid = workloads.count_valid(inp_cpu.topk_idxs, T)
+    flops = 4.0 * H * D * valid                   # QK^T and P.V, valid slots only
+    gathered = float(valid) * D * 2               # bf16 kv rows gathered
+    compulsory = gathered + 2 * inp.q.numel() * 2 + inp.topk_idxs.numel() * 4 + H * 4
+    out = torch.empty_like(inp.q)
+    ns = binding.sa_sparse_attn_num_splits(B, S, H, D, K)
+    wsbuf = binding.workspace_for(B, S, H, D, K, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + (1 if ns > 1 else 0)
+
+    def step():
+        binding.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, out=out,
+                            workspace=wsbuf)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if binding.sa_device_error(True) != 0:
+        raise RuntimeError("kernel reported a device-side failure during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                       # cold L2, outside the events
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    per = [a.elapsed_time(b) for a, b in evs]   # ms
+    ms = sum(per) / len(per)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert binding.sa_device_error(True) == 0
+
+    # ---- end to end through the public API: pinned host q / indices in, o out
+    q_h = inp_cpu.q.pin_memory()
+    idx_h = inp_cpu.topk_idxs.pin_memory()
+    o_h = torch.empty(inp_cpu.q.shape, dtype=torch.bfloat16).pin_memory()
+    q_d = torch.empty_like(inp.q)
+    idx_d = torch.empty_like(inp.topk_idxs)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        binding.sparse_attn(q_d, inp.kv, inp.attn_sink, idx_d, inp.softmax_scale, out=out, workspace=wsbuf)
+        o_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = sum(e_ms) / len(e_ms)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- mask build on the mask workload (B=4, Q=2048, 8193 keys, K=2048)
+    mask_obj = None
+    if rank == 0 and not args.no_mask:
+        mi = workloads.topk_mask().to(dev)
+        shape = binding.topk_mask_shape(mi.batch, mi.max_q_len, mi.max_key_len, True)
+        mbuf = torch.zeros(shape, dtype=torch.int32, device=dev)
+
+        def mstep():
+            binding.build_topk_mask(mi.topk, mi.cu_q_lens, mi.max_q_len, mi.max_key_len, mi.key_starts, out=mbuf)
+
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            mstep()
+        torch.cuda.synchronize()
+        m_ms = []
+        for _ in range(max(args.steps, 10)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            mstep()
+            b.record(stream)
+            b.synchronize()
+            m_ms.append(a.elapsed_time(b))
+        mms = sum(m_ms) / len(m_ms)
+        live_words = (mi.max_key_len + 31) // 32
+        m_bytes = mi.topk.numel() * 4 + mi.batch * mi.max_q_len * live_words * 4
+        hbm, _, _, src = _peaks()
+        m_gbs = m_bytes / (mms * 1e-3) / 1e9
+        mask_obj = {"workload": mi.name, "us_per_call": mms * 1e3, "gbs": m_gbs,
+                    "algorithmic_bytes": m_bytes,
+                    "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": hbm, "unit": "GB/s",
+                                 "frac": m_gbs / hbm, "peak_source": src}}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    hbm, tf_burst, _, src = _peaks()
+    sec = ms * 1e-3
+    achieved_gbs = gathered / sec / 1e9
+    tflops = flops / sec / 1e12
+    roof_t = max(flops / (tf_burst * 1e12), gathered / (hbm * 1e9))
+    bound = "hbm" if gathered / (hbm * 1e9) >= flops / (tf_burst * 1e12) else "tensor"
+    ktag = "sparse_attn"
+    traffic = _profile_traffic(ktag, _source_hash(_attn_kernel_sources()))
+    cpu_v, cpu_n, cpu_s, cpu_threads = cpu_oracle_time(inp_cpu, args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": tokens * ws / sec, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": inp.name, "tokens_per_rank": tokens, "valid_slots": valid, "num_splits": ns,
+                   "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "inputs": "seeded N(0,1) bf16 q/kv, fp32 sink, ragged top-k indices (see DESIGN.md)"},
+        "tflops": tflops, "gathered_kv_gbs": achieved_gbs,
+        "roofline": {"bound": bound, "achieved": achieved_gbs if bound == "hbm" else tflops,
+                     "peak": hbm if bound == "hbm" else tf_burst, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": roof_t / sec, "traffic": traffic, "peak_source": src + " (burst)",
+                     "algorithmic_bytes": gathered, "compulsory_bytes": compulsory,
+                     "flops": flops, "kernel": ktag},
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
+                         "sample": f"{cpu_n} query tokens x 128 heads of the same workload, {cpu_s:.1f} s"},
+        "clocks": clk,
+        "e2e": {"value": tokens * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": inp.q.numel() * 2 + inp.topk_idxs.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2,
+                "note": "kv cache resident in HBM; q and indices copied in, o copied out each step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_loop": wall,
+        "mask_build": mask_obj,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-mask", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -7,14 +7,14 @@ The compute lives in a C-ABI shared library (``libsa.so``, built from
 it; ``workloads`` only generates seeded synthetic inputs.
 """
 
-__all__ = ["binding", "workloads"]
+import importlib
+
+__all__ = ["binding", "workloads", "sparse_attn", "build_topk_mask", "topk_mask_shape"]
 
 
 def __getattr__(name):
     # Lazy: importing the package (e.g. for `workloads`) must not require the
     # CUDA library; calling into it does, and fails loudly when it is missing.
-    if name in ("sparse_attn", "build_topk_mask", "topk_mask_shape", "binding"):
-        from . import binding
-
-        return binding if name == "binding" else getattr(binding, name)
+    if name in ("sparse_attn", "build_topk_mask", "topk_mask_shape"):
+        return getattr(importlib.import_module(__name__ + ".binding"), name)
     raise AttributeError(name)

@@ -1,0 +1,200 @@
+"""Thin ctypes binding of libsa.so (include/sa.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libsa.so.  torch supplies device memory and streams.  There is no
+fallback: if the library cannot be loaded, or a call returns an error status,
+a ``RuntimeError`` is raised.
+
+The C entry points are exposed under their C names (``sa_sparse_attn_fwd``,
+``sa_topk_mask_shape``, ``sa_build_topk_mask`` ...) taking raw pointers and
+sizes, and wrapped by tensor-level helpers ``sparse_attn``,
+``topk_mask_shape`` and ``build_topk_mask``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SA_OK = 0
+_STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_ALIGNMENT",
+           4: "SA_ERR_WORKSPACE", 5: "SA_ERR_UNSUPPORTED_DEVICE", 6: "SA_ERR_CUDA"}
+
+EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
+           "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
+           "sa_build_topk_mask", "sa_device_error")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {_STATUS.get(code, code)}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libsa.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing; run deepseek_top_sparse_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.sa_status_string.argtypes = [i32]
+        lib.sa_status_string.restype = ctypes.c_char_p
+        lib.sa_sparse_attn_num_splits.argtypes = [i64] * 5
+        lib.sa_sparse_attn_num_splits.restype = i32
+        lib.sa_sparse_attn_workspace_size.argtypes = [i64] * 5 + [i32]
+        lib.sa_sparse_attn_workspace_size.restype = sz
+        lib.sa_sparse_attn_fwd.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [p, sz, p]
+        lib.sa_sparse_attn_fwd.restype = i32
+        lib.sa_sparse_attn_fwd_splits.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p, sz, p]
+        lib.sa_sparse_attn_fwd_splits.restype = i32
+        lib.sa_topk_mask_shape.argtypes = [i64, i64, i64, i32, p]
+        lib.sa_topk_mask_shape.restype = i32
+        lib.sa_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p, p]
+        lib.sa_build_topk_mask.restype = i32
+        lib.sa_device_error.argtypes = [i32]
+        lib.sa_device_error.restype = i32
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ C names
+
+def sa_status_string(code: int) -> str:
+    return load().sa_status_string(int(code)).decode()
+
+
+def sa_sparse_attn_num_splits(B, S, H, D, K) -> int:
+    return int(load().sa_sparse_attn_num_splits(B, S, H, D, K))
+
+
+def sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits=0) -> int:
+    return int(load().sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits))
+
+
+def sa_sparse_attn_fwd(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
+                       workspace, workspace_bytes, stream) -> int:
+    return int(load().sa_sparse_attn_fwd(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
+                                          workspace, workspace_bytes, stream))
+
+
+def sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
+                              num_splits, workspace, workspace_bytes, stream) -> int:
+    return int(load().sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T,
+                                                 K, num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_topk_mask_shape(batch, max_query_len, max_key_len, reserve_key_starts_word) -> tuple[int, int, int]:
+    out = (ctypes.c_int64 * 3)()
+    rc = load().sa_topk_mask_shape(batch, max_query_len, max_key_len, int(bool(reserve_key_starts_word)), out)
+    if rc != SA_OK:
+        raise SAError("sa_topk_mask_shape", rc)
+    return int(out[0]), int(out[1]), int(out[2])
+
+
+def sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K, key_starts, mask,
+                       mask_shape, stream) -> int:
+    shp = (ctypes.c_int64 * 3)(*[int(v) for v in mask_shape])
+    return int(load().sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K, key_starts,
+                                         mask, shp, stream))
+
+
+def sa_device_error(clear: bool = True) -> int:
+    return int(load().sa_device_error(int(bool(clear))))
+
+
+# ------------------------------------------------------------------ tensor helpers
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _check(fn: str, rc: int):
+    if rc != SA_OK:
+        raise SAError(fn, rc)
+
+
+def workspace_for(B, S, H, D, K, num_splits=0, device=None) -> torch.Tensor | None:
+    n = sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def sparse_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk_idxs: torch.Tensor,
+                softmax_scale: float, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                num_splits: int = 0, stream=None) -> torch.Tensor:
+    """o = sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale) on the GPU.
+
+    q bf16 [B,S,H,D], kv bf16 [B,T,D], attn_sink fp32 [H], topk_idxs int32
+    [B,S,K] (-1 = invalid), all contiguous on one CUDA device."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("kv", kv, torch.bfloat16),
+                        ("attn_sink", attn_sink, torch.float32), ("topk_idxs", topk_idxs, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    B, S, H, D = q.shape
+    T = kv.shape[1]
+    K = topk_idxs.shape[-1]
+    if kv.shape != (B, T, D) or topk_idxs.shape != (B, S, K) or attn_sink.shape != (H,):
+        raise ValueError("shape mismatch among q, kv, attn_sink, topk_idxs")
+    if out is None:
+        out = torch.empty_like(q)
+    need = sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = sa_sparse_attn_fwd_splits(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(topk_idxs), float(softmax_scale),
+                                   _dptr(out), B, S, H, D, T, K, int(num_splits), _dptr(workspace), ws_bytes,
+                                   _stream_ptr(stream))
+    _check("sa_sparse_attn_fwd_splits", rc)
+    return out
+
+
+def topk_mask_shape(batch: int, max_query_len: int, max_key_len: int,
+                    reserve_key_starts_word: bool = False) -> tuple[int, int, int]:
+    return sa_topk_mask_shape(batch, max_query_len, max_key_len, reserve_key_starts_word)
+
+
+def build_topk_mask(topk: torch.Tensor, cu_q_lens: torch.Tensor, max_q_len: int, max_key_len: int,
+                    key_starts: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """uint32 mask [B, rows, words] (stored as int32 storage when ``out`` is
+    int32, as the pages' test allocates it).  Words the build does not write
+    keep the contents of ``out``."""
+    B = cu_q_lens.numel() - 1
+    shape = topk_mask_shape(B, max_q_len, max_key_len, key_starts is not None)
+    if out is None:
+        out = torch.zeros(shape, dtype=torch.int32, device=topk.device)
+    if tuple(out.shape) != shape or out.element_size() != 4 or not out.is_contiguous():
+        raise ValueError(f"mask buffer must be a contiguous 32-bit tensor of shape {shape}")
+    if topk.dtype != torch.int32 or cu_q_lens.dtype != torch.int32:
+        raise ValueError("topk and cu_q_lens must be int32")
+    tk = topk if topk.dim() == 2 else topk.reshape(-1, topk.shape[-1] if topk.dim() else 1)
+    rc = sa_build_topk_mask(_dptr(tk), tk.shape[0], _dptr(cu_q_lens), B, max_q_len, max_key_len, tk.shape[1],
+                            _dptr(key_starts), _dptr(out), shape, _stream_ptr(stream))
+    _check("sa_build_topk_mask", rc)
+    return out

@@ -1,0 +1,205 @@
+// C ABI entry points (include/sa.h): host-side validation, planning and
+// launch.  Nothing here computes the method; every step of it runs in the
+// kernels of the other translation units.
+#include <cmath>
+#include <mutex>
+
+#include "sa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int sms = 0;
+    int major = 0, minor = 0;
+    bool ok = false;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+sa_status current_device(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SA_ERR_CUDA;
+    std::call_once(g_dev_once[dev], [dev] {
+        cudaDeviceProp p{};
+        if (cudaGetDeviceProperties(&p, dev) == cudaSuccess) {
+            g_dev[dev].sms = p.multiProcessorCount;
+            g_dev[dev].major = p.major;
+            g_dev[dev].minor = p.minor;
+            g_dev[dev].ok = true;
+        }
+    });
+    if (!g_dev[dev].ok) return SA_ERR_CUDA;
+    *out = g_dev[dev];
+    // The kernels are built for sm_103a only (tcgen05, TMA gather4).
+    if (!(out->major == 10 && out->minor == 3)) return SA_ERR_UNSUPPORTED_DEVICE;
+    return SA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool attn_sizes_ok(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K) {
+    if (B < 0 || S < 0 || H < 1 || H > 128 || K < 1) return false;
+    if (!(D == 64 || D == 128 || D == 256 || D == 512)) return false;
+    return true;
+}
+
+// Split plan: a function of the sizes and the SM count only (never of index
+// values), so a captured graph keeps a fixed grid.
+int plan_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K, int num_sms) {
+    (void)H;
+    (void)D;
+    (void)B;
+    (void)S;
+    (void)K;
+    (void)num_sms;
+    return 1;
+}
+
+size_t workspace_bytes_for(int64_t B, int64_t S, int64_t H, int64_t D, int splits) {
+    if (splits <= 1) return 0;
+    const size_t tok = size_t(B) * size_t(S);
+    size_t o_bytes = tok * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
+    o_bytes = (o_bytes + 255) / 256 * 256;
+    return o_bytes + tok * size_t(splits) * size_t(H) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sa_status_string(sa_status s) {
+    switch (s) {
+        case SA_OK: return "SA_OK";
+        case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+        case SA_ERR_SHAPE: return "SA_ERR_SHAPE";
+        case SA_ERR_ALIGNMENT: return "SA_ERR_ALIGNMENT";
+        case SA_ERR_WORKSPACE: return "SA_ERR_WORKSPACE";
+        case SA_ERR_UNSUPPORTED_DEVICE: return "SA_ERR_UNSUPPORTED_DEVICE";
+        case SA_ERR_CUDA: return "SA_ERR_CUDA";
+    }
+    return "SA_ERR_UNKNOWN";
+}
+
+int sa_sparse_attn_num_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K) {
+    if (!attn_sizes_ok(B, S, H, D, K)) return 0;
+    DeviceInfo dev;
+    const sa_status st = current_device(&dev);
+    if (st != SA_OK) return 0;
+    return plan_splits(B, S, H, D, K, dev.sms);
+}
+
+size_t sa_sparse_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K,
+                                     int num_splits) {
+    if (!attn_sizes_ok(B, S, H, D, K)) return 0;
+    int splits = num_splits;
+    if (splits <= 0) splits = sa_sparse_attn_num_splits(B, S, H, D, K);
+    if (splits > cdiv(K, 64)) splits = int(cdiv(K, 64));
+    return workspace_bytes_for(B, S, H, D, splits);
+}
+
+sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
+                                    const int32_t *topk_idxs, float softmax_scale, void *o,
+                                    int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                    int64_t K, int num_splits, void *workspace,
+                                    size_t workspace_bytes, sa_stream_t stream) {
+    if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || K < 0) return SA_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
+    if (num_splits > 64) return SA_ERR_INVALID_ARG;
+    if (!attn_sizes_ok(B, S, H, D, K) || T < 1) return SA_ERR_SHAPE;
+    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S == 0) return SA_OK;
+    if (!q || !kv || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return SA_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3))
+        return SA_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const sa_status st = current_device(&dev);
+    if (st != SA_OK) return st;
+
+    int splits = num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms);
+    if (splits > cdiv(K, 64)) splits = int(cdiv(K, 64));
+    if (splits < 1) splits = 1;
+    const size_t need = workspace_bytes_for(B, S, H, D, splits);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
+
+    sa::AttnArgs a{};
+    a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = topk_idxs; a.scale = softmax_scale; a.o = o;
+    a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
+    a.num_splits = splits;
+    if (splits > 1) {
+        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
+        o_bytes = (o_bytes + 255) / 256 * 256;
+        a.ws_o = static_cast<float *>(workspace);
+        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (sa::launch_sparse_attn(a, dev.sms, s) != cudaSuccess) return SA_ERR_CUDA;
+    if (splits > 1 && sa::launch_attn_combine(a, s) != cudaSuccess) return SA_ERR_CUDA;
+    return SA_OK;
+}
+
+sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_sink,
+                             const int32_t *topk_idxs, float softmax_scale, void *o, int64_t B,
+                             int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
+                             void *workspace, size_t workspace_bytes, sa_stream_t stream) {
+    return sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T,
+                                     K, 0, workspace, workspace_bytes, stream);
+}
+
+sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key_len,
+                             int reserve_key_starts_word, int64_t out_shape[3]) {
+    if (out_shape == nullptr || batch < 0 || max_query_len < 0 || max_key_len < 0)
+        return SA_ERR_INVALID_ARG;
+    const int64_t tile_m = max_query_len <= 128 ? 128 : 256;
+    out_shape[0] = batch;
+    out_shape[1] = cdiv(max_query_len, tile_m) * tile_m;
+    out_shape[2] = cdiv(cdiv(max_key_len, 32) + (reserve_key_starts_word ? 1 : 0), 4) * 4;
+    return SA_OK;
+}
+
+sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                             int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
+                             const int32_t *key_starts, uint32_t *mask,
+                             const int64_t mask_shape[3], sa_stream_t stream) {
+    if (mask_shape == nullptr || B < 0 || max_q_len < 0 || max_key_len < 0 || K < 0 || topk_rows < 0)
+        return SA_ERR_INVALID_ARG;
+    if (max_key_len > INT32_MAX) return SA_ERR_SHAPE;
+    int64_t want[3];
+    sa_status st = sa_topk_mask_shape(B, max_q_len, max_key_len, key_starts != nullptr, want);
+    if (st != SA_OK) return st;
+    if (mask_shape[0] != want[0] || mask_shape[1] != want[1] || mask_shape[2] != want[2])
+        return SA_ERR_SHAPE;
+    const bool any_rows = B * max_q_len > 0 && topk_rows > 0;
+    const bool any_ks = key_starts != nullptr && want[1] > 0 && B > 0;
+    if (!any_rows && !any_ks) return SA_OK;
+    if (mask == nullptr || cu_q_lens == nullptr) return SA_ERR_INVALID_ARG;
+    if (any_rows && K > 0 && topk == nullptr) return SA_ERR_INVALID_ARG;
+    if (!aligned16(mask)) return SA_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(cu_q_lens) & 3) || (reinterpret_cast<uintptr_t>(topk) & 3))
+        return SA_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != SA_OK) return st;
+    sa::MaskArgs a{};
+    a.topk = topk; a.topk_rows = topk_rows; a.cu_q_lens = cu_q_lens;
+    a.B = B; a.max_q_len = max_q_len; a.max_key_len = max_key_len; a.K = K;
+    a.key_starts = key_starts; a.mask = mask; a.rows = want[1]; a.words = want[2];
+    if (!any_rows) a.max_q_len = 0;  // only the reserved words remain to write
+    if (sa::launch_build_topk_mask(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return SA_OK;
+}
+
+int sa_device_error(int clear) {
+    int v = 0;
+    if (sa::read_device_error(&v, clear != 0) != cudaSuccess) return -1;
+    return v;
+}
+
+}  // extern "C"

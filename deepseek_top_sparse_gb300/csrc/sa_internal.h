@@ -1,0 +1,55 @@
+// Internal declarations shared by the translation units of libsa.so.
+// Not part of the public ABI (see include/sa.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sa.h"
+
+namespace sa {
+
+// Codes written to the device error word (see sa_device_error in sa.h).
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrWaitTimeout = 1,   // an mbarrier wait ran past its iteration limit
+    kErrBadPlan = 2,       // a kernel received a launch shape it cannot handle
+};
+
+// The device error word lives in attn_tc.cu; every kernel that can fail
+// records into it with atomicCAS(0 -> code) so the first failure sticks.
+cudaError_t read_device_error(int *value, bool clear);
+
+// ---- launchers (host side, enqueue only; arguments already validated) ----
+
+struct AttnArgs {
+    const void *q;          // bf16 [B,S,H,D]
+    const void *kv;         // bf16 [B,T,D]
+    const float *sink;      // [H]
+    const int32_t *idx;     // [B,S,K]
+    float scale;
+    void *o;                // bf16 [B,S,H,D]
+    int64_t B, S, H, D, T, K;
+    int num_splits;         // >= 1
+    float *ws_o;            // fp32 [tokens, splits, H, D]   (splits > 1)
+    float *ws_lse;          // fp32 [tokens, splits, H]      (splits > 1)
+};
+
+// Slots handled by one split (a multiple of the 64-row tile).
+int64_t split_slots(int64_t K, int num_splits);
+
+cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream);
+
+struct MaskArgs {
+    const int32_t *topk;
+    int64_t topk_rows;
+    const int32_t *cu_q_lens;
+    int64_t B, max_q_len, max_key_len, K;
+    const int32_t *key_starts;
+    uint32_t *mask;
+    int64_t rows, words;    // mask shape [B, rows, words]
+};
+cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t stream);
+
+}  // namespace sa

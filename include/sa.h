@@ -1,0 +1,158 @@
+/*
+ * sa.h -- C ABI of the GB300 (sm_103a) top-k sparse attention library.
+ *
+ * Two operations, both from the DeepSeek V4 sparse-attention path:
+ *
+ *  1. o = sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale)
+ *     "DeepSeek V4 源码剖析, 第5章 sparse_attn 与 FlashMLA": §5.1 (argument
+ *     shapes and dtypes, -1 marks an invalid slot, softmax_scale =
+ *     head_dim^-0.5), §5.2 (per query token and head: gather K indexed kv
+ *     rows, logits = scale * q.k, -inf on invalid slots, append the head's
+ *     sink logit, softmax, weighted sum of the gathered rows -- the sink's
+ *     weight is dropped; V is the same row as K), §5.5 (online softmax over
+ *     64-row tiles, sink added once to the denominator, the log-sum-exp form
+ *     of the sink for split-KV combine).
+ *
+ *  2. The bit-packed top-k mask: vLLM PR 52217 page ("Sparse MLA mask
+ *     向量化 128-bit 加载", `_topk_mask_shape`, `_build_topk_mask`, the two
+ *     alignment tests) and vLLM PR 48770 page (masked MHA for sparse-MLA
+ *     prefill: `dense_mask_mod` reads bit kv&31 of word kv>>5, LSB first;
+ *     `offset_dense_mask_mod` reads key_start from the last word of row 0).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major (C order), in DEVICE memory of the current
+ *     CUDA device unless stated otherwise.  The caller owns every buffer,
+ *     workspace included; the library allocates no device memory and keeps no
+ *     per-call state.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  A call returns once its kernels are enqueued.
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     error nothing is launched and no output byte is written.
+ *   - Index VALUES are data, not arguments: an index outside [0, T) (or
+ *     [0, max_key_len) for the mask) is treated as an invalid slot and never
+ *     dereferenced.
+ *   - No entry point throws or aborts.
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers (same underlying type). */
+typedef struct CUstream_st *sa_stream_t;
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, non-finite scale */
+    SA_ERR_SHAPE = 2,              /* a size combination the kernels do not support */
+    SA_ERR_ALIGNMENT = 3,          /* a tensor that must start on 16 bytes does not */
+    SA_ERR_WORKSPACE = 4,          /* workspace smaller than the size query returned */
+    SA_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
+    SA_ERR_CUDA = 6                /* a CUDA runtime call or launch failed */
+} sa_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *sa_status_string(sa_status status);
+
+/* ------------------------------------------------------------------------ */
+/* sparse_attn                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Number of KV splits the library picks for this problem on the current
+ * device (1 = no split).  Depends only on the sizes and the device's SM
+ * count, never on index values, so a captured CUDA graph keeps its grid.
+ * Returns 0 on invalid sizes. */
+int sa_sparse_attn_num_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K);
+
+/* Workspace bytes sa_sparse_attn_fwd_splits needs for `num_splits` splits
+ * (num_splits <= 0 means the library's choice, as above).  Holds one float32
+ * partial output [B*S, splits, H, D] and one float32 log-sum-exp
+ * [B*S, splits, H]; 0 when no split is made. */
+size_t sa_sparse_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K,
+                                     int num_splits);
+
+/* o[b,s,h,:] = sum_j w_j * kv[b, topk_idxs[b,s,j], :] with
+ *   x_j = softmax_scale * <q[b,s,h,:], kv[b, topk_idxs[b,s,j], :]>  (slot j valid),
+ *   w   = softmax([x_0 .. x_{K-1}, attn_sink[h]])[0..K-1],
+ * invalid slots (index < 0 or >= T) contributing weight 0.  A token with no
+ * valid slot yields o = 0; attn_sink[h] = +inf yields o = 0; -inf is plain
+ * softmax attention.
+ *
+ *   q          bf16  [B,S,H,D]   16-byte aligned
+ *   kv         bf16  [B,T,D]     16-byte aligned (shared by all heads: MQA)
+ *   attn_sink  fp32  [H]
+ *   topk_idxs  int32 [B,S,K]
+ *   o          bf16  [B,S,H,D]   16-byte aligned, may not alias the inputs
+ *   workspace  >= sa_sparse_attn_workspace_size(B,S,H,D,K,0) bytes, 256-byte
+ *              aligned; may be NULL when that size is 0.
+ * Supported sizes: 1 <= H <= 128, D in {64, 128, 256, 512}, K >= 1,
+ * B*S >= 0 (0 launches nothing), T >= 1, B*T < 2^31.
+ * Computes in bf16 x bf16 -> fp32 on the tensor cores (tcgen05), softmax in
+ * fp32, probabilities rounded to bf16 before P.V, output rounded to bf16. */
+sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_sink,
+                             const int32_t *topk_idxs, float softmax_scale, void *o, int64_t B,
+                             int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
+                             void *workspace, size_t workspace_bytes, sa_stream_t stream);
+
+/* Same as sa_sparse_attn_fwd with an explicit split count (1..64; <= 0 picks
+ * as sa_sparse_attn_num_splits).  The result does not depend on the split
+ * count beyond fp32 rounding. */
+sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
+                                    const int32_t *topk_idxs, float softmax_scale, void *o,
+                                    int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                    int64_t K, int num_splits, void *workspace,
+                                    size_t workspace_bytes, sa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* bit-packed top-k mask                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Host-only.  out_shape = (batch, rows, words) with
+ *   tile_m = 128 if max_query_len <= 128 else 256,
+ *   rows   = ceil(max_query_len / tile_m) * tile_m,
+ *   words  = round_up(ceil(max_key_len / 32) + (reserve ? 1 : 0), 4),
+ * so every row is a whole number of 16-byte vectors (vLLM PR 52217 page,
+ * `_topk_mask_shape`).  SA_ERR_INVALID_ARG on negative sizes or NULL. */
+sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key_len,
+                             int reserve_key_starts_word, int64_t out_shape[3]);
+
+/* Scatters each request's top-k rows into the mask.
+ *   topk        int32 [topk_rows, K]: rows cu_q_lens[b] .. cu_q_lens[b+1]-1
+ *               belong to request b (query q of b is row cu_q_lens[b] + q)
+ *   cu_q_lens   int32 [B+1] prefix sums of the per-request query counts
+ *   key_starts  int32 [B] or NULL (NULL: no reserved word)
+ *   mask        uint32 [mask_shape], 16-byte aligned; mask_shape must equal
+ *               sa_topk_mask_shape(B, max_q_len, max_key_len, key_starts!=NULL)
+ *   mask_shape  HOST array of 3 int64.
+ * For each live row (b, q) with q < min(q_len_b, max_q_len) and source row
+ * < topk_rows: words [0, ceil(max_key_len/32)) are overwritten with the OR of
+ * (1u << (k & 31)) into word k >> 5 over the row's indices with
+ * 0 <= k < max_key_len.  If key_starts != NULL, word words-1 of row (b, 0)
+ * receives key_starts[b] (bit pattern) for every b.  Nothing else is written:
+ * padding words and rows past each request's query count keep their contents. */
+sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                             int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
+                             const int32_t *key_starts, uint32_t *mask,
+                             const int64_t mask_shape[3], sa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* diagnostics                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Every wait inside the kernels is bounded; a wait that runs out records a
+ * nonzero code in a device-side word and the kernel returns early (its output
+ * is then undefined).  This call synchronises the current device, returns
+ * that word (0 = no failure since the last clear) and clears it if `clear`.
+ * Returns -1 if the word cannot be read. */
+int sa_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

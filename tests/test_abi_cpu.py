@@ -1,0 +1,119 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function include/*.h declares, and the host-side paths (shape query, argument
+validation) behave as documented.  No kernel is launched here."""
+
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from deepseek_top_sparse_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(sa_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_three_operations():
+    names = _declared_functions()
+    for required in ("sa_sparse_attn_fwd", "sa_topk_mask_shape", "sa_build_topk_mask"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib_path = binding.load().__dict__.get("_name") or binding.library_path()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in _declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = binding.load()
+    for n in _declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_exposes_c_names():
+    for n in binding.EXPORTS:
+        assert callable(getattr(binding, n))
+    assert set(binding.EXPORTS) == set(_declared_functions())
+
+
+def test_status_strings():
+    assert binding.sa_status_string(0) == "SA_OK"
+    assert binding.sa_status_string(4) == "SA_ERR_WORKSPACE"
+    assert binding.sa_status_string(99) == "SA_ERR_UNKNOWN"
+
+
+def test_mask_shape_matches_oracle_and_golden():
+    for b, q, k, r in [(2, 129, 129, 0), (2, 129, 129, 1), (1, 1, 129, 0), (4, 2048, 8193, 1), (3, 128, 32, 0),
+                       (3, 129, 33, 0), (1, 257, 96, 1), (1, 513, 97, 1), (2, 0, 10, 0), (0, 5, 0, 1)]:
+        assert binding.sa_topk_mask_shape(b, q, k, r) == oracle.topk_mask_shape(b, q, k, bool(r))
+    assert binding.sa_topk_mask_shape(2, 129, 129, 0) == (2, 256, 8)
+
+
+def test_mask_shape_rejects_negative_and_null():
+    with pytest.raises(binding.SAError):
+        binding.sa_topk_mask_shape(-1, 1, 1, 0)
+    assert binding.load().sa_topk_mask_shape(1, 1, 1, 0, None) == 1  # SA_ERR_INVALID_ARG
+
+
+def _fwd(**over):
+    args = dict(q=16, kv=16, attn_sink=16, topk_idxs=16, softmax_scale=0.125, o=32, B=1, S=1, H=8, D=64, T=10,
+                K=4, num_splits=0, workspace=None, workspace_bytes=0, stream=None)
+    args.update(over)
+    return binding.sa_sparse_attn_fwd_splits(**args)
+
+
+def test_attn_validation_happens_before_any_device_work():
+    # none of these reach the device: sizes, pointers and alignment are checked first
+    assert _fwd(D=96) == 2                # SA_ERR_SHAPE: D not in {64,128,256,512}
+    assert _fwd(H=129) == 2               # more than 128 heads
+    assert _fwd(K=0) == 2
+    assert _fwd(T=0) == 2
+    assert _fwd(B=1 << 20, T=1 << 12) == 2  # B*T >= 2^31
+    assert _fwd(B=-1) == 1
+    assert _fwd(softmax_scale=float("nan")) == 1
+    assert _fwd(num_splits=65) == 1
+    assert _fwd(q=None) == 1
+    assert _fwd(o=None) == 1
+    assert _fwd(q=8) == 3                 # q not 16-byte aligned
+    assert _fwd(o=40) == 3
+    assert _fwd(topk_idxs=2) == 3
+    assert _fwd(B=0) == 0                 # nothing to do
+    assert _fwd(S=0) == 0
+
+
+def test_mask_validation_happens_before_any_device_work():
+    f = binding.sa_build_topk_mask
+    shape = binding.sa_topk_mask_shape(1, 1, 129, 0)
+    assert f(16, 1, 16, 1, 1, 129, 2, None, 16, (1, 128, 4), None) == 2   # wrong shape
+    no_reserve = binding.sa_topk_mask_shape(1, 1, 128, 0)                # (1, 128, 4)
+    assert f(16, 1, 16, 1, 1, 128, 2, 16, 16, no_reserve, None) == 2      # key_starts needs a reserved word
+    assert f(16, 1, 16, -1, 1, 129, 2, None, 16, shape, None) == 1
+    assert f(16, 1, None, 1, 1, 129, 2, None, 16, shape, None) == 1       # cu_q_lens NULL
+    assert f(16, 1, 16, 1, 1, 129, 2, None, 8, shape, None) == 3          # mask not 16-byte aligned
+    assert f(16, 0, 16, 1, 0, 129, 2, None, 16, binding.sa_topk_mask_shape(1, 0, 129, 0), None) == 0  # empty
+    assert binding.load().sa_build_topk_mask(16, 1, 16, 1, 1, 129, 2, None, 16, None, None) == 1
+
+
+def test_workspace_size_is_zero_without_splits_and_for_bad_sizes():
+    assert binding.sa_sparse_attn_workspace_size(1, 1, 8, 96, 4, 1) == 0
+    assert binding.sa_sparse_attn_workspace_size(1, 1, 8, 64, 4, 1) == 0
+    # explicit split counts size the partials: tokens*splits*H*D fp32 (256-aligned) + tokens*splits*H fp32
+    n = binding.sa_sparse_attn_workspace_size(2, 3, 8, 64, 256, 2)
+    o_bytes = 2 * 3 * 2 * 8 * 64 * 4
+    assert n == (o_bytes + 255) // 256 * 256 + 2 * 3 * 2 * 8 * 4
+    # never more splits than 64-slot tiles
+    assert binding.sa_sparse_attn_workspace_size(1, 1, 8, 64, 64, 8) == 0
