@@ -49,15 +49,34 @@ bool attn_sizes_ok(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K) {
 }
 
 // Split plan: a function of the sizes and the SM count only (never of index
-// values), so a captured graph keeps a fixed grid.
+// values), so a captured graph keeps a fixed grid.  One work unit (token,
+// split) occupies one CTA, or a 2-CTA cluster when D = 512; a unit holds at
+// most sa::max_unit_slots() slots.  Small batches are split so that the units
+// cover the SMs once, keeping at least 3 tiles of 64 slots per split.
+int min_splits(int64_t K) {
+    const int64_t tiles = cdiv(K, 64);
+    return int(cdiv(tiles, sa::max_unit_slots() / 64));
+}
+
+int clamp_splits(int64_t K, int ns) {
+    const int64_t tiles = cdiv(K, 64);
+    if (ns > tiles) ns = int(tiles);
+    if (ns < min_splits(K)) ns = min_splits(K);
+    if (ns < 1) ns = 1;
+    return ns;
+}
+
 int plan_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K, int num_sms) {
     (void)H;
-    (void)D;
-    (void)B;
-    (void)S;
-    (void)K;
-    (void)num_sms;
-    return 1;
+    const int64_t ctas_per_unit = D == 512 ? 2 : 1;
+    const int64_t ctas = B * S * ctas_per_unit;
+    const int64_t tiles = cdiv(K, 64);
+    int64_t ns = 1;
+    if (ctas > 0 && ctas < num_sms) ns = num_sms / ctas;
+    const int64_t cap = tiles / 3 > 1 ? tiles / 3 : 1;
+    if (ns > cap) ns = cap;
+    if (ns > 64) ns = 64;
+    return clamp_splits(K, int(ns));
 }
 
 size_t workspace_bytes_for(int64_t B, int64_t S, int64_t H, int64_t D, int splits) {
@@ -98,8 +117,8 @@ size_t sa_sparse_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D,
     if (!attn_sizes_ok(B, S, H, D, K)) return 0;
     int splits = num_splits;
     if (splits <= 0) splits = sa_sparse_attn_num_splits(B, S, H, D, K);
-    if (splits > cdiv(K, 64)) splits = int(cdiv(K, 64));
-    return workspace_bytes_for(B, S, H, D, splits);
+    if (splits <= 0) return 0;
+    return workspace_bytes_for(B, S, H, D, clamp_splits(K, splits));
 }
 
 sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
@@ -121,9 +140,7 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
     const sa_status st = current_device(&dev);
     if (st != SA_OK) return st;
 
-    int splits = num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms);
-    if (splits > cdiv(K, 64)) splits = int(cdiv(K, 64));
-    if (splits < 1) splits = 1;
+    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms));
     const size_t need = workspace_bytes_for(B, S, H, D, splits);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;

@@ -37,6 +37,8 @@ struct AttnArgs {
 
 // Slots handled by one split (a multiple of the 64-row tile).
 int64_t split_slots(int64_t K, int num_splits);
+// Largest number of slots one work unit (token, split) may hold.
+int max_unit_slots();
 
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream);
