@@ -47,6 +47,23 @@ def _dist():
     return ws, rank, local
 
 
+def rank_seed(rank: int) -> int:
+    """Weak scaling: every rank runs the same workload shape on its own
+    seeded batch (independent query tokens, no data-path collective)."""
+    return 1001 + rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Slowest rank's value (the job's time); identity without a process group."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled during the timed region."""
 
@@ -192,7 +209,7 @@ def run_gpu(args):
     from deepseek_top_sparse_gb300 import binding, workloads
 
     dev = torch.device("cuda", local)
-    inp_cpu = workloads.v4_ratio4_decode(seed=1001 + rank)
+    inp_cpu = workloads.v4_ratio4_decode(seed=rank_seed(rank))
     inp = inp_cpu.to(dev)
     B, S, H, D = inp.q.shape
     T, K = inp.kv.shape[1], inp.topk_idxs.shape[-1]
@@ -237,11 +254,7 @@ def run_gpu(args):
     if ws > 1:
         torch.distributed.barrier()
     per = [a.elapsed_time(b) for a, b in evs]   # ms
-    ms = sum(per) / len(per)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(per) / len(per), device=dev)
     assert binding.sa_device_error(True) == 0
 
     # ---- end to end through the public API: pinned host q / indices in, o out
@@ -270,11 +283,7 @@ def run_gpu(args):
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e2e_ms = sum(e_ms) / len(e_ms)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), device=dev)
 
     # ---- mask build on the mask workload (B=4, Q=2048, 8193 keys, K=2048)
     mask_obj = None
