@@ -27,7 +27,7 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
-           "sa_build_topk_mask", "sa_device_error")
+           "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +70,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_topk_mask_shape.restype = i32
         lib.sa_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p, p]
         lib.sa_build_topk_mask.restype = i32
+        lib.sa_sparse_attn_fwd_static_ws.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p]
+        lib.sa_sparse_attn_fwd_static_ws.restype = i32
         lib.sa_device_error.argtypes = [i32]
         lib.sa_device_error.restype = i32
         _lib = lib
@@ -100,6 +102,14 @@ def sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, 
                               num_splits, workspace, workspace_bytes, stream) -> int:
     return int(load().sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T,
                                                  K, num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K, num_splits,
+                                 stream) -> int:
+    """Allocation-free sparse_attn (workspace inside the library); same
+    arguments as sa_sparse_attn_fwd_splits without the workspace pair."""
+    return int(load().sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
+                                                   num_splits, stream))
 
 
 def sa_topk_mask_shape(batch, max_query_len, max_key_len, reserve_key_starts_word) -> tuple[int, int, int]:

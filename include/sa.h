@@ -108,6 +108,24 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
                                     int64_t K, int num_splits, void *workspace,
                                     size_t workspace_bytes, sa_stream_t stream);
 
+/* Allocation-free variant of sa_sparse_attn_fwd_splits, for callers that
+ * cannot supply device memory: a plain C host program with no device
+ * allocator, or a serving loop that plans all memory up front and must not
+ * call cudaMalloc on its hot path (it can block and can fail under memory
+ * pressure).  The split-KV workspace is a 32 MiB array inside the library
+ * (held on every GPU that uses the library, until the process exits); the
+ * caller passes only inputs and outputs, with the same meaning, layout and
+ * validation as sa_sparse_attn_fwd_splits.  Returns SA_ERR_WORKSPACE when
+ * the planned workspace exceeds 32 MiB.  The first call on a device looks
+ * up the array's address (make it before any stream capture).  All calls on
+ * a device share the array: calls that overlap on the GPU race and must be
+ * serialised by the caller.  The pages have no counterpart of this entry
+ * point; it exists for callers that cannot allocate. */
+sa_status sa_sparse_attn_fwd_static_ws(const void *q, const void *kv, const float *attn_sink,
+                                       const int32_t *topk_idxs, float softmax_scale, void *o,
+                                       int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                       int64_t K, int num_splits, sa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* bit-packed top-k mask                                                    */
 /* ------------------------------------------------------------------------ */
