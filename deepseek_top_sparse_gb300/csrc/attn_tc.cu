@@ -48,6 +48,21 @@ namespace sa {
 
 static __device__ int g_device_error = 0;
 
+// Timeline hooks for performance work: with SA_TRACE defined, CTA 0 records
+// clock64() at fixed points of each role into g_sa_trace[role][tile][event];
+// otherwise they compile to nothing.
+#ifdef SA_TRACE
+__device__ long long g_sa_trace[4][64][16];
+#define SA_TRACE_POINT(role, tile, ev)                                                              \
+    do {                                                                                            \
+        if (blockIdx.x == 0 && (tile) >= 0 && (tile) < 64) g_sa_trace[role][tile][ev] = clock64(); \
+    } while (0)
+#else
+#define SA_TRACE_POINT(role, tile, ev) \
+    do {                               \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,20 +79,18 @@ constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;
 constexpr int kFirstGatherWarp = kMmaWarp + 1;
 constexpr int kGatherWarps = 2;               // both fill every tile, 32 rows each
-// A gather warp publishes tile a once it has issued tile a + kGatherLag
-// (kGatherLag + 1 tiles in flight per warp).  The softmax needs S(a+1) to
-// finish tile a, so publication may not wait on stage reuse past tile a-2:
-// kGatherLag <= stages - 2.
-constexpr int kGatherLag = 1;
 
 template <int DC, int CL>
 struct Cfg {
     static_assert(DC == 64 || DC == 128 || DC == 256, "per-CTA head-dim slice");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
-    static constexpr int NS = 4;                          // kv ring depth
-    static_assert(kGatherLag <= NS - 2, "gather publication must not depend on the tile being finished");
+    static constexpr int NS = CL == 2 ? 5 : 4;            // kv ring depth
     static constexpr int THREADS = (kFirstGatherWarp + kGatherWarps) * 32;
-    static constexpr int X_BYTES = kM * kBN * 4;          // 32 KB fp32 partial logits
+    // partner's partial logits of one tile as block floating point: 16-bit
+    // codes [8 chunks][128 rows][16 B] then one fp32 step per (row, half)
+    static constexpr int XQ_BYTES = kM * kBN * 2;         // 16 KB
+    static constexpr int X_BYTES = XQ_BYTES + 2 * kM * 4; // + 1 KB of steps
+    static_assert(X_BYTES % 1024 == 0, "receive buffers keep 1 KB alignment");
     static constexpr int OFF_KV = 0;
     static constexpr int OFF_X = OFF_KV + NS * STAGE_BYTES;
     static constexpr int OFF_IDX = OFF_X + (CL == 2 ? 2 * X_BYTES : 0);
@@ -86,8 +99,8 @@ struct Cfg {
     static constexpr int OFF_RED = OFF_LIST + kMaxUnitTiles * 4 + 16;   // float [3][2][128]
     static constexpr int OFF_BAR = OFF_RED + 3 * 2 * kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
-    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar
-    static constexpr int NUM_BARS = 2 * NS + 15;
+    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar epi_bar
+    static constexpr int NUM_BARS = 2 * NS + 16;
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_TSLOT + 16 + 1024;    // + slack to align the base to 1 KB
     // TMEM columns: O_c fp32, S fp32 (one tile), P bf16 pairs (two tiles), Q_c bf16 pairs
@@ -99,6 +112,7 @@ struct Cfg {
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(NS * STAGE_BYTES >= kM * DC * 4, "the kv ring can stage a full fp32 output tile");
 };
 
 struct TcParams {
@@ -135,6 +149,34 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, wait_bar<kCluster>(bar, parity));
+}
+
+// Block floating point for the partner exchange: 32 partial logits become
+// 16-bit codes sharing one power-of-two step 2^(e-14), where max|x| < 2^e,
+// so |x| / step < 2^14 and the absolute error is at most half a step
+// (<= max|x| * 2^-15).  Encoding adds kBfpMagic = 1.5*2^23 + 2^15 to x/step:
+// the float's low 16 bits are then (round(x/step) + 2^15), with no integer
+// conversion.  Decoding ORs a code into 2^23 and removes 2^23 + 2^15.  A
+// non-finite block gets a NaN step, so NaN still propagates.
+constexpr float kBfpMagic = 12615680.0f;      // 1.5 * 2^23 + 2^15
+constexpr float kBfpDecodeBias = 8421376.0f;  // 2^23 + 2^15
+
+struct BfpStep {
+    float step, inv;
+};
+
+__device__ __forceinline__ BfpStep bfp_step(float amax) {
+    const uint32_t bexp = (__float_as_uint(amax) >> 23) & 0xFFu;   // biased exponent of max|x|
+    if (bexp == 0xFFu || amax != amax) return {__uint_as_float(0x7FC00000u), 0.f};  // inf / NaN
+    if (bexp < 20u) return {__uint_as_float(6u << 23), __uint_as_float(248u << 23)};  // ~0: 2^-121
+    // max|x| < 2^(bexp-126); step = 2^(bexp-126-14): biased exponent bexp-13
+    return {__uint_as_float((bexp - 13u) << 23), __uint_as_float((267u - bexp) << 23)};
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float &sum) {
@@ -181,8 +223,10 @@ attn_tc_kernel(const TcParams p) {
     const uint32_t mma_done = bar(2 * C::NS + 12);
     const uint32_t red_bar = bar(2 * C::NS + 13);
     const uint32_t l_bar = bar(2 * C::NS + 14);
+    const uint32_t epi_bar = bar(2 * C::NS + 15);
 
     // ---------------------------------------------------------------- prologue
+    if (tid == 0) SA_TRACE_POINT(3, 0, 0);
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tslot), C::TMEM_COLS);
         ptx::tmem_relinquish();
@@ -205,6 +249,7 @@ attn_tc_kernel(const TcParams p) {
         ptx::mbar_init(mma_done, 1);
         ptx::mbar_init(red_bar, kSoftmaxThreads);
         ptx::mbar_init(l_bar, kSoftmaxThreads);
+        ptx::mbar_init(epi_bar, kSoftmaxThreads);
         ptx::fence_mbar_init();
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
@@ -236,12 +281,13 @@ attn_tc_kernel(const TcParams p) {
     ptx::tc_fence_after();
     const uint32_t tbase = *tslot;
     const int n_act = act[kMaxUnitTiles];
+    if (tid == 0) SA_TRACE_POINT(3, 0, 1);
 
     if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ gather
-        // every gather warp copies its share of the rows of every tile; a tile
-        // is published (fence + arrive) once the warp has issued kGatherLag
-        // more, so kGatherLag + 1 tiles per warp are in flight
+        // every gather warp copies its share of the rows of every tile; each
+        // lane's copies arrive on the stage's mbarrier when they land, so a
+        // warp runs ahead into every free stage (up to NS tiles in flight)
         constexpr int CPR = DC / 8;     // 16-byte chunks per row slice
         constexpr int RPI = 32 / CPR;   // rows per warp instruction
         constexpr int RPW = kBN / kGatherWarps;
@@ -253,10 +299,12 @@ attn_tc_kernel(const TcParams p) {
         int a = 0;
         for (; a < n_act; ++a) {
             const int s = a % C::NS, f = a / C::NS;
+            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
             if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
                 ok = false;
                 break;
             }
+            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
             const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
             const int32_t *rc = rowc + act[a] * kBN;
 #pragma unroll
@@ -267,18 +315,11 @@ attn_tc_kernel(const TcParams p) {
                 const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
                 ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
             }
-            ptx::cp_async_commit();
-            if (a >= kGatherLag) {
-                asm volatile("cp.async.wait_group %0;" ::"n"(kGatherLag) : "memory");
-                ptx::fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-                ptx::mbar_arrive(kv_full((a - kGatherLag) % C::NS));
-            }
+            ptx::cp_async_arrive_noinc(kv_full(s));
+            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
         }
-        ptx::cp_async_wait_all();
-        if (ok) {
-            ptx::fence_proxy_async_smem();
-            for (int k = a - kGatherLag < 0 ? 0 : a - kGatherLag; k < a; ++k) ptx::mbar_arrive(kv_full(k % C::NS));
-        }
+        ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
+        (void)ok;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -294,6 +335,7 @@ attn_tc_kernel(const TcParams p) {
                 // S(q) overwrites the single S buffer once S(q-1) has been read
                 if (qn < n_act && qn <= pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1) &&
                     (qn == 0 || ptx::mbar_test_wait(s_empty, (qn - 1) & 1))) {
+                    ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> MMA reads
                     ptx::tc_fence_after();
                     const uint32_t ka = ptx::smem_u32(smem + C::OFF_KV + (qn % C::NS) * C::STAGE_BYTES);
 #pragma unroll
@@ -302,6 +344,7 @@ attn_tc_kernel(const TcParams p) {
                         ptx::mma_ts(tbase + C::S_COL, tbase + C::Q_COL + k * 8, bd, idesc_qk, k > 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(s_full);
+                    SA_TRACE_POINT(1, qn, 0);
                     ++qn;
                     prog = true;
                 } else if (pn < qn && ptx::mbar_test_wait(p_full(pn & 1), (pn >> 1) & 1)) {
@@ -316,6 +359,7 @@ attn_tc_kernel(const TcParams p) {
                     ptx::mma_commit(kv_empty(pn % C::NS));
                     ptx::mma_commit(p_empty(pn & 1));
                     ptx::mma_commit(o_done);
+                    SA_TRACE_POINT(1, pn, 1);
                     ++pn;
                     prog = true;
                 }
@@ -388,26 +432,50 @@ attn_tc_kernel(const TcParams p) {
         // and, with a partner, send them to its receive buffer j & 1 as
         // asynchronous stores that complete_tx on the partner's x_full
         auto take = [&](int j, uint32_t (&r)[32]) -> bool {
+            if (tid == 0) SA_TRACE_POINT(2, j, 0);
             if (!wait_all(s_full, j & 1)) return false;
+            if (tid == 0) SA_TRACE_POINT(2, j, 1);
             ptx::tc_fence_after();
             ptx::tmem_ld32(s_addr, r);
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             ptx::mbar_arrive(s_empty);
             if constexpr (CL == 2) {
+                // Both CTAs use the block-floating-point value of BOTH partials,
+                // so the two sums (and everything after them) are bit-identical.
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(r[i])));
+                const BfpStep st = bfp_step(amax);
+                const float step = st.step;
+                const float nbias = -kBfpMagic * step;
+                uint32_t m[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float y0 = fmaf(__uint_as_float(r[2 * i]), st.inv, kBfpMagic);
+                    const float y1 = fmaf(__uint_as_float(r[2 * i + 1]), st.inv, kBfpMagic);
+                    m[i] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
+                    r[2 * i] = __float_as_uint(fmaf(y0, step, nbias));   // own partial, same rounding
+                    r[2 * i + 1] = __float_as_uint(fmaf(y1, step, nbias));
+                }
                 if (j >= 2 && !wait_all(x_empty(j & 1), ((j >> 1) - 1) & 1)) return false;
-                // chunk-major layout [16 chunks][128 rows][16 B]: each warp
-                // instruction writes 512 contiguous bytes of the partner's buffer
-                const uint32_t row = xrow_rem + uint32_t(j & 1) * C::X_BYTES;
+                if (tid == 0) SA_TRACE_POINT(2, j, 2);
+                // chunk-major codes [8 chunks][128 rows][16 B] (each warp
+                // instruction writes 512 contiguous bytes), then the steps
+                const uint32_t buf = xrow_rem + uint32_t(j & 1) * C::X_BYTES;
                 const uint32_t xb = (j & 1) ? xfull_rem1 : xfull_rem0;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    ptx::st_async_v4(row + uint32_t(8 * half + c) * (kM * 16u), r[4 * c], r[4 * c + 1], r[4 * c + 2],
-                                     r[4 * c + 3], xb);
+                for (int c = 0; c < 4; ++c)
+                    ptx::st_async_v4(buf + uint32_t(4 * half + c) * (kM * 16u), m[4 * c], m[4 * c + 1], m[4 * c + 2],
+                                     m[4 * c + 3], xb);
+                ptx::st_async_b32(buf - uint32_t(h) * 16u + C::XQ_BYTES + uint32_t(half * kM + h) * 4u,
+                                  __float_as_uint(step), xb);
+                if (tid == 0) SA_TRACE_POINT(2, j, 3);
             }
             return true;
         };
         bool ok = true;
+        const bool pos_scale = p.scale_log2 >= 0.f;
         float m_run = -INFINITY, l_run = 0.f;
         uint32_t cur[32], nxt[32];
         if (n_act > 0) ok = take(0, cur);
@@ -421,30 +489,49 @@ attn_tc_kernel(const TcParams p) {
             float s[32];
             if constexpr (CL == 2) {
                 if (tid == 0) ptx::mbar_arrive_expect_tx(x_full(a & 1), C::X_BYTES);
+                if (tid == 0) SA_TRACE_POINT(2, a, 4);
                 if (!wait_all<true>(x_full(a & 1), (a >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *xr = smem + C::OFF_X + (a & 1) * C::X_BYTES + h * 16;
+                if (tid == 0) SA_TRACE_POINT(2, a, 5);
+                const uint8_t *xbuf = smem + C::OFF_X + (a & 1) * C::X_BYTES;
+                const float step = *reinterpret_cast<const float *>(xbuf + C::XQ_BYTES + (half * kM + h) * 4);
+                const float dbias = -kBfpDecodeBias * step;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 v = *reinterpret_cast<const float4 *>(xr + (8 * half + c) * (kM * 16));
-                    s[4 * c] = __uint_as_float(cur[4 * c]) + v.x;
-                    s[4 * c + 1] = __uint_as_float(cur[4 * c + 1]) + v.y;
-                    s[4 * c + 2] = __uint_as_float(cur[4 * c + 2]) + v.z;
-                    s[4 * c + 3] = __uint_as_float(cur[4 * c + 3]) + v.w;
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xbuf + (4 * half + c) * (kM * 16) + h * 16);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 8 * c + 2 * e;
+                        const float lo = fmaf(__uint_as_float((w[e] & 0xFFFFu) | 0x4B000000u), step, dbias);
+                        const float hi = fmaf(__uint_as_float((w[e] >> 16) | 0x4B000000u), step, dbias);
+                        s[i] = __uint_as_float(cur[i]) + lo;
+                        s[i + 1] = __uint_as_float(cur[i + 1]) + hi;
+                    }
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(cur[j]);
             }
+            // masked, scaled row max of this half (the scale is applied once,
+            // to the max, when it is positive; invalid slots become -inf)
             float mloc = -INFINITY;
+            if (vm != 0xFFFFFFFFu) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                s[j] = ((vm >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
-                mloc = fmaxf(mloc, s[j]);
+                for (int j = 0; j < 32; ++j) s[j] = ((vm >> j) & 1u) ? s[j] : -INFINITY;
+            }
+            if (pos_scale) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mloc = fmaxf(mloc, s[j]);
+                mloc *= p.scale_log2;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mloc = fmaxf(mloc, s[j] * p.scale_log2);
             }
             // row max over both column halves
+            if (tid == 0) SA_TRACE_POINT(2, a, 6);
             red[(a & 1) * 256 + half * 128 + h] = mloc;
             ptx::mbar_arrive(red_bar);
             if (!wait_all(red_bar, a & 1)) {
@@ -455,12 +542,14 @@ attn_tc_kernel(const TcParams p) {
                 // every softmax thread has read receive buffer a & 1: return the credit
                 if (tid == 0) ptx::mbar_arrive_remote_relaxed((a & 1) ? xempty_rem1 : xempty_rem0);
             }
+            if (tid == 0) SA_TRACE_POINT(2, a, 7);
             const float mx = fmaxf(mloc, red[(a & 1) * 256 + (half ^ 1) * 128 + h]);
             // P buffer a & 1 is free once the P.V of tile a-2 has completed
             if (a >= 2 && !wait_all(p_empty(a & 1), ((a >> 1) - 1) & 1)) {
                 ok = false;
                 break;
             }
+            if (tid == 0) SA_TRACE_POINT(2, a, 8);
             if (a == 0) {
                 m_run = mx;
             } else {
@@ -490,20 +579,31 @@ attn_tc_kernel(const TcParams p) {
                     }
                 }
             }
-            // P = 2^(x - m) as bf16 pairs into TMEM (A operand of P.V)
+            // P = 2^(scale*s - m) as bf16 pairs into TMEM (A operand of P.V);
+            // invalid slots hold -inf and give exactly 0
             uint32_t pw[16];
             float lsum = 0.f;
+            const float nm = -m_run;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pw[c] = pack_bf16(exp2f(s[2 * c] - m_run), exp2f(s[2 * c + 1] - m_run), lsum);
+            for (int c = 0; c < 16; ++c) {
+                const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
+                const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
+                lsum += p0 + p1;
+                const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                pw[c] = *reinterpret_cast<const uint32_t *>(&v);
+            }
             ptx::tmem_st16(lane_addr + C::P_COL + (a & 1) * (kBN / 2) + half * 16, pw);
             ptx::tmem_wait_st();
+            if (tid == 0) SA_TRACE_POINT(2, a, 9);
             l_run += lsum;
             ptx::tc_fence_before();
             ptx::mbar_arrive(p_full(a & 1));
+            if (tid == 0) SA_TRACE_POINT(2, a, 10);
 #pragma unroll
             for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
         }
         // ------------------------------------------------------------ epilogue
+        if (tid == 0) SA_TRACE_POINT(3, 0, 2);
         if (ok) ok = wait_all(mma_done, 0);
         float l_tot = l_run;
         if (ok) {
@@ -514,70 +614,87 @@ attn_tc_kernel(const TcParams p) {
         }
         ptx::tc_fence_after();
         if (ok) {
-            if (p.num_splits == 1) {
+            // Output rows are staged in shared memory (the kv ring is idle once
+            // every MMA has completed) and then written with coalesced 16-byte
+            // stores, 512 contiguous bytes per warp instruction.  Staged row h
+            // holds this CTA's DC columns; its 16-byte chunk c sits at chunk
+            // position c ^ (h & 7), so the per-row writes are conflict-free.
+            const bool split_out = p.num_splits > 1;
+            float f = 0.f, lse = -INFINITY;
+            if (!split_out) {
                 const float s2 = hv ? p.sink[h] * kLog2e : 0.f;
-                float f = 0.f;
                 if (n_act > 0 && s2 != INFINITY) {
                     const float M = fmaxf(m_run, s2);
                     const float e = exp2f(m_run - M);
                     f = e / (l_tot * e + exp2f(s2 - M));
                 }
                 if (isnan(s2)) f = NAN;
-                __nv_bfloat16 *orow = p.o + (tok * p.H + (hv ? h : 0)) * p.D + int64_t(crank) * DC + half * (DC / 2);
-#pragma unroll 1
-                for (int ch = 0; ch < DC / 64; ++ch) {
-                    uint32_t r[32];
-                    if (n_act > 0) {
-                        ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r);
-                        ptx::tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = 0u;
-                    }
-                    if (hv) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-                        float dummy = 0.f;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(r[8 * v + 0]) * f, __uint_as_float(r[8 * v + 1]) * f, dummy);
-                            w.y = pack_bf16(__uint_as_float(r[8 * v + 2]) * f, __uint_as_float(r[8 * v + 3]) * f, dummy);
-                            w.z = pack_bf16(__uint_as_float(r[8 * v + 4]) * f, __uint_as_float(r[8 * v + 5]) * f, dummy);
-                            w.w = pack_bf16(__uint_as_float(r[8 * v + 6]) * f, __uint_as_float(r[8 * v + 7]) * f, dummy);
-                            dst[v] = w;
-                        }
-                    }
-                }
-            } else {
+            } else if (n_act > 0) {
                 // split partial: O / l (fp32) and lse = m + log2(l) (base 2)
-                const float inv = n_act > 0 ? 1.f / l_tot : 0.f;
-                const float lse = n_act > 0 ? m_run + log2f(l_tot) : -INFINITY;
-                const int64_t prow_i = (tok * p.num_splits + split) * p.H + (hv ? h : 0);
-                float *wrow = p.ws_o + prow_i * p.D + int64_t(crank) * DC + half * (DC / 2);
+                f = 1.f / l_tot;
+                lse = m_run + log2f(l_tot);
+            }
+            const int rb = split_out ? DC * 4 : DC * 2;     // staged row bytes
+            uint8_t *stage = smem + C::OFF_KV;
+            uint8_t *srow = stage + h * rb;
 #pragma unroll 1
-                for (int ch = 0; ch < DC / 64; ++ch) {
-                    uint32_t r[32];
-                    if (n_act > 0) {
-                        ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r);
-                        ptx::tmem_wait_ld();
-                    } else {
+            for (int ch = 0; ch < DC / 64; ++ch) {
+                uint32_t r[32];
+                if (n_act > 0) {
+                    ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r);
+                    ptx::tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (split_out) {
+                    const int c0 = (half * (DC / 2) + ch * 32) / 4;   // first 16-byte chunk
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float4 w = make_float4(__uint_as_float(r[4 * v]) * f, __uint_as_float(r[4 * v + 1]) * f,
+                                                     __uint_as_float(r[4 * v + 2]) * f,
+                                                     __uint_as_float(r[4 * v + 3]) * f);
+                        *reinterpret_cast<float4 *>(srow + (((c0 + v) ^ (h & 7)) * 16)) = w;
                     }
-                    if (hv) {
-                        float4 *dst = reinterpret_cast<float4 *>(wrow + ch * 32);
+                } else {
+                    const int c0 = (half * (DC / 2) + ch * 32) / 8;
+                    float dummy = 0.f;
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                                 __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(r[8 * v + 0]) * f, __uint_as_float(r[8 * v + 1]) * f, dummy);
+                        w.y = pack_bf16(__uint_as_float(r[8 * v + 2]) * f, __uint_as_float(r[8 * v + 3]) * f, dummy);
+                        w.z = pack_bf16(__uint_as_float(r[8 * v + 4]) * f, __uint_as_float(r[8 * v + 5]) * f, dummy);
+                        w.w = pack_bf16(__uint_as_float(r[8 * v + 6]) * f, __uint_as_float(r[8 * v + 7]) * f, dummy);
+                        *reinterpret_cast<uint4 *>(srow + (((c0 + v) ^ (h & 7)) * 16)) = w;
                     }
                 }
-                if (hv && crank == 0 && half == 0) p.ws_lse[prow_i] = lse;
+            }
+            if (split_out && hv && crank == 0 && half == 0)
+                p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
+            ptx::mbar_arrive(epi_bar);
+            ok = wait_all(epi_bar, 0);
+            if (ok) {
+                // warp w copies rows [16w, 16w + 16)
+                const int nch = rb / 16;
+                for (int rr = 0; rr < kM / kSoftmaxWarps; ++rr) {
+                    const int row = warp * (kM / kSoftmaxWarps) + rr;
+                    if (row >= p.H) break;
+                    uint8_t *dst = split_out
+                        ? reinterpret_cast<uint8_t *>(p.ws_o + ((tok * p.num_splits + split) * p.H + row) * p.D +
+                                                      int64_t(crank) * DC)
+                        : reinterpret_cast<uint8_t *>(p.o + (tok * p.H + row) * p.D + int64_t(crank) * DC);
+                    const uint8_t *src = stage + row * rb;
+                    for (int c = lane; c < nch; c += 32)
+                        *reinterpret_cast<uint4 *>(dst + c * 16) =
+                            *reinterpret_cast<const uint4 *>(src + ((c ^ (row & 7)) * 16));
+                }
             }
         }
     }
 
     // ---------------------------------------------------------------- teardown
+    if (tid == 0) SA_TRACE_POINT(3, 0, 3);
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -725,6 +842,16 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
     }
     return cudaGetLastError();
 }
+
+#ifdef SA_TRACE
+}  // namespace sa
+extern "C" int sa_trace_read(long long *out) { return (int)cudaMemcpyFromSymbol(out, sa::g_sa_trace, sizeof(sa::g_sa_trace)); }
+extern "C" int sa_trace_clear() {
+    static long long z[4 * 64 * 16] = {0};
+    return (int)cudaMemcpyToSymbol(sa::g_sa_trace, z, sizeof(z));
+}
+namespace sa {
+#endif
 
 cudaError_t read_device_error(int *value, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();

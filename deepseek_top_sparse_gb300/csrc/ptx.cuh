@@ -123,6 +123,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                  : "memory");
 }
 
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
+                 "r"(remote_bar)
+                 : "memory");
+}
+
 // ------------------------------------------------------------- cp.async (LSU)
 
 // 16-byte global -> shared copy; src_bytes = 0 zero-fills the destination
@@ -131,6 +137,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// The mbarrier receives one arrival from this thread once all of its earlier
+// cp.async copies have landed (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -94,6 +94,15 @@ def test_wide_rows_use_global_path_bit_exact():
     np.testing.assert_array_equal(_gpu_build(mi), _oracle_build(mi))
 
 
+def test_mid_width_rows_use_cta_path_bit_exact():
+    # 100000 keys -> 3125 words per row: too wide for a warp's image, one CTA per row
+    rng = np.random.default_rng(8)
+    topk = torch.from_numpy(rng.integers(-3, 100003, size=(7, 1000)).astype(np.int32))
+    mi = workloads.MaskInputs(topk, torch.tensor([0, 3, 7], dtype=torch.int32), 2, 5, 100000,
+                              torch.tensor([-1, 12], dtype=torch.int32))
+    np.testing.assert_array_equal(_gpu_build(mi), _oracle_build(mi))
+
+
 def test_unaligned_topk_rows_scalar_path():
     rng = np.random.default_rng(6)
     topk = torch.from_numpy(rng.integers(0, 500, size=(9, 37)).astype(np.int32))  # K % 4 != 0
