@@ -53,6 +53,19 @@ static __device__ int g_device_error = 0;
 // otherwise they compile to nothing.
 #ifdef SA_TRACE
 __device__ long long g_sa_trace[4][64][16];
+// per CTA: globaltimer (ns) at start, prologue end, epilogue start, end;
+// combine kernel: earliest start and latest end
+__device__ unsigned long long g_sa_cta[4096][4];
+__device__ unsigned long long g_sa_comb[2];
+__device__ __forceinline__ unsigned long long sa_gtime() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#define SA_CTA_POINT(ev)                                                     \
+    do {                                                                     \
+        if (threadIdx.x == 0 && blockIdx.x < 4096) g_sa_cta[blockIdx.x][ev] = sa_gtime(); \
+    } while (0)
 #define SA_TRACE_POINT(role, tile, ev)                                                              \
     do {                                                                                            \
         if (blockIdx.x == 0 && (tile) >= 0 && (tile) < 64) g_sa_trace[role][tile][ev] = clock64(); \
@@ -60,6 +73,9 @@ __device__ long long g_sa_trace[4][64][16];
 #else
 #define SA_TRACE_POINT(role, tile, ev) \
     do {                               \
+    } while (0)
+#define SA_CTA_POINT(ev) \
+    do {                 \
     } while (0)
 #endif
 
@@ -78,7 +94,16 @@ constexpr int kSoftmaxWarps = 8;              // two per TMEM lane quarter, 32 c
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;
 constexpr int kFirstGatherWarp = kMmaWarp + 1;
-constexpr int kGatherWarps = 2;               // both fill every tile, 32 rows each
+// cp.async gather throughput per SM grows with the number of issuing warps
+// (each warp keeps a bounded number of copies in flight): 7 gather warps.
+constexpr int kGatherWarps = 7;               // all fill every tile, rows interleaved
+// 16 warps = 4 warpgroups launched at 128 registers a thread; after the
+// prologue the two softmax warpgroups grow to 160 and the MMA + gather
+// warpgroups shrink to 96: 256 * 160 + 256 * 96 = 512 * 128 (the smallest
+// split with no spills on either side).
+constexpr int kLaunchRegs = 128;
+constexpr int kSoftmaxRegs = 160;
+constexpr int kOtherRegs = 96;
 
 template <int DC, int CL>
 struct Cfg {
@@ -86,6 +111,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = kBN * DC * 2;
     static constexpr int NS = CL == 2 ? 5 : 4;            // kv ring depth
     static constexpr int THREADS = (kFirstGatherWarp + kGatherWarps) * 32;
+    static_assert(THREADS == 512, "four warpgroups");
+    static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
+                  "register split equals the launch allocation");
     // partner's partial logits of one tile as block floating point: 16-bit
     // codes [8 chunks][128 rows][16 B] then one fp32 step per (row, half)
     static constexpr int XQ_BYTES = kM * kBN * 2;         // 16 KB
@@ -97,7 +125,8 @@ struct Cfg {
     static constexpr int OFF_VALID = OFF_IDX + kMaxUnitSlots * 4;
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
     static constexpr int OFF_RED = OFF_LIST + kMaxUnitTiles * 4 + 16;   // float [3][2][128]
-    static constexpr int OFF_BAR = OFF_RED + 3 * 2 * kM * 4;
+    static constexpr int OFF_LSE = OFF_RED + 3 * 2 * kM * 4;             // float [8 splits][128]
+    static constexpr int OFF_BAR = OFF_LSE + 8 * kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
     // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar epi_bar
     static constexpr int NUM_BARS = 2 * NS + 16;
@@ -112,7 +141,10 @@ struct Cfg {
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(NS * STAGE_BYTES >= kM * DC * 4, "the kv ring can stage a full fp32 output tile");
+    // output staging (epilogue): kM rows of up to DC fp32, padded by 16 bytes,
+    // over the kv ring, receive buffers and index lists (all dead by then)
+    static constexpr int STAGE_ROW = DC * 4 + 16;
+    static_assert(kM * STAGE_ROW <= OFF_RED - OFF_KV, "output staging fits below the reduction scratch");
 };
 
 struct TcParams {
@@ -125,6 +157,7 @@ struct TcParams {
     float *ws_lse;            // [tokens, splits, H]
     int64_t S, H, D, T, K;
     int num_splits;
+    int fused;                // 1: the token's splits share a cluster and combine in-kernel
     int unit_slots;           // slots per split, a multiple of kBN, <= kMaxUnitSlots
     float scale_log2;         // softmax_scale * log2(e)
 };
@@ -173,6 +206,8 @@ __device__ __forceinline__ BfpStep bfp_step(float amax) {
     return {__uint_as_float((bexp - 13u) << 23), __uint_as_float((267u - bexp) << 23)};
 }
 
+constexpr int ptx_log2(int x) { return x <= 1 ? 0 : 1 + ptx_log2(x >> 1); }
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -185,6 +220,97 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float &sum) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// In-cluster split combine for one CTA (see the kernel's teardown), run by
+// all C::THREADS threads.  Rows [cr0, cr1) of this CTA's DC columns:
+//   1. every split's log-sum-exp of those rows into a table (one L2 round
+//      trip for the whole CTA; this split's own values are already there),
+//   2. per row the final weights w_i / den (the combine kernel's formula),
+//   3. (row, 16-byte chunk) items spread over all threads, 4 per batch, so
+//      the partial loads of a batch are in flight together.
+template <int DC, typename C>
+__device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int split,
+                                             uint32_t crank, int tid) {
+    const int ns = p.num_splits;
+    const int rp = int((p.H + ns - 1) / ns);
+    const int cr0 = split * rp;
+    const int cr1 = cr0 + rp < p.H ? cr0 + rp : int(p.H);
+    const int nrows = cr1 > cr0 ? cr1 - cr0 : 0;
+    float *tab = reinterpret_cast<float *>(smem + C::OFF_LSE);   // [split][row]
+    const uint8_t *stage = smem + C::OFF_KV;
+    for (int t = tid; t < ns * nrows; t += C::THREADS) {
+        const int i = t / nrows, r = cr0 + t % nrows;
+        if (i != split) tab[i * kM + r] = __ldcg(p.ws_lse + (tok * ns + i) * p.H + r);
+    }
+    __syncthreads();
+    for (int t = tid; t < nrows; t += C::THREADS) {
+        const int r = cr0 + t;
+        float mx = -INFINITY;
+        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, tab[i * kM + r]);
+        const float s2 = p.sink[r] * kLog2e;
+        const float M = fmaxf(mx, s2);
+        const bool zero = (s2 == INFINITY) || (M == -INFINITY);
+        float den = 0.f;
+        if (!zero) {
+            for (int i = 0; i < ns; ++i) {
+                const float li = tab[i * kM + r];
+                if (li != -INFINITY) den += exp2f(li - M);
+            }
+            den += exp2f(s2 - M);
+        }
+        const float f = zero ? 0.f : 1.f / den;
+        const float fn = isnan(s2) ? NAN : f;
+        for (int i = 0; i < ns; ++i) {
+            const float li = tab[i * kM + r];
+            tab[i * kM + r] = (zero || li == -INFINITY) ? 0.f * fn : exp2f(li - M) * fn;
+        }
+    }
+    __syncthreads();
+    constexpr int CH = DC / 4;     // float4 chunks per row
+    constexpr int kB = 4;
+    const int items = nrows * CH;
+    for (int base = tid; base < items; base += kB * C::THREADS) {
+        float4 acc[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < ns; ++i) {
+            float4 v[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int it = base + u * C::THREADS;
+                if (it < items) {
+                    const int r = cr0 + it / CH, c = it % CH;
+                    v[u] = i == split
+                        ? reinterpret_cast<const float4 *>(stage + r * C::STAGE_ROW)[c]
+                        : __ldcg(reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + r) * p.D +
+                                                                  int64_t(crank) * DC) + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int it = base + u * C::THREADS;
+                if (it < items) {
+                    const float w = tab[i * kM + cr0 + it / CH];
+                    acc[u].x = fmaf(w, v[u].x, acc[u].x);
+                    acc[u].y = fmaf(w, v[u].y, acc[u].y);
+                    acc[u].z = fmaf(w, v[u].z, acc[u].z);
+                    acc[u].w = fmaf(w, v[u].w, acc[u].w);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int it = base + u * C::THREADS;
+            if (it < items) {
+                const int r = cr0 + it / CH, c = it % CH;
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+                reinterpret_cast<uint2 *>(p.o + (tok * p.H + r) * p.D + int64_t(crank) * DC)[c] =
+                    make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+            }
+        }
+    }
+}
+
 template <int DC, int CL>
 __global__ void __launch_bounds__(Cfg<DC, CL>::THREADS, 1)
 attn_tc_kernel(const TcParams p) {
@@ -193,7 +319,11 @@ attn_tc_kernel(const TcParams p) {
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t crank = CL == 2 ? ptx::cluster_ctarank() : 0u;
+    // A cluster is one token: its splits x the CL head-dim halves (CL alone
+    // when the splits are combined by a separate kernel).  Rank = local split
+    // * CL + crank, so the head-dim partner is rank ^ 1.
+    const uint32_t rank = (CL == 2 || p.fused) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t crank = CL == 2 ? (rank & 1u) : 0u;
     const int64_t unit = blockIdx.x / CL;
     const int64_t tok = unit / p.num_splits;
     const int split = int(unit % p.num_splits);
@@ -227,6 +357,17 @@ attn_tc_kernel(const TcParams p) {
 
     // ---------------------------------------------------------------- prologue
     if (tid == 0) SA_TRACE_POINT(3, 0, 0);
+    SA_CTA_POINT(0);
+    if (warp < kSoftmaxWarps) {
+        // this thread's Q slice (loaded after the prologue) into L2 now
+        const int hq = (warp & 3) * 32 + lane;
+        if (hq < p.H) {
+            const char *qs = reinterpret_cast<const char *>(p.q + (tok * p.H + hq) * p.D + int64_t(crank) * DC +
+                                                            (warp >> 2) * (DC / 2));
+#pragma unroll
+            for (int o = 0; o < DC; o += 128) ptx::prefetch_l2(qs + o);
+        }
+    }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tslot), C::TMEM_COLS);
         ptx::tmem_relinquish();
@@ -253,16 +394,28 @@ attn_tc_kernel(const TcParams p) {
         ptx::fence_mbar_init();
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
-    // mask per tile, 32 slots per warp step
+    // mask per tile, 32 slots per warp step; every load of a thread is issued
+    // before the first is used, so the whole list costs one memory latency
     {
+        constexpr int kWarpsAll = C::THREADS / 32;
+        constexpr int kSteps = (kMaxUnitSlots / 32 + kWarpsAll - 1) / kWarpsAll;
         const int32_t *irow = p.idx + tok * p.K + slot0;
-        for (int ch = warp; ch < ntiles * 2; ch += C::THREADS / 32) {
-            const int j = ch * 32 + lane;
-            const int32_t t = j < nslots ? __ldg(irow + j) : -1;
-            const bool v = t >= 0 && int64_t(t) < p.T;
-            rowc[j] = v ? int32_t(b * p.T + t) : -1;
-            const uint32_t m = __ballot_sync(0xffffffffu, v);
-            if (lane == 0) reinterpret_cast<uint32_t *>(vmask)[ch] = m;
+        int32_t tv[kSteps];
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) {
+            const int j = (u * kWarpsAll + warp) * 32 + lane;
+            tv[u] = j < nslots ? __ldg(irow + j) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) {
+            const int ch = u * kWarpsAll + warp;
+            if (ch < ntiles * 2) {
+                const int j = ch * 32 + lane;
+                const bool v = tv[u] >= 0 && int64_t(tv[u]) < p.T;
+                rowc[j] = v ? int32_t(b * p.T + tv[u]) : -1;
+                const uint32_t m = __ballot_sync(0xffffffffu, v);
+                if (lane == 0) reinterpret_cast<uint32_t *>(vmask)[ch] = m;
+            }
         }
     }
     __syncthreads();
@@ -282,99 +435,108 @@ attn_tc_kernel(const TcParams p) {
     const uint32_t tbase = *tslot;
     const int n_act = act[kMaxUnitTiles];
     if (tid == 0) SA_TRACE_POINT(3, 0, 1);
-
-    if (warp >= kFirstGatherWarp) {
-        // ------------------------------------------------------------ gather
-        // every gather warp copies its share of the rows of every tile; each
-        // lane's copies arrive on the stage's mbarrier when they land, so a
-        // warp runs ahead into every free stage (up to NS tiles in flight)
-        constexpr int CPR = DC / 8;     // 16-byte chunks per row slice
-        constexpr int RPI = 32 / CPR;   // rows per warp instruction
-        constexpr int RPW = kBN / kGatherWarps;
-        const int g = warp - kFirstGatherWarp;
-        const int sub = lane / CPR, ch = lane % CPR;
-        const uint32_t dst_col = uint32_t(ch >> 3) * (kBN * 128);
-        const char *kvb = reinterpret_cast<const char *>(p.kv) + (int64_t(crank) * DC + ch * 8) * 2;
-        bool ok = true;
-        int a = 0;
-        for (; a < n_act; ++a) {
-            const int s = a % C::NS, f = a / C::NS;
-            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
-            if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
-            const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
-            const int32_t *rc = rowc + act[a] * kBN;
-#pragma unroll
-            for (int i = 0; i < RPW / RPI; ++i) {
-                const int r = g * RPW + i * RPI + sub;
-                const int32_t row = rc[r];
-                const char *src = kvb + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
-                const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
-                ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
-            }
-            ptx::cp_async_arrive_noinc(kv_full(s));
-            if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
-        }
-        ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
-        (void)ok;
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kM, kBN, false);
-            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kM, DC, true);
-            bool ok = wait_bar(q_ready, 0);
-            ptx::tc_fence_after();
-            int qn = 0, pn = 0;
-            uint32_t idle = 0;
-            long long t0 = 0;
-            while (ok && pn < n_act) {
-                bool prog = false;
-                // S(q) overwrites the single S buffer once S(q-1) has been read
-                if (qn < n_act && qn <= pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1) &&
-                    (qn == 0 || ptx::mbar_test_wait(s_empty, (qn - 1) & 1))) {
-                    ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> MMA reads
-                    ptx::tc_fence_after();
-                    const uint32_t ka = ptx::smem_u32(smem + C::OFF_KV + (qn % C::NS) * C::STAGE_BYTES);
-#pragma unroll
-                    for (int k = 0; k < DC / 16; ++k) {
-                        const uint64_t bd = ptx::sdesc_sw128(ka + (k / 4) * (kBN * 128) + (k % 4) * 32, 16, 1024);
-                        ptx::mma_ts(tbase + C::S_COL, tbase + C::Q_COL + k * 8, bd, idesc_qk, k > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(s_full);
-                    SA_TRACE_POINT(1, qn, 0);
-                    ++qn;
-                    prog = true;
-                } else if (pn < qn && ptx::mbar_test_wait(p_full(pn & 1), (pn >> 1) & 1)) {
-                    ptx::tc_fence_after();
-                    const uint32_t va = ptx::smem_u32(smem + C::OFF_KV + (pn % C::NS) * C::STAGE_BYTES);
-                    const uint32_t pa = tbase + C::P_COL + (pn & 1) * (kBN / 2);
-#pragma unroll
-                    for (int t = 0; t < kBN / 16; ++t) {
-                        const uint64_t bd = ptx::sdesc_sw128(va + t * 2048, kBN * 128, 1024);
-                        ptx::mma_ts(tbase + C::O_COL, pa + t * 8, bd, idesc_pv, (pn > 0 || t > 0) ? 1u : 0u);
-                    }
-                    ptx::mma_commit(kv_empty(pn % C::NS));
-                    ptx::mma_commit(p_empty(pn & 1));
-                    ptx::mma_commit(o_done);
-                    SA_TRACE_POINT(1, pn, 1);
-                    ++pn;
-                    prog = true;
-                }
-                if (prog) {
-                    idle = 0;
-                } else if (++idle == 1) {
-                    t0 = clock64();
-                } else if ((idle & 1023u) == 0 && clock64() - t0 > kWaitCycles) {
-                    record_error(kErrWaitTimeout);
+    SA_CTA_POINT(1);
+    if (warp >= kSoftmaxWarps) {
+        // MMA and gather warpgroups: a small register budget
+        ptx::setmaxnreg_dec<kOtherRegs>();
+        if (warp >= kFirstGatherWarp) {
+            // ------------------------------------------------------------ gather
+            // every gather warp copies its share of the rows of every tile; each
+            // lane's copies arrive on the stage's mbarrier when they land, so a
+            // warp runs ahead into every free stage (up to NS tiles in flight)
+            constexpr int CPR = DC / 8;     // 16-byte chunks per row slice
+            constexpr int RPI = 32 / CPR;   // rows per warp instruction
+            constexpr int STEP = RPI * kGatherWarps;
+            constexpr int ITERS = (kBN + STEP - 1) / STEP;
+            const int g = warp - kFirstGatherWarp;
+            const int sub = lane / CPR, ch = lane % CPR;
+            const uint32_t dst_col = uint32_t(ch >> 3) * (kBN * 128);
+            const char *kvb = reinterpret_cast<const char *>(p.kv) + (int64_t(crank) * DC + ch * 8) * 2;
+            bool ok = true;
+            int a = 0;
+            for (; a < n_act; ++a) {
+                const int s = a % C::NS, f = a / C::NS;
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
+                if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
                     ok = false;
+                    break;
                 }
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
+                const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
+                const int32_t *rc = rowc + act[a] * kBN;
+    #pragma unroll
+                for (int i = 0; i < ITERS; ++i) {
+                    const int r = i * STEP + g * RPI + sub;   // warp g: row groups g, g + G, ...
+                    if (STEP * ITERS > kBN && r >= kBN) break;
+                    const int32_t row = rc[r];
+                    const char *src = kvb + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
+                    const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
+                    ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
+                }
+                ptx::cp_async_arrive_noinc(kv_full(s));
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
             }
-            ptx::mma_commit(mma_done);
+            ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
+            (void)ok;
+        } else {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kM, kBN, false);
+                constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kM, DC, true);
+                bool ok = wait_bar(q_ready, 0);
+                ptx::tc_fence_after();
+                int qn = 0, pn = 0;
+                uint32_t idle = 0;
+                long long t0 = 0;
+                while (ok && pn < n_act) {
+                    bool prog = false;
+                    // S(q) overwrites the single S buffer once S(q-1) has been read
+                    if (qn < n_act && qn <= pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1) &&
+                        (qn == 0 || ptx::mbar_test_wait(s_empty, (qn - 1) & 1))) {
+                        ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> MMA reads
+                        ptx::tc_fence_after();
+                        const uint32_t ka = ptx::smem_u32(smem + C::OFF_KV + (qn % C::NS) * C::STAGE_BYTES);
+    #pragma unroll
+                        for (int k = 0; k < DC / 16; ++k) {
+                            const uint64_t bd = ptx::sdesc_sw128(ka + (k / 4) * (kBN * 128) + (k % 4) * 32, 16, 1024);
+                            ptx::mma_ts(tbase + C::S_COL, tbase + C::Q_COL + k * 8, bd, idesc_qk, k > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(s_full);
+                        SA_TRACE_POINT(1, qn, 0);
+                        ++qn;
+                        prog = true;
+                    } else if (pn < qn && ptx::mbar_test_wait(p_full(pn & 1), (pn >> 1) & 1)) {
+                        ptx::tc_fence_after();
+                        const uint32_t va = ptx::smem_u32(smem + C::OFF_KV + (pn % C::NS) * C::STAGE_BYTES);
+                        const uint32_t pa = tbase + C::P_COL + (pn & 1) * (kBN / 2);
+    #pragma unroll
+                        for (int t = 0; t < kBN / 16; ++t) {
+                            const uint64_t bd = ptx::sdesc_sw128(va + t * 2048, kBN * 128, 1024);
+                            ptx::mma_ts(tbase + C::O_COL, pa + t * 8, bd, idesc_pv, (pn > 0 || t > 0) ? 1u : 0u);
+                        }
+                        ptx::mma_commit(kv_empty(pn % C::NS));
+                        ptx::mma_commit(p_empty(pn & 1));
+                        ptx::mma_commit(o_done);
+                        SA_TRACE_POINT(1, pn, 1);
+                        ++pn;
+                        prog = true;
+                    }
+                    if (prog) {
+                        idle = 0;
+                    } else if (++idle == 1) {
+                        t0 = clock64();
+                    } else if ((idle & 1023u) == 0 && clock64() - t0 > kWaitCycles) {
+                        record_error(kErrWaitTimeout);
+                        ok = false;
+                    }
+                }
+                ptx::mma_commit(mma_done);
+            }
         }
+        // back to the launch allocation: the teardown below is common code
+        ptx::setmaxnreg_inc<kLaunchRegs>();
     } else {
+        ptx::setmaxnreg_inc<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax / epilogue
         // thread = (head row h, column half): columns [32*half, 32*half+32) of
         // every tile and [half*DC/2, (half+1)*DC/2) of q and o
@@ -421,11 +583,11 @@ attn_tc_kernel(const TcParams p) {
 
         uint32_t xrow_rem = 0, xfull_rem0 = 0, xfull_rem1 = 0, xempty_rem0 = 0, xempty_rem1 = 0;
         if constexpr (CL == 2) {
-            xrow_rem = ptx::map_to_rank(ptx::smem_u32(smem + C::OFF_X + h * 16), crank ^ 1u);
-            xfull_rem0 = ptx::map_to_rank(x_full(0), crank ^ 1u);
-            xfull_rem1 = ptx::map_to_rank(x_full(1), crank ^ 1u);
-            xempty_rem0 = ptx::map_to_rank(x_empty(0), crank ^ 1u);
-            xempty_rem1 = ptx::map_to_rank(x_empty(1), crank ^ 1u);
+            xrow_rem = ptx::map_to_rank(ptx::smem_u32(smem + C::OFF_X + h * 16), rank ^ 1u);
+            xfull_rem0 = ptx::map_to_rank(x_full(0), rank ^ 1u);
+            xfull_rem1 = ptx::map_to_rank(x_full(1), rank ^ 1u);
+            xempty_rem0 = ptx::map_to_rank(x_empty(0), rank ^ 1u);
+            xempty_rem1 = ptx::map_to_rank(x_empty(1), rank ^ 1u);
         }
         const uint32_t s_addr = lane_addr + C::S_COL + 32 * half;
         // read this thread's 32 partial logits of tile j (frees the S buffer)
@@ -604,7 +766,9 @@ attn_tc_kernel(const TcParams p) {
         }
         // ------------------------------------------------------------ epilogue
         if (tid == 0) SA_TRACE_POINT(3, 0, 2);
+        SA_CTA_POINT(2);
         if (ok) ok = wait_all(mma_done, 0);
+        if (tid == 0) SA_TRACE_POINT(3, 0, 4);
         float l_tot = l_run;
         if (ok) {
             red[2 * 256 + half * 128 + h] = l_run;
@@ -612,13 +776,14 @@ attn_tc_kernel(const TcParams p) {
             ok = wait_all(l_bar, 0);
             if (ok) l_tot = l_run + red[2 * 256 + (half ^ 1) * 128 + h];
         }
+        if (tid == 0) SA_TRACE_POINT(3, 0, 5);
         ptx::tc_fence_after();
         if (ok) {
-            // Output rows are staged in shared memory (the kv ring is idle once
-            // every MMA has completed) and then written with coalesced 16-byte
-            // stores, 512 contiguous bytes per warp instruction.  Staged row h
-            // holds this CTA's DC columns; its 16-byte chunk c sits at chunk
-            // position c ^ (h & 7), so the per-row writes are conflict-free.
+            // Output rows are staged in shared memory (the kv ring, receive
+            // buffers and index lists are dead once every MMA has completed)
+            // and then written out row by row.  Staged rows are linear with a
+            // 16-byte pad (stride STAGE_ROW), so the 16-byte writes of 32
+            // consecutive rows spread over all banks.
             const bool split_out = p.num_splits > 1;
             float f = 0.f, lse = -INFINITY;
             if (!split_out) {
@@ -634,30 +799,17 @@ attn_tc_kernel(const TcParams p) {
                 f = 1.f / l_tot;
                 lse = m_run + log2f(l_tot);
             }
-            const int rb = split_out ? DC * 4 : DC * 2;     // staged row bytes
             uint8_t *stage = smem + C::OFF_KV;
-            uint8_t *srow = stage + h * rb;
-#pragma unroll 1
-            for (int ch = 0; ch < DC / 64; ++ch) {
-                uint32_t r[32];
-                if (n_act > 0) {
-                    ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r);
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
-                }
+            uint8_t *srow = stage + h * C::STAGE_ROW;
+            auto stage_chunk = [&](const uint32_t (&r)[32], int ch) {
                 if (split_out) {
-                    const int c0 = (half * (DC / 2) + ch * 32) / 4;   // first 16-byte chunk
+                    float4 *d = reinterpret_cast<float4 *>(srow + (half * (DC / 2) + ch * 32) * 4);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float4 w = make_float4(__uint_as_float(r[4 * v]) * f, __uint_as_float(r[4 * v + 1]) * f,
-                                                     __uint_as_float(r[4 * v + 2]) * f,
-                                                     __uint_as_float(r[4 * v + 3]) * f);
-                        *reinterpret_cast<float4 *>(srow + (((c0 + v) ^ (h & 7)) * 16)) = w;
-                    }
+                    for (int v = 0; v < 8; ++v)
+                        d[v] = make_float4(__uint_as_float(r[4 * v]) * f, __uint_as_float(r[4 * v + 1]) * f,
+                                           __uint_as_float(r[4 * v + 2]) * f, __uint_as_float(r[4 * v + 3]) * f);
                 } else {
-                    const int c0 = (half * (DC / 2) + ch * 32) / 8;
+                    uint4 *d = reinterpret_cast<uint4 *>(srow + (half * (DC / 2) + ch * 32) * 2);
                     float dummy = 0.f;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -666,57 +818,122 @@ attn_tc_kernel(const TcParams p) {
                         w.y = pack_bf16(__uint_as_float(r[8 * v + 2]) * f, __uint_as_float(r[8 * v + 3]) * f, dummy);
                         w.z = pack_bf16(__uint_as_float(r[8 * v + 4]) * f, __uint_as_float(r[8 * v + 5]) * f, dummy);
                         w.w = pack_bf16(__uint_as_float(r[8 * v + 6]) * f, __uint_as_float(r[8 * v + 7]) * f, dummy);
-                        *reinterpret_cast<uint4 *>(srow + (((c0 + v) ^ (h & 7)) * 16)) = w;
+                        d[v] = w;
+                    }
+                }
+            };
+            // two 32-column TMEM loads share one wait
+#pragma unroll
+            for (int ch = 0; ch < DC / 64; ch += 2) {
+                constexpr int NCH = DC / 64;
+                uint32_t r0[32], r1[32];
+                if (n_act > 0) {
+                    ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r0);
+                    if (ch + 1 < NCH) ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + (ch + 1) * 32, r1);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
+                }
+                stage_chunk(r0, ch);
+                if (ch + 1 < NCH) stage_chunk(r1, ch + 1);
+            }
+            if (split_out && hv && half == 0) {
+                if (p.fused) reinterpret_cast<float *>(smem + C::OFF_LSE)[(split % 8) * kM + h] = lse;
+                if (crank == 0) p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
+            }
+            if (tid == 0) SA_TRACE_POINT(3, 0, 6);
+            ptx::mbar_arrive(epi_bar);
+            ok = wait_all(epi_bar, 0);
+            if (tid == 0) SA_TRACE_POINT(3, 0, 7);
+            if (ok) {
+                // Warp w writes rows [16w, 16w + 16) as coalesced 16-byte
+                // stores (512 contiguous bytes per warp instruction).  The
+                // (row, chunk) pairs are flattened and every lane issues 8
+                // shared-memory loads before its 8 stores, so the copy is not
+                // serialised on the load latency.  (One TMA bulk store per row
+                // measured slower: ~60 cycles per bulk operation.)
+                constexpr int kRowsPerWarp = kM / kSoftmaxWarps;
+                constexpr int kBatch = 8;
+                const int lg = split_out ? ptx_log2(DC * 4 / 16) : ptx_log2(DC * 2 / 16);   // log2 chunks per row
+                const int total = kRowsPerWarp << lg;
+                const int row0 = warp * kRowsPerWarp;
+                // fused splits combine rows [cr0, cr1) here: those stay in shared memory
+                int cr0 = 0, cr1 = 0;
+                if (p.fused) {
+                    const int rp = int((p.H + p.num_splits - 1) / p.num_splits);
+                    cr0 = split * rp;
+                    cr1 = cr0 + rp;
+                }
+                const int64_t row_bytes = split_out ? p.D * 4 : p.D * 2;
+                char *dst0 = split_out
+                    ? reinterpret_cast<char *>(p.ws_o + ((tok * p.num_splits + split) * p.H) * p.D + int64_t(crank) * DC)
+                    : reinterpret_cast<char *>(p.o + (tok * p.H) * p.D + int64_t(crank) * DC);
+                for (int base = 0; base < total; base += 32 * kBatch) {
+                    uint4 v[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int q = base + u * 32 + lane;
+                        const int r = row0 + (q >> lg), c = q & ((1 << lg) - 1);
+                        if (q < total && r < p.H && (r < cr0 || r >= cr1))
+                            v[u] = *reinterpret_cast<const uint4 *>(stage + r * C::STAGE_ROW + c * 16);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int q = base + u * 32 + lane;
+                        const int r = row0 + (q >> lg), c = q & ((1 << lg) - 1);
+                        if (q < total && r < p.H && (r < cr0 || r >= cr1))
+                            *reinterpret_cast<uint4 *>(dst0 + r * row_bytes + c * 16) = v[u];
                     }
                 }
             }
-            if (split_out && hv && crank == 0 && half == 0)
-                p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
-            ptx::mbar_arrive(epi_bar);
-            ok = wait_all(epi_bar, 0);
-            if (ok) {
-                // warp w copies rows [16w, 16w + 16)
-                const int nch = rb / 16;
-                for (int rr = 0; rr < kM / kSoftmaxWarps; ++rr) {
-                    const int row = warp * (kM / kSoftmaxWarps) + rr;
-                    if (row >= p.H) break;
-                    uint8_t *dst = split_out
-                        ? reinterpret_cast<uint8_t *>(p.ws_o + ((tok * p.num_splits + split) * p.H + row) * p.D +
-                                                      int64_t(crank) * DC)
-                        : reinterpret_cast<uint8_t *>(p.o + (tok * p.H + row) * p.D + int64_t(crank) * DC);
-                    const uint8_t *src = stage + row * rb;
-                    for (int c = lane; c < nch; c += 32)
-                        *reinterpret_cast<uint4 *>(dst + c * 16) =
-                            *reinterpret_cast<const uint4 *>(src + ((c ^ (row & 7)) * 16));
-                }
-            }
         }
+        ptx::setmaxnreg_dec<kLaunchRegs>();
     }
 
     // ---------------------------------------------------------------- teardown
     if (tid == 0) SA_TRACE_POINT(3, 0, 3);
     ptx::tc_fence_before();
     __syncthreads();
+    if (tid == 0) SA_TRACE_POINT(3, 0, 8);
     if (warp == kMmaWarp) {
         if (lane == 0) wait_bar(mma_done, 0);  // no MMA in flight before TMEM is released
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, C::TMEM_COLS);
     }
-    if constexpr (CL == 2) ptx::cluster_sync();  // no remote access outlives the partner
+    if (p.fused) {
+        // Every split of this token has published its partial rows and
+        // log-sum-exp (release/acquire at cluster scope); all partner
+        // exchanges are over too.  Split s now combines rows [s*rp, s*rp+rp)
+        // of this CTA's DC columns: its own partial from shared memory, the
+        // others' from L2, in the log-sum-exp form with the sink added once.
+        ptx::cluster_sync();
+        combine_rows<DC, C>(p, smem, tok, split, crank, tid);
+    } else if constexpr (CL == 2) {
+        ptx::cluster_sync();  // no remote access outlives the partner
+    }
+    if (tid == 0) SA_TRACE_POINT(3, 0, 9);
+    SA_CTA_POINT(3);
 }
 
 // Split-KV combine (§5.5, log-sum-exp form with the sink added exactly once):
 //   M = max(max_i lse_i, sink*log2e),  w_i = 2^(lse_i - M),
 //   o = sum_i w_i O_i / (sum_i w_i + 2^(sink*log2e - M)).
-// One warp per (token, head); each lane owns D/32 contiguous columns.
+// One warp per (token, head); lane l owns the 4-column groups l, l + 32, ...
+// so every warp load is 512 contiguous bytes.
 template <int D>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, const float *__restrict__ sink,
                     __nv_bfloat16 *__restrict__ o, int64_t rows, int64_t H, int ns) {
-    constexpr int E = D / 32;
+    constexpr int E = D / 32;              // columns per lane
+    constexpr int V = E >= 4 ? 4 : 2;      // columns per vector access
+    constexpr int G = E / V;               // vectors per lane
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);  // tok * H + h
+#ifdef SA_TRACE
+    if (threadIdx.x == 0) atomicMin(&g_sa_comb[0], sa_gtime());
+#endif
     if (row >= rows) return;
     const int64_t tok = row / H, h = row % H;
     const float *lse = ws_lse + tok * ns * H + h;
@@ -737,33 +954,57 @@ attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws
             if (li == -INFINITY) continue;
             const float w = exp2f(li - M);
             den += w;
-            const float *src = ws_o + ((tok * ns + i) * H + h) * D + lane * E;
+            const float *src = ws_o + ((tok * ns + i) * H + h) * D + lane * V;
 #pragma unroll
-            for (int e = 0; e < E; e += 2) {
-                const float2 v = *reinterpret_cast<const float2 *>(src + e);
-                acc[e] = fmaf(w, v.x, acc[e]);
-                acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+            for (int g = 0; g < G; ++g) {
+                if constexpr (V == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src + g * 128);
+                    acc[4 * g] = fmaf(w, v.x, acc[4 * g]);
+                    acc[4 * g + 1] = fmaf(w, v.y, acc[4 * g + 1]);
+                    acc[4 * g + 2] = fmaf(w, v.z, acc[4 * g + 2]);
+                    acc[4 * g + 3] = fmaf(w, v.w, acc[4 * g + 3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src + g * 64);
+                    acc[2 * g] = fmaf(w, v.x, acc[2 * g]);
+                    acc[2 * g + 1] = fmaf(w, v.y, acc[2 * g + 1]);
+                }
             }
         }
         den += exp2f(s2 - M);
     }
     const float f = zero ? 0.f : 1.f / den;
     const float fn = isnan(s2) ? NAN : f;
-    __nv_bfloat16 *dst = o + row * D + lane * E;
+    __nv_bfloat16 *dst = o + row * D + lane * V;
 #pragma unroll
-    for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(acc[e] * fn, acc[e + 1] * fn);
+    for (int g = 0; g < G; ++g) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[V * g] * fn, acc[V * g + 1] * fn);
+        if constexpr (V == 4) {
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[4 * g + 2] * fn, acc[4 * g + 3] * fn);
+            *reinterpret_cast<uint2 *>(dst + g * 128) =
+                make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+        } else {
+            *reinterpret_cast<__nv_bfloat162 *>(dst + g * 64) = lo;
+        }
+    }
+#ifdef SA_TRACE
+    if (lane == 0) atomicMax(&g_sa_comb[1], sa_gtime());
+#endif
 }
 
 // ---------------------------------------------------------------- host side
 
 constexpr int kMaxDev = 64;
 
+constexpr int kMaxFusedCluster = 8;   // portable cluster size
+
 template <int DC, int CL>
-cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream) {
+cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     using C = Cfg<DC, CL>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
+    // whether a cluster of n CTAs of this kernel can be resident (0 = not yet asked)
+    static std::once_flag fit_once[kMaxDev][kMaxFusedCluster + 1];
+    static int fits[kMaxDev][kMaxFusedCluster + 1];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -785,6 +1026,32 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream) {
     p.S = a.S; p.H = a.H; p.D = a.D; p.T = a.T; p.K = a.K;
     p.num_splits = a.num_splits;
     p.unit_slots = int(split_slots(a.K, a.num_splits));
+    // A token's splits are combined inside the kernel when they fit one
+    // portable cluster together with their head-dim halves.
+    const int cs_fused = CL * a.num_splits;
+    bool fused = a.num_splits > 1 && cs_fused <= kMaxFusedCluster;
+    if (fused) {
+        std::call_once(fit_once[dev][cs_fused], [&] {
+            cudaLaunchConfig_t q{};
+            q.gridDim = dim3(static_cast<unsigned>(cs_fused), 1, 1);
+            q.blockDim = dim3(C::THREADS, 1, 1);
+            q.dynamicSmemBytes = C::SMEM;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = static_cast<unsigned>(cs_fused);
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL>, &q);
+            fits[dev][cs_fused] = (qe == cudaSuccess && n >= 1) ? 1 : -1;
+            (void)cudaGetLastError();   // a refused query is not a launch error
+        });
+        fused = fits[dev][cs_fused] == 1;
+    }
+    p.fused = fused ? 1 : 0;
+    *fused_out = fused;
     p.scale_log2 = a.scale * kLog2e;
     if (p.unit_slots > kMaxUnitSlots) return cudaErrorInvalidValue;
 
@@ -796,7 +1063,7 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(fused ? cs_fused : CL);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -818,15 +1085,19 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stre
     (void)num_sms;
     if (a.B * a.S == 0) return cudaSuccess;
     cudaError_t e;
+    bool fused = false;
     switch (a.D) {
-        case 64: e = launch_tc<64, 1>(a, stream); break;
-        case 128: e = launch_tc<128, 1>(a, stream); break;
-        case 256: e = launch_tc<256, 1>(a, stream); break;
-        case 512: e = launch_tc<256, 2>(a, stream); break;
+        case 64: e = launch_tc<64, 1>(a, stream, &fused); break;
+        case 128: e = launch_tc<128, 1>(a, stream, &fused); break;
+        case 256: e = launch_tc<256, 1>(a, stream, &fused); break;
+        case 512: e = launch_tc<256, 2>(a, stream, &fused); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.num_splits > 1 && !fused) return launch_attn_combine(a, stream);
+    return cudaSuccess;
 }
 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
@@ -848,7 +1119,15 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
 extern "C" int sa_trace_read(long long *out) { return (int)cudaMemcpyFromSymbol(out, sa::g_sa_trace, sizeof(sa::g_sa_trace)); }
 extern "C" int sa_trace_clear() {
     static long long z[4 * 64 * 16] = {0};
+    static unsigned long long zc[4096 * 4] = {0};
+    unsigned long long comb[2] = {~0ull, 0ull};
+    cudaMemcpyToSymbol(sa::g_sa_cta, zc, sizeof(zc));
+    cudaMemcpyToSymbol(sa::g_sa_comb, comb, sizeof(comb));
     return (int)cudaMemcpyToSymbol(sa::g_sa_trace, z, sizeof(z));
+}
+extern "C" int sa_trace_read_cta(unsigned long long *cta, unsigned long long *comb) {
+    cudaMemcpyFromSymbol(comb, sa::g_sa_comb, sizeof(sa::g_sa_comb));
+    return (int)cudaMemcpyFromSymbol(cta, sa::g_sa_cta, sizeof(sa::g_sa_cta));
 }
 namespace sa {
 #endif

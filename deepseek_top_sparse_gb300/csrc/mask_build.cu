@@ -9,11 +9,14 @@
 // index of the row is OR-ed in with a shared-memory atomic, and the live words
 // go out with 16-byte stores.  The pages' Triton scatter ORs straight into
 // global memory; building in shared memory turns K scattered 4-byte global
-// atomics per row into ceil(keys/128) coalesced 16-byte stores, so the kernel
-// is bound by the streaming read of the indices.
+// atomics per row into ceil(keys/128) coalesced 16-byte stores (on GB300, L2
+// atomics measured 4x slower than shared-memory ones for this pattern).
 //   * rows of up to kWarpRowWords words: one WARP per row, each warp with its
-//     own image, so a CTA has 8 rows in flight and needs no CTA barrier; each
-//     lane keeps 8 16-byte index loads in flight before it ORs them in.
+//     own image, so a CTA has 8 rows in flight and needs no CTA barrier.  The
+//     row image is ORed with shared-memory atomics, whose bank conflicts on
+//     random words bound the kernel; narrow rows are sized for occupancy (32
+//     registers, 8 CTAs per SM), which measured faster than deep per-lane
+//     load queues.
 //   * wider rows up to kSmemWordsMax words: one CTA per row.
 //   * wider still: global atomics straight into the output row.
 #include "sa_internal.h"
@@ -25,7 +28,11 @@ constexpr int kMaskThreads = 256;
 constexpr int kMaskWarps = kMaskThreads / 32;
 constexpr int64_t kSmemWordsMax = 8192;  // 32 KB row image: up to 262144 keys
 constexpr int64_t kWarpRowWords = 2048;  // 8 KB image per warp: up to 65536 keys
-constexpr int kLoadsInFlight = 8;        // 16-byte index loads per lane per batch
+// Row images of up to kSmallRowWords words let 8 CTAs of 8 warps share an SM:
+// those rows take the 32-register variant with 2 16-byte index loads per lane
+// in flight; wider images limit occupancy anyway, so their variant keeps 8
+// loads per lane in flight instead.
+constexpr int64_t kSmallRowWords = 768;
 
 __device__ __forceinline__ void or_bit(uint32_t *img, int32_t k, uint32_t key_limit) {
     // (uint32_t)k < key_limit rejects negative and too-large indices at once
@@ -93,61 +100,70 @@ build_topk_mask_kernel(MaskArgs a, int64_t live_words, int smem_path) {
     }
 }
 
-__global__ void __launch_bounds__(kMaskThreads)
-build_topk_mask_warp_kernel(MaskArgs a, int64_t live_words) {
+// Arguments of the warp-per-row path, every count below 2^31 (the host checks)
+// so the kernel fits 32 registers and 8 CTAs per SM with no spills.
+struct WarpMaskArgs {
+    const int32_t *topk;
+    const int32_t *cu_q_lens;
+    const int32_t *key_starts;
+    uint32_t *mask;
+    int topk_rows, B, max_q_len, K, rows, words, live_words;
+    uint32_t key_limit;
+};
+
+template <int kLoadsInFlight, int kMinBlocks>
+__global__ void __launch_bounds__(kMaskThreads, kMinBlocks)
+build_topk_mask_warp_kernel(WarpMaskArgs a) {
     extern __shared__ __align__(16) uint32_t images[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t img_words = (live_words + 3) / 4 * 4;
+    const int img_words = (a.live_words + 3) / 4 * 4;
     uint32_t *img = images + warp * img_words;
-    const uint32_t key_limit = static_cast<uint32_t>(a.max_key_len);
 
     if (a.key_starts != nullptr && a.rows > 0) {
-        for (int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; b < a.B;
-             b += int64_t(gridDim.x) * blockDim.x)
-            a.mask[(b * a.rows) * a.words + (a.words - 1)] = static_cast<uint32_t>(a.key_starts[b]);
+        for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x)
+            a.mask[(int64_t(b) * a.rows) * a.words + (a.words - 1)] = static_cast<uint32_t>(a.key_starts[b]);
     }
 
-    const int64_t n_slots = a.B * a.max_q_len;
-    for (int64_t r = int64_t(blockIdx.x) * kMaskWarps + warp; r < n_slots;
-         r += int64_t(gridDim.x) * kMaskWarps) {
+    const int n_slots = a.B * a.max_q_len;
+    for (int r = blockIdx.x * kMaskWarps + warp; r < n_slots; r += gridDim.x * kMaskWarps) {
         // everything below is uniform across the warp
-        const int64_t b = r / a.max_q_len, q = r % a.max_q_len;
-        const int64_t c0 = a.cu_q_lens[b], c1 = a.cu_q_lens[b + 1];
+        const int b = r / a.max_q_len, q = r - b * a.max_q_len;
+        const int c0 = a.cu_q_lens[b], c1 = a.cu_q_lens[b + 1];
         if (q >= c1 - c0) continue;
-        const int64_t src = c0 + q;
+        const int64_t src = int64_t(c0) + q;
         if (src < 0 || src >= a.topk_rows) continue;
         const int32_t *row = a.topk + src * a.K;
-        uint32_t *dst = a.mask + (b * a.rows + q) * a.words;
+        uint32_t *dst = a.mask + (int64_t(b) * a.rows + q) * a.words;
 
-        for (int64_t w = lane; w < img_words; w += 32) img[w] = 0u;
+        for (int w = lane; w < img_words; w += 32) img[w] = 0u;
         __syncwarp();
         if ((a.K % 4 == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0)) {
             const int4 *r4 = reinterpret_cast<const int4 *>(row);
-            const int64_t n4 = a.K / 4;
-            for (int64_t base = 0; base < n4; base += 32 * kLoadsInFlight) {
+            const int n4 = a.K / 4;
+            for (int base = lane; base < n4; base += 32 * kLoadsInFlight) {
                 int4 x[kLoadsInFlight];
 #pragma unroll
                 for (int u = 0; u < kLoadsInFlight; ++u) {
-                    const int64_t v = base + u * 32 + lane;
+                    const int v = base + u * 32;
                     x[u] = v < n4 ? __ldcs(r4 + v) : make_int4(-1, -1, -1, -1);
                 }
 #pragma unroll
                 for (int u = 0; u < kLoadsInFlight; ++u) {
-                    or_bit(img, x[u].x, key_limit);
-                    or_bit(img, x[u].y, key_limit);
-                    or_bit(img, x[u].z, key_limit);
-                    or_bit(img, x[u].w, key_limit);
+                    or_bit(img, x[u].x, a.key_limit);
+                    or_bit(img, x[u].y, a.key_limit);
+                    or_bit(img, x[u].z, a.key_limit);
+                    or_bit(img, x[u].w, a.key_limit);
                 }
             }
         } else {
-            for (int64_t j = lane; j < a.K; j += 32) or_bit(img, __ldcs(row + j), key_limit);
+            for (int j = lane; j < a.K; j += 32) or_bit(img, __ldcs(row + j), a.key_limit);
         }
         __syncwarp();
-        const int64_t nvec = live_words / 4;
+        const int nvec = a.live_words / 4;
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);  // rows start on 16 B (words % 4 == 0)
         const uint4 *s4 = reinterpret_cast<const uint4 *>(img);
-        for (int64_t v = lane; v < nvec; v += 32) d4[v] = s4[v];
-        for (int64_t w = nvec * 4 + lane; w < live_words; w += 32) dst[w] = img[w];
+        for (int v = lane; v < nvec; v += 32) d4[v] = s4[v];
+        for (int w = nvec * 4 + lane; w < a.live_words; w += 32) dst[w] = img[w];
         __syncwarp();  // the image is reused by the warp's next row
     }
 }
@@ -160,17 +176,29 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
     const bool need_ks = a.key_starts != nullptr && a.rows > 0 && a.B > 0;
     if (n_slots == 0 && !need_ks) return cudaSuccess;
     const int64_t cap = int64_t(num_sms) * 8;
-    if (live_words <= kWarpRowWords) {
+    const int64_t lim31 = int64_t(1) << 31;
+    if (live_words <= kWarpRowWords && a.K < lim31 && a.topk_rows < lim31 && n_slots < lim31 &&
+        a.B + 1 < lim31 && a.rows < lim31 && a.words < lim31) {
+        WarpMaskArgs w;
+        w.topk = a.topk; w.cu_q_lens = a.cu_q_lens; w.key_starts = a.key_starts; w.mask = a.mask;
+        w.topk_rows = int(a.topk_rows); w.B = int(a.B); w.max_q_len = int(a.max_q_len); w.K = int(a.K);
+        w.rows = int(a.rows); w.words = int(a.words); w.live_words = int(live_words);
+        w.key_limit = static_cast<uint32_t>(a.max_key_len);
         const size_t smem = size_t(kMaskWarps) * size_t((live_words + 3) / 4 * 4) * sizeof(uint32_t);
-        if (smem > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(build_topk_mask_warp_kernel,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-            if (e != cudaSuccess) return e;
-        }
         int64_t grid = (n_slots + kMaskWarps - 1) / kMaskWarps;
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
-        build_topk_mask_warp_kernel<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(a, live_words);
+        if (live_words <= kSmallRowWords) {
+            build_topk_mask_warp_kernel<2, 8><<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(w);
+        } else {
+            auto kern = build_topk_mask_warp_kernel<8, 3>;
+            if (smem > 48 * 1024) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                if (e != cudaSuccess) return e;
+            }
+            kern<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(w);
+        }
         return cudaGetLastError();
     }
     const int smem_path = live_words <= kSmemWordsMax ? 1 : 0;

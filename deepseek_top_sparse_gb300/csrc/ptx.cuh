@@ -156,6 +156,33 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ------------------------------------------------------------- TMA
 
+// TMA bulk store of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to global memory, tracked by the issuing
+// thread's bulk-group state.
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// returns once every committed bulk store of this thread has read its source
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Warpgroup register reallocation: every warp of the warpgroup executes it.
+// An increase waits until other warpgroups have released enough registers of
+// the CTA's launch allocation.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Fetch of the 128-byte line holding addr into L2 (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void *addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

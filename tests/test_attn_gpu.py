@@ -110,6 +110,33 @@ def test_split_count_does_not_change_the_result():
         assert (o - outs[0]).abs().max().item() < 2e-2
 
 
+@pytest.mark.parametrize("H,D,K,T,ns,p", [
+    (100, 512, 700, 1500, 3, 0.1),    # 6-CTA cluster, rows split 34/34/32
+    (128, 512, 1152, 2000, 4, 0.0),   # 8-CTA cluster
+    (7, 512, 200, 300, 2, 0.3),       # fewer heads than splits x warps
+    (128, 256, 1024, 1500, 8, 0.1),   # one head-dim CTA, 8 splits in a cluster
+    (64, 64, 300, 500, 2, 0.2),
+    (128, 512, 1152, 2000, 5, 0.1),   # 10 CTAs: too many for a cluster, separate combine
+])
+def test_split_combine_paths(H, D, K, T, ns, p):
+    inp = workloads.random_attn(3, 2, H, D, T, K, p_invalid=p, seed=H + D + K + ns)
+    assert_close(run_gpu(inp, num_splits=ns), run_oracle(inp), f"H={H} D={D} K={K} splits={ns}")
+
+
+def test_split_with_no_active_tile_and_infinite_sinks():
+    # the last splits of token (0, 0) see only invalid slots; two heads have sink = +inf
+    inp = workloads.random_attn(2, 2, 128, 512, 1500, 1152, p_invalid=0.05, seed=31)
+    inp.topk_idxs[0, 0, 300:] = -1
+    inp.topk_idxs[1, 1, :700] = 5000     # out of range: the first splits are empty
+    inp.attn_sink[3] = math.inf
+    inp.attn_sink[77] = math.inf
+    inp.attn_sink[5] = -math.inf
+    for ns in (2, 3, 4):
+        o = run_gpu(inp, num_splits=ns)
+        assert torch.count_nonzero(o[:, :, 3]) == 0 and torch.count_nonzero(o[:, :, 77]) == 0
+        assert_close(o, run_oracle(inp), f"empty splits, splits={ns}")
+
+
 def test_deterministic():
     inp = workloads.random_attn(2, 2, 128, 512, 500, 300, p_invalid=0.1, seed=9)
     a, b = run_gpu(inp), run_gpu(inp)
