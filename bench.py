@@ -139,12 +139,13 @@ def _profile_traffic(kernel_tag: str, src_hash: str):
     return None
 
 
-KERNEL_SOURCES = ["deepseek_top_sparse_gb300/csrc/attn_tc.cu", "deepseek_top_sparse_gb300/csrc/attn_tc_kernel.cuh"]
+# the sources that define the sparse_attn kernel: a profile's traffic figure
+# is used only while their hash matches the one recorded with it
+KERNEL_SOURCES = ["deepseek_top_sparse_gb300/csrc/attn_tc.cu", "deepseek_top_sparse_gb300/csrc/ptx.cuh"]
 
 
 def _attn_kernel_sources():
-    return [p for p in KERNEL_SOURCES + ["deepseek_top_sparse_gb300/csrc/attn_simt.cu"]
-            if os.path.exists(os.path.join(ROOT, p))]
+    return [p for p in KERNEL_SOURCES if os.path.exists(os.path.join(ROOT, p))]
 
 
 def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None):
@@ -222,7 +223,7 @@ def run_gpu(args):
     ns = binding.sa_sparse_attn_num_splits(B, S, H, D, K)
     wsbuf = binding.workspace_for(B, S, H, D, K, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + (1 if ns > 1 else 0)
+    launches_per_step = binding.sa_sparse_attn_launch_count(B, S, H, D, K)
 
     def step():
         binding.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, out=out,

@@ -27,7 +27,8 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
-           "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws")
+           "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
+           "sa_sparse_attn_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_status_string.restype = ctypes.c_char_p
         lib.sa_sparse_attn_num_splits.argtypes = [i64] * 5
         lib.sa_sparse_attn_num_splits.restype = i32
+        lib.sa_sparse_attn_launch_count.argtypes = [i64] * 5 + [i32]
+        lib.sa_sparse_attn_launch_count.restype = i32
         lib.sa_sparse_attn_workspace_size.argtypes = [i64] * 5 + [i32]
         lib.sa_sparse_attn_workspace_size.restype = sz
         lib.sa_sparse_attn_fwd.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [p, sz, p]
@@ -86,6 +89,10 @@ def sa_status_string(code: int) -> str:
 
 def sa_sparse_attn_num_splits(B, S, H, D, K) -> int:
     return int(load().sa_sparse_attn_num_splits(B, S, H, D, K))
+
+
+def sa_sparse_attn_launch_count(B, S, H, D, K, num_splits=0) -> int:
+    return int(load().sa_sparse_attn_launch_count(B, S, H, D, K, num_splits))
 
 
 def sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits=0) -> int:

@@ -997,23 +997,59 @@ constexpr int kMaxDev = 64;
 
 constexpr int kMaxFusedCluster = 8;   // portable cluster size
 
+// Opt the kernel into its dynamic shared memory once per device.
 template <int DC, int CL>
-cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
+cudaError_t prepare_kernel(int dev) {
     using C = Cfg<DC, CL>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
-    // whether a cluster of n CTAs of this kernel can be resident (0 = not yet asked)
-    static std::once_flag fit_once[kMaxDev][kMaxFusedCluster + 1];
-    static int fits[kMaxDev][kMaxFusedCluster + 1];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [dev] {
         attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
     });
-    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    return attr_err[dev];
+}
+
+// Whether a token's ns splits are combined inside the kernel: they must fit
+// one portable cluster together with their head-dim halves, and such a
+// cluster must be placeable on this device (asked once per cluster size).
+template <int DC, int CL>
+bool fused_combine(int dev, int ns) {
+    using C = Cfg<DC, CL>;
+    static std::once_flag fit_once[kMaxDev][kMaxFusedCluster + 1];
+    static bool fits[kMaxDev][kMaxFusedCluster + 1];
+    const int cs = CL * ns;
+    if (ns < 2 || cs > kMaxFusedCluster || dev < 0 || dev >= kMaxDev) return false;
+    if (prepare_kernel<DC, CL>(dev) != cudaSuccess) return false;
+    std::call_once(fit_once[dev][cs], [dev, cs] {
+        cudaLaunchConfig_t q{};
+        q.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+        q.blockDim = dim3(C::THREADS, 1, 1);
+        q.dynamicSmemBytes = C::SMEM;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = static_cast<unsigned>(cs);
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL>, &q);
+        fits[dev][cs] = qe == cudaSuccess && n >= 1;
+        (void)cudaGetLastError();   // a refused query is not a launch error
+    });
+    return fits[dev][cs];
+}
+
+template <int DC, int CL>
+cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
+    using C = Cfg<DC, CL>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = prepare_kernel<DC, CL>(dev);
+    if (e != cudaSuccess) return e;
 
     TcParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -1026,30 +1062,8 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.S = a.S; p.H = a.H; p.D = a.D; p.T = a.T; p.K = a.K;
     p.num_splits = a.num_splits;
     p.unit_slots = int(split_slots(a.K, a.num_splits));
-    // A token's splits are combined inside the kernel when they fit one
-    // portable cluster together with their head-dim halves.
     const int cs_fused = CL * a.num_splits;
-    bool fused = a.num_splits > 1 && cs_fused <= kMaxFusedCluster;
-    if (fused) {
-        std::call_once(fit_once[dev][cs_fused], [&] {
-            cudaLaunchConfig_t q{};
-            q.gridDim = dim3(static_cast<unsigned>(cs_fused), 1, 1);
-            q.blockDim = dim3(C::THREADS, 1, 1);
-            q.dynamicSmemBytes = C::SMEM;
-            cudaLaunchAttribute qa[1];
-            qa[0].id = cudaLaunchAttributeClusterDimension;
-            qa[0].val.clusterDim.x = static_cast<unsigned>(cs_fused);
-            qa[0].val.clusterDim.y = 1;
-            qa[0].val.clusterDim.z = 1;
-            q.attrs = qa;
-            q.numAttrs = 1;
-            int n = 0;
-            const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL>, &q);
-            fits[dev][cs_fused] = (qe == cudaSuccess && n >= 1) ? 1 : -1;
-            (void)cudaGetLastError();   // a refused query is not a launch error
-        });
-        fused = fits[dev][cs_fused] == 1;
-    }
+    const bool fused = fused_combine<DC, CL>(dev, a.num_splits);
     p.fused = fused ? 1 : 0;
     *fused_out = fused;
     p.scale_log2 = a.scale * kLog2e;
@@ -1098,6 +1112,21 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stre
     if (e != cudaSuccess) return e;
     if (a.num_splits > 1 && !fused) return launch_attn_combine(a, stream);
     return cudaSuccess;
+}
+
+int kernels_per_call(int64_t D, int num_splits) {
+    if (num_splits <= 1) return 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    bool fused = false;
+    switch (D) {
+        case 64: fused = fused_combine<64, 1>(dev, num_splits); break;
+        case 128: fused = fused_combine<128, 1>(dev, num_splits); break;
+        case 256: fused = fused_combine<256, 1>(dev, num_splits); break;
+        case 512: fused = fused_combine<256, 2>(dev, num_splits); break;
+        default: return 0;
+    }
+    return fused ? 1 : 2;
 }
 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {

@@ -121,6 +121,15 @@ size_t sa_sparse_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D,
     return workspace_bytes_for(B, S, H, D, clamp_splits(K, splits));
 }
 
+int sa_sparse_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K, int num_splits) {
+    if (!attn_sizes_ok(B, S, H, D, K) || num_splits > 64) return 0;
+    if (B * S == 0) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev) != SA_OK) return 0;
+    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms));
+    return sa::kernels_per_call(D, splits);
+}
+
 sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
                                     const int32_t *topk_idxs, float softmax_scale, void *o,
                                     int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,

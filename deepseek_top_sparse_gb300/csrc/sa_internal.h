@@ -42,6 +42,9 @@ int max_unit_slots();
 
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream);
+// Kernels one sparse_attn call enqueues on the current device: 1, or 2 when
+// the splits are too many to combine inside the main kernel (0 on error).
+int kernels_per_call(int64_t D, int num_splits);
 
 struct MaskArgs {
     const int32_t *topk;

@@ -76,6 +76,15 @@ int sa_sparse_attn_num_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_
 size_t sa_sparse_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K,
                                      int num_splits);
 
+/* Kernels one sa_sparse_attn_fwd_splits call with these sizes enqueues on the
+ * current device: 1 when every token's splits fit one thread-block cluster
+ * (splits x head-dim halves <= 8 CTAs) and are combined inside the main
+ * kernel, 2 when a separate combine kernel follows.  Host-only; 0 on invalid
+ * sizes, B*S == 0, or a device this library does not support.  The pages have
+ * no counterpart of this query: it describes this library's launch plan, for
+ * callers that budget launches (CUDA graphs, launch-count accounting). */
+int sa_sparse_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K, int num_splits);
+
 /* o[b,s,h,:] = sum_j w_j * kv[b, topk_idxs[b,s,j], :] with
  *   x_j = softmax_scale * <q[b,s,h,:], kv[b, topk_idxs[b,s,j], :]>  (slot j valid),
  *   w   = softmax([x_0 .. x_{K-1}, attn_sink[h]])[0..K-1],

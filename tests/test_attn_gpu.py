@@ -137,6 +137,17 @@ def test_split_with_no_active_tile_and_infinite_sinks():
         assert_close(o, run_oracle(inp), f"empty splits, splits={ns}")
 
 
+def test_launch_count_query():
+    # splits x head-dim halves <= 8 CTAs combine in-kernel: one launch
+    assert binding.sa_sparse_attn_launch_count(32, 1, 128, 512, 1152, 2) == 1
+    assert binding.sa_sparse_attn_launch_count(32, 1, 128, 512, 1152, 4) == 1
+    assert binding.sa_sparse_attn_launch_count(32, 1, 128, 512, 1152, 5) == 2
+    assert binding.sa_sparse_attn_launch_count(32, 1, 128, 256, 1152, 8) == 1
+    assert binding.sa_sparse_attn_launch_count(32, 1, 128, 512, 1152, 1) == 1
+    assert binding.sa_sparse_attn_launch_count(0, 1, 128, 512, 1152, 2) == 0
+    assert binding.sa_sparse_attn_launch_count(1, 1, 128, 96, 1152, 2) == 0
+
+
 def test_deterministic():
     inp = workloads.random_attn(2, 2, 128, 512, 500, 300, p_invalid=0.1, seed=9)
     a, b = run_gpu(inp), run_gpu(inp)
