@@ -39,6 +39,7 @@
 // code and the kernel drains and returns instead of hanging.
 #include <cuda_bf16.h>
 
+#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -128,8 +129,13 @@ struct Cfg {
     static constexpr int OFF_LSE = OFF_RED + 3 * 2 * kM * 4;             // float [8 splits][128]
     static constexpr int OFF_BAR = OFF_LSE + 8 * kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
-    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar epi_bar
-    static constexpr int NUM_BARS = 2 * NS + 16;
+    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar epi_bar q_smem q_free
+    static constexpr int NUM_BARS = 2 * NS + 18;
+    // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
+    // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
+    static constexpr int OFF_QS = OFF_KV + (NS - 2) * STAGE_BYTES;
+    static constexpr int Q_BYTES = kM * DC * 2;
+    static_assert(Q_BYTES == 2 * STAGE_BYTES, "Q_c fills two kv stages");
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_TSLOT + 16 + 1024;    // + slack to align the base to 1 KB
     // TMEM columns: O_c fp32, S fp32 (one tile), P bf16 pairs (two tiles), Q_c bf16 pairs
@@ -221,12 +227,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float &sum) {
 }
 
 // In-cluster split combine for one CTA (see the kernel's teardown), run by
-// all C::THREADS threads.  Rows [cr0, cr1) of this CTA's DC columns:
-//   1. every split's log-sum-exp of those rows into a table (one L2 round
-//      trip for the whole CTA; this split's own values are already there),
-//   2. per row the final weights w_i / den (the combine kernel's formula),
-//   3. (row, 16-byte chunk) items spread over all threads, 4 per batch, so
-//      the partial loads of a batch are in flight together.
+// all C::THREADS threads.  Rows [cr0, cr1) of this CTA's DC columns; work
+// items are (row, 16-byte column chunk), kB per thread per batch.
+//   1. every split's log-sum-exp of those rows goes to a table, and, in the
+//      same round trip, each thread loads its first batch of partial chunks
+//      from the first other split (they do not depend on the weights);
+//   2. per row the final weights w_i / den (the combine kernel's formula);
+//   3. weighted sums: this split's own partial from shared memory, the others
+//      from L2, kB loads in flight per thread per split.
 template <int DC, typename C>
 __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int split,
                                              uint32_t crank, int tid) {
@@ -237,6 +245,20 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
     const int nrows = cr1 > cr0 ? cr1 - cr0 : 0;
     float *tab = reinterpret_cast<float *>(smem + C::OFF_LSE);   // [split][row]
     const uint8_t *stage = smem + C::OFF_KV;
+    constexpr int CH = DC / 4;     // float4 chunks per row
+    constexpr int kB = 8;
+    const int items = nrows * CH;
+    const int first_other = split == 0 ? 1 : 0;
+    auto partial = [&](int i, int it) {
+        const int r = cr0 + it / CH, c = it % CH;
+        return reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + r) * p.D + int64_t(crank) * DC) + c;
+    };
+    float4 pre[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+        const int it = tid + u * C::THREADS;
+        if (it < items) pre[u] = __ldcg(partial(first_other, it));
+    }
     for (int t = tid; t < ns * nrows; t += C::THREADS) {
         const int i = t / nrows, r = cr0 + t % nrows;
         if (i != split) tab[i * kM + r] = __ldcg(p.ws_lse + (tok * ns + i) * p.H + r);
@@ -265,24 +287,24 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
         }
     }
     __syncthreads();
-    constexpr int CH = DC / 4;     // float4 chunks per row
-    constexpr int kB = 4;
-    const int items = nrows * CH;
     for (int base = tid; base < items; base += kB * C::THREADS) {
         float4 acc[kB];
 #pragma unroll
         for (int u = 0; u < kB; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < ns; ++i) {
             float4 v[kB];
+            const bool preloaded = base == tid && i == first_other;
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
                 const int it = base + u * C::THREADS;
                 if (it < items) {
-                    const int r = cr0 + it / CH, c = it % CH;
-                    v[u] = i == split
-                        ? reinterpret_cast<const float4 *>(stage + r * C::STAGE_ROW)[c]
-                        : __ldcg(reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + r) * p.D +
-                                                                  int64_t(crank) * DC) + c);
+                    if (preloaded) {
+                        v[u] = pre[u];
+                    } else if (i == split) {
+                        v[u] = reinterpret_cast<const float4 *>(stage + (cr0 + it / CH) * C::STAGE_ROW)[it % CH];
+                    } else {
+                        v[u] = __ldcg(partial(i, it));
+                    }
                 }
             }
 #pragma unroll
@@ -313,7 +335,7 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
 
 template <int DC, int CL>
 __global__ void __launch_bounds__(Cfg<DC, CL>::THREADS, 1)
-attn_tc_kernel(const TcParams p) {
+attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     using C = Cfg<DC, CL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -354,18 +376,24 @@ attn_tc_kernel(const TcParams p) {
     const uint32_t red_bar = bar(2 * C::NS + 13);
     const uint32_t l_bar = bar(2 * C::NS + 14);
     const uint32_t epi_bar = bar(2 * C::NS + 15);
+    const uint32_t q_smem = bar(2 * C::NS + 16);   // Q_c landed in shared memory
+    const uint32_t q_free = bar(2 * C::NS + 17);   // Q_c copied to TMEM: its stages are free
 
     // ---------------------------------------------------------------- prologue
     if (tid == 0) SA_TRACE_POINT(3, 0, 0);
     SA_CTA_POINT(0);
-    if (warp < kSoftmaxWarps) {
-        // this thread's Q slice (loaded after the prologue) into L2 now
-        const int hq = (warp & 3) * 32 + lane;
-        if (hq < p.H) {
-            const char *qs = reinterpret_cast<const char *>(p.q + (tok * p.H + hq) * p.D + int64_t(crank) * DC +
-                                                            (warp >> 2) * (DC / 2));
+    // The index list heads the longest dependency chain (index -> kv row ->
+    // QK^T), so its loads go out first; every load of a thread is issued
+    // before the first is used.
+    constexpr int kWarpsAll = C::THREADS / 32;
+    constexpr int kSteps = (kMaxUnitSlots / 32 + kWarpsAll - 1) / kWarpsAll;
+    int32_t tv[kSteps];
+    {
+        const int32_t *irow = p.idx + tok * p.K + slot0;
 #pragma unroll
-            for (int o = 0; o < DC; o += 128) ptx::prefetch_l2(qs + o);
+        for (int u = 0; u < kSteps; ++u) {
+            const int j = (u * kWarpsAll + warp) * 32 + lane;
+            tv[u] = j < nslots ? __ldg(irow + j) : -1;
         }
     }
     if (warp == kMmaWarp) {
@@ -391,21 +419,20 @@ attn_tc_kernel(const TcParams p) {
         ptx::mbar_init(red_bar, kSoftmaxThreads);
         ptx::mbar_init(l_bar, kSoftmaxThreads);
         ptx::mbar_init(epi_bar, kSoftmaxThreads);
+        ptx::mbar_init(q_smem, 1);
+        ptx::mbar_init(q_free, kSoftmaxThreads);
         ptx::fence_mbar_init();
+        // Q_c of this unit: DC / 64 boxes of 128 head rows x 64 columns
+        ptx::mbar_arrive_expect_tx(q_smem, C::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < DC / 64; ++c)
+            ptx::tma_load_2d(ptx::smem_u32(smem + C::OFF_QS + c * (kM * 128)), &qmap, int32_t(crank) * DC + c * 64,
+                             int32_t(tok * p.H), q_smem);
+        SA_TRACE_POINT(3, 0, 10);
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
-    // mask per tile, 32 slots per warp step; every load of a thread is issued
-    // before the first is used, so the whole list costs one memory latency
+    // mask per tile, 32 slots per warp step
     {
-        constexpr int kWarpsAll = C::THREADS / 32;
-        constexpr int kSteps = (kMaxUnitSlots / 32 + kWarpsAll - 1) / kWarpsAll;
-        const int32_t *irow = p.idx + tok * p.K + slot0;
-        int32_t tv[kSteps];
-#pragma unroll
-        for (int u = 0; u < kSteps; ++u) {
-            const int j = (u * kWarpsAll + warp) * 32 + lane;
-            tv[u] = j < nslots ? __ldg(irow + j) : -1;
-        }
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int ch = u * kWarpsAll + warp;
@@ -418,12 +445,17 @@ attn_tc_kernel(const TcParams p) {
             }
         }
     }
+    if (tid == 0) SA_TRACE_POINT(3, 0, 11);
     __syncthreads();
-    if (tid == 0) {
-        int n = 0;
-        for (int t = 0; t < ntiles; ++t)
-            if (vmask[t] != 0) act[n++] = t;
-        act[kMaxUnitTiles] = n;
+    if (tid == 0) SA_TRACE_POINT(3, 0, 12);
+    if (warp == 0) {
+        // list of tiles with a valid slot, in order (ntiles <= 32: one warp)
+        static_assert(kMaxUnitTiles <= 32, "one lane per tile");
+        const bool live = lane < ntiles && vmask[lane] != 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, live);
+        if (live) act[__popc(bal & ((1u << lane) - 1u))] = lane;
+        if (lane == 0) act[kMaxUnitTiles] = __popc(bal);
+        if (lane == 0) SA_TRACE_POINT(3, 0, 13);
     }
     ptx::tc_fence_before();
     if constexpr (CL == 2) {
@@ -432,6 +464,7 @@ attn_tc_kernel(const TcParams p) {
         __syncthreads();
     }
     ptx::tc_fence_after();
+    if (tid == 0) SA_TRACE_POINT(3, 0, 14);
     const uint32_t tbase = *tslot;
     const int n_act = act[kMaxUnitTiles];
     if (tid == 0) SA_TRACE_POINT(3, 0, 1);
@@ -461,10 +494,18 @@ attn_tc_kernel(const TcParams p) {
                     ok = false;
                     break;
                 }
+                // the last two stages hold Q_c until the softmax warps copied it
+                if (a == C::NS - 2 && !wait_all(q_free, 0)) {
+                    ok = false;
+                    break;
+                }
                 if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
                 const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
                 const int32_t *rc = rowc + act[a] * kBN;
-    #pragma unroll
+                    // unrolled by 2 only: the first tile runs this code cold (the
+                // instruction cache misses of a fully unrolled body cost more
+                // than the loop)
+#pragma unroll 2
                 for (int i = 0; i < ITERS; ++i) {
                     const int r = i * STEP + g * RPI + sub;   // warp g: row groups g, g + G, ...
                     if (STEP * ITERS > kBN && r >= kBN) break;
@@ -546,17 +587,24 @@ attn_tc_kernel(const TcParams p) {
         const uint32_t lane_addr = tbase + (uint32_t(quarter * 32) << 16);
         const bool hv = h < p.H;
         {
-            // this thread's half of Q_c into TMEM (bf16 pairs, DC/4 columns)
+            // this thread's half of Q_c (DC/2 columns of row h) from the TMA
+            // boxes into TMEM (bf16 pairs, DC/4 columns).  16-byte unit u of
+            // the row sits in box u/8 at unit position (u%8) ^ (h&7).
             constexpr int QW = DC / 4;
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + (tok * p.H + (hv ? h : 0)) * p.D +
-                                                                int64_t(crank) * DC + half * (DC / 2));
+            const bool qok = wait_all(q_smem, 0);
+            const uint8_t *qs = smem + C::OFF_QS + h * 128;
+            auto qunit = [&](int u) -> uint4 {
+                if (!hv || !qok) return make_uint4(0u, 0u, 0u, 0u);
+                return *reinterpret_cast<const uint4 *>(qs + (u >> 3) * (kM * 128) + (((u & 7) ^ (h & 7)) << 4));
+            };
+            const int u0 = half * (DC / 16);
             if constexpr (QW >= 32) {
 #pragma unroll
                 for (int c = 0; c < QW / 32; ++c) {
                     uint32_t v[32];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const uint4 x = hv ? __ldg(qrow + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 x = qunit(u0 + c * 8 + i);
                         v[4 * i] = x.x;
                         v[4 * i + 1] = x.y;
                         v[4 * i + 2] = x.z;
@@ -568,7 +616,7 @@ attn_tc_kernel(const TcParams p) {
                 uint32_t v[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 x = hv ? __ldg(qrow + i) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 x = qunit(u0 + i);
                     v[4 * i] = x.x;
                     v[4 * i + 1] = x.y;
                     v[4 * i + 2] = x.z;
@@ -576,9 +624,11 @@ attn_tc_kernel(const TcParams p) {
                 }
                 ptx::tmem_st16(lane_addr + C::Q_COL + half * QW, v);
             }
+            ptx::mbar_arrive(q_free);   // the two kv stages holding Q_c may be refilled
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(q_ready);
+            if (tid == 0) SA_TRACE_POINT(2, 0, 11);
         }
 
         uint32_t xrow_rem = 0, xfull_rem0 = 0, xfull_rem1 = 0, xempty_rem0 = 0, xempty_rem1 = 0;
@@ -909,6 +959,7 @@ attn_tc_kernel(const TcParams p) {
         // of this CTA's DC columns: its own partial from shared memory, the
         // others' from L2, in the log-sum-exp form with the sink added once.
         ptx::cluster_sync();
+        if (tid == 0) SA_TRACE_POINT(3, 0, 15);
         combine_rows<DC, C>(p, smem, tok, split, crank, tid);
     } else if constexpr (CL == 2) {
         ptx::cluster_sync();  // no remote access outlives the partner
@@ -997,6 +1048,38 @@ constexpr int kMaxDev = 64;
 
 constexpr int kMaxFusedCluster = 8;   // portable cluster size
 
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// q viewed as [tokens * H rows][D columns] bf16; boxes of 128 rows x 64
+// columns (128 B), 128B-swizzled, rows past the end read as zeros.
+cudaError_t encode_q_map(CUtensorMap *m, const AttnArgs &a) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.B * a.S * a.H)};
+    cuuint64_t strides[1] = {cuuint64_t(a.D) * 2};
+    cuuint32_t box[2] = {64, cuuint32_t(kM)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.q), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Opt the kernel into its dynamic shared memory once per device.
 template <int DC, int CL>
 cudaError_t prepare_kernel(int dev) {
@@ -1007,6 +1090,12 @@ cudaError_t prepare_kernel(int dev) {
     std::call_once(attr_once[dev], [dev] {
         attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM);
+        // The warpgroups' setmaxnreg split is drawn from the launch allocation;
+        // a build that launched with fewer registers per thread could never
+        // satisfy the softmax warpgroups' increase, so it is not launched.
+        cudaFuncAttributes fa{};
+        if (attr_err[dev] == cudaSuccess) attr_err[dev] = cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL>);
+        if (attr_err[dev] == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err[dev] = cudaErrorInvalidConfiguration;
     });
     return attr_err[dev];
 }
@@ -1082,7 +1171,10 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL>, p);
+    CUtensorMap qmap;
+    e = encode_q_map(&qmap, a);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL>, p, qmap);
 }
 
 }  // namespace

@@ -140,6 +140,7 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
     if (num_splits > 64) return SA_ERR_INVALID_ARG;
     if (!attn_sizes_ok(B, S, H, D, K) || T < 1) return SA_ERR_SHAPE;
     if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;   // q rows are 32-bit tensor-map coordinates
     if (B * S == 0) return SA_OK;
     if (!q || !kv || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return SA_ERR_ALIGNMENT;

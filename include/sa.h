@@ -100,7 +100,7 @@ int sa_sparse_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int6
  *   workspace  >= sa_sparse_attn_workspace_size(B,S,H,D,K,0) bytes, 256-byte
  *              aligned; may be NULL when that size is 0.
  * Supported sizes: 1 <= H <= 128, D in {64, 128, 256, 512}, K >= 1,
- * B*S >= 0 (0 launches nothing), T >= 1, B*T < 2^31.
+ * B*S >= 0 (0 launches nothing), T >= 1, B*T < 2^31, B*S*H < 2^31.
  * Computes in bf16 x bf16 -> fp32 on the tensor cores (tcgen05), softmax in
  * fp32, probabilities rounded to bf16 before P.V, output rounded to bf16. */
 sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_sink,

@@ -83,6 +83,7 @@ def test_attn_validation_happens_before_any_device_work():
     assert _fwd(K=0) == 2
     assert _fwd(T=0) == 2
     assert _fwd(B=1 << 20, T=1 << 12) == 2  # B*T >= 2^31
+    assert _fwd(B=1 << 17, S=1 << 7, H=128, T=1) == 2  # B*S*H >= 2^31
     assert _fwd(B=-1) == 1
     assert _fwd(softmax_scale=float("nan")) == 1
     assert _fwd(num_splits=65) == 1
