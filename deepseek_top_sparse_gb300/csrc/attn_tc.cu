@@ -129,7 +129,7 @@ struct Cfg {
     static constexpr int OFF_LSE = OFF_RED + 3 * 2 * kM * 4;             // float [8 splits][128]
     static constexpr int OFF_BAR = OFF_LSE + 8 * kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
-    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar epi_bar q_smem q_free
+    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar (spare) q_smem q_free
     static constexpr int NUM_BARS = 2 * NS + 18;
     // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
     // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
@@ -226,49 +226,99 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float &sum) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Rows a split combines inside the cluster: [split * rp, split * rp + rp) with
+// rp = ceil(H / splits), clipped to H.
+__device__ __forceinline__ void combine_range(const TcParams &p, int split, int &cr0, int &cr1) {
+    const int rp = int((p.H + p.num_splits - 1) / p.num_splits);
+    cr0 = split * rp;
+    cr1 = cr0 + rp < p.H ? cr0 + rp : int(p.H);
+}
+
+// Staged output rows to global memory, by all C::THREADS threads: thread t
+// copies 16-byte chunk t % CHK of rows t / CHK, t / CHK + THREADS / CHK, ...
+// (each warp instruction covers 512 contiguous bytes), 8 shared-memory loads
+// in flight before their stores.  Non-split: bf16 rows of o.  Split: fp32
+// partial rows of the workspace, except (fused) the rows this split combines
+// itself.  (One TMA bulk store per row measured slower: ~60 cycles per bulk
+// operation.)
+template <int DC, typename C>
+__device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *smem, int64_t tok, int split,
+                                              uint32_t crank, int tid) {
+    const bool split_out = p.num_splits > 1;
+    int cr0 = 0, cr1 = 0;
+    if (p.fused) combine_range(p, split, cr0, cr1);
+    const int chk = split_out ? DC * 4 / 16 : DC * 2 / 16;         // 16-byte chunks per row
+    const int rows_per_pass = C::THREADS / chk;
+    const int c = tid % chk;
+    const int r0 = tid / chk;
+    const int64_t row_bytes = split_out ? p.D * 4 : p.D * 2;
+    char *dst = split_out
+        ? reinterpret_cast<char *>(p.ws_o + ((tok * p.num_splits + split) * p.H) * p.D + int64_t(crank) * DC)
+        : reinterpret_cast<char *>(p.o + (tok * p.H) * p.D + int64_t(crank) * DC);
+    dst += c * 16;
+    const uint8_t *src = smem + C::OFF_KV + c * 16;
+    constexpr int kBatch = 8;
+    for (int rb = r0; rb < kM; rb += kBatch * rows_per_pass) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int r = rb + u * rows_per_pass;
+            if (r < p.H && (r < cr0 || r >= cr1)) v[u] = *reinterpret_cast<const uint4 *>(src + r * C::STAGE_ROW);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int r = rb + u * rows_per_pass;
+            if (r < p.H && (r < cr0 || r >= cr1)) *reinterpret_cast<uint4 *>(dst + r * row_bytes) = v[u];
+        }
+    }
+}
+
 // In-cluster split combine for one CTA (see the kernel's teardown), run by
-// all C::THREADS threads.  Rows [cr0, cr1) of this CTA's DC columns; work
-// items are (row, 16-byte column chunk), kB per thread per batch.
-//   1. every split's log-sum-exp of those rows goes to a table, and, in the
-//      same round trip, each thread loads its first batch of partial chunks
-//      from the first other split (they do not depend on the weights);
+// all C::THREADS threads, over rows [cr0, cr1) of this CTA's DC columns.
+// Thread t owns float4 column chunk t % CH of rows cr0 + t / CH + k * RP
+// (RP = THREADS / CH rows per pass), so one base pointer per split serves
+// all its loads.
+//   1. each thread loads its partial chunks from the first other split and,
+//      for the weights, its row's sink (the lse table was filled through
+//      distributed shared memory before the cluster barrier);
 //   2. per row the final weights w_i / den (the combine kernel's formula);
-//   3. weighted sums: this split's own partial from shared memory, the others
-//      from L2, kB loads in flight per thread per split.
+//   3. weighted sums, 4 passes at a time: this split's own partial from
+//      shared memory, the others from L2 (the first batch of the first other
+//      split was loaded in step 1).
 template <int DC, typename C>
 __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int split,
                                              uint32_t crank, int tid) {
     const int ns = p.num_splits;
-    const int rp = int((p.H + ns - 1) / ns);
-    const int cr0 = split * rp;
-    const int cr1 = cr0 + rp < p.H ? cr0 + rp : int(p.H);
+    int cr0, cr1;
+    combine_range(p, split, cr0, cr1);
     const int nrows = cr1 > cr0 ? cr1 - cr0 : 0;
     float *tab = reinterpret_cast<float *>(smem + C::OFF_LSE);   // [split][row]
-    const uint8_t *stage = smem + C::OFF_KV;
-    constexpr int CH = DC / 4;     // float4 chunks per row
-    constexpr int kB = 8;
-    const int items = nrows * CH;
+    constexpr int CH = DC / 4;                 // float4 chunks per row
+    constexpr int RP = C::THREADS / CH;        // rows per pass
+    constexpr int kB = 4;                      // passes per batch
+    static_assert(C::THREADS % CH == 0 && kM <= C::THREADS, "thread -> (row, chunk) map");
+    const int c = tid % CH;
+    const int rt = cr0 + tid / CH;             // this thread's first row
     const int first_other = split == 0 ? 1 : 0;
-    auto partial = [&](int i, int it) {
-        const int r = cr0 + it / CH, c = it % CH;
-        return reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + r) * p.D + int64_t(crank) * DC) + c;
+    auto part = [&](int i) {                   // split i's chunk c of row rt
+        return reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + rt) * p.D + int64_t(crank) * DC) + c;
     };
+    const int64_t pass_f4 = int64_t(RP) * p.D / 4;   // float4 stride between passes
     float4 pre[kB];
+    {
+        const float4 *src = part(first_other);
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
-        const int it = tid + u * C::THREADS;
-        if (it < items) pre[u] = __ldcg(partial(first_other, it));
+        for (int u = 0; u < kB; ++u)
+            if (rt + u * RP < cr1) pre[u] = __ldcg(src + u * pass_f4);
     }
-    for (int t = tid; t < ns * nrows; t += C::THREADS) {
-        const int i = t / nrows, r = cr0 + t % nrows;
-        if (i != split) tab[i * kM + r] = __ldcg(p.ws_lse + (tok * ns + i) * p.H + r);
-    }
-    __syncthreads();
-    for (int t = tid; t < nrows; t += C::THREADS) {
-        const int r = cr0 + t;
+    const float sink_r = tid < nrows ? p.sink[cr0 + tid] : 0.f;
+    if (tid == 0) SA_TRACE_POINT(1, 60, 0);
+    // (pre holds passes 0..kB-1 of the first other split)
+    if (tid < nrows) {
+        const int r = cr0 + tid;
         float mx = -INFINITY;
         for (int i = 0; i < ns; ++i) mx = fmaxf(mx, tab[i * kM + r]);
-        const float s2 = p.sink[r] * kLog2e;
+        const float s2 = sink_r * kLog2e;
         const float M = fmaxf(mx, s2);
         const bool zero = (s2 == INFINITY) || (M == -INFINITY);
         float den = 0.f;
@@ -286,32 +336,36 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
             tab[i * kM + r] = (zero || li == -INFINITY) ? 0.f * fn : exp2f(li - M) * fn;
         }
     }
+    if (tid == 0) SA_TRACE_POINT(1, 60, 1);
     __syncthreads();
-    for (int base = tid; base < items; base += kB * C::THREADS) {
+    const uint8_t *own = smem + C::OFF_KV + rt * C::STAGE_ROW + c * 16;
+    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (tok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
+    const int64_t pass_u2 = int64_t(RP) * p.D / 4;
+    for (int k0 = 0; rt + k0 * RP < cr1; k0 += kB) {
         float4 acc[kB];
 #pragma unroll
         for (int u = 0; u < kB; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < ns; ++i) {
             float4 v[kB];
-            const bool preloaded = base == tid && i == first_other;
+            if (i == first_other && k0 == 0) {
 #pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int it = base + u * C::THREADS;
-                if (it < items) {
-                    if (preloaded) {
-                        v[u] = pre[u];
-                    } else if (i == split) {
-                        v[u] = reinterpret_cast<const float4 *>(stage + (cr0 + it / CH) * C::STAGE_ROW)[it % CH];
-                    } else {
-                        v[u] = __ldcg(partial(i, it));
-                    }
-                }
+                for (int u = 0; u < kB; ++u) v[u] = pre[u];
+            } else if (i == split) {
+#pragma unroll
+                for (int u = 0; u < kB; ++u)
+                    if (rt + (k0 + u) * RP < cr1)
+                        v[u] = *reinterpret_cast<const float4 *>(own + (k0 + u) * RP * C::STAGE_ROW);
+            } else {
+                const float4 *src = part(i);
+#pragma unroll
+                for (int u = 0; u < kB; ++u)
+                    if (rt + (k0 + u) * RP < cr1) v[u] = __ldcg(src + (k0 + u) * pass_f4);
             }
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-                const int it = base + u * C::THREADS;
-                if (it < items) {
-                    const float w = tab[i * kM + cr0 + it / CH];
+                const int r = rt + (k0 + u) * RP;
+                if (r < cr1) {
+                    const float w = tab[i * kM + r];
                     acc[u].x = fmaf(w, v[u].x, acc[u].x);
                     acc[u].y = fmaf(w, v[u].y, acc[u].y);
                     acc[u].z = fmaf(w, v[u].z, acc[u].z);
@@ -321,12 +375,10 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
         }
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
-            const int it = base + u * C::THREADS;
-            if (it < items) {
-                const int r = cr0 + it / CH, c = it % CH;
+            if (rt + (k0 + u) * RP < cr1) {
                 const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
                 const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-                reinterpret_cast<uint2 *>(p.o + (tok * p.H + r) * p.D + int64_t(crank) * DC)[c] =
+                dst[(k0 + u) * pass_u2] =
                     make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
             }
         }
@@ -375,7 +427,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     const uint32_t mma_done = bar(2 * C::NS + 12);
     const uint32_t red_bar = bar(2 * C::NS + 13);
     const uint32_t l_bar = bar(2 * C::NS + 14);
-    const uint32_t epi_bar = bar(2 * C::NS + 15);
     const uint32_t q_smem = bar(2 * C::NS + 16);   // Q_c landed in shared memory
     const uint32_t q_free = bar(2 * C::NS + 17);   // Q_c copied to TMEM: its stages are free
 
@@ -418,7 +469,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         ptx::mbar_init(mma_done, 1);
         ptx::mbar_init(red_bar, kSoftmaxThreads);
         ptx::mbar_init(l_bar, kSoftmaxThreads);
-        ptx::mbar_init(epi_bar, kSoftmaxThreads);
         ptx::mbar_init(q_smem, 1);
         ptx::mbar_init(q_free, kSoftmaxThreads);
         ptx::fence_mbar_init();
@@ -889,54 +939,19 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 if (ch + 1 < NCH) stage_chunk(r1, ch + 1);
             }
             if (split_out && hv && half == 0) {
-                if (p.fused) reinterpret_cast<float *>(smem + C::OFF_LSE)[(split % 8) * kM + h] = lse;
-                if (crank == 0) p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
+                if (p.fused) {
+                    // this split's lse of row h into the lse table of every
+                    // split CTA with the same head-dim half (cluster rank
+                    // s * CL + crank); the teardown's cluster barrier orders it
+                    const uint32_t slot =
+                        ptx::smem_u32(smem + C::OFF_LSE + ((split % 8) * kM + h) * 4);
+                    for (int s2 = 0; s2 < p.num_splits; ++s2)
+                        ptx::st_cluster_b32(ptx::map_to_rank(slot, uint32_t(s2 * CL) + crank), __float_as_uint(lse));
+                } else if (crank == 0) {
+                    p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
+                }
             }
             if (tid == 0) SA_TRACE_POINT(3, 0, 6);
-            ptx::mbar_arrive(epi_bar);
-            ok = wait_all(epi_bar, 0);
-            if (tid == 0) SA_TRACE_POINT(3, 0, 7);
-            if (ok) {
-                // Warp w writes rows [16w, 16w + 16) as coalesced 16-byte
-                // stores (512 contiguous bytes per warp instruction).  The
-                // (row, chunk) pairs are flattened and every lane issues 8
-                // shared-memory loads before its 8 stores, so the copy is not
-                // serialised on the load latency.  (One TMA bulk store per row
-                // measured slower: ~60 cycles per bulk operation.)
-                constexpr int kRowsPerWarp = kM / kSoftmaxWarps;
-                constexpr int kBatch = 8;
-                const int lg = split_out ? ptx_log2(DC * 4 / 16) : ptx_log2(DC * 2 / 16);   // log2 chunks per row
-                const int total = kRowsPerWarp << lg;
-                const int row0 = warp * kRowsPerWarp;
-                // fused splits combine rows [cr0, cr1) here: those stay in shared memory
-                int cr0 = 0, cr1 = 0;
-                if (p.fused) {
-                    const int rp = int((p.H + p.num_splits - 1) / p.num_splits);
-                    cr0 = split * rp;
-                    cr1 = cr0 + rp;
-                }
-                const int64_t row_bytes = split_out ? p.D * 4 : p.D * 2;
-                char *dst0 = split_out
-                    ? reinterpret_cast<char *>(p.ws_o + ((tok * p.num_splits + split) * p.H) * p.D + int64_t(crank) * DC)
-                    : reinterpret_cast<char *>(p.o + (tok * p.H) * p.D + int64_t(crank) * DC);
-                for (int base = 0; base < total; base += 32 * kBatch) {
-                    uint4 v[kBatch];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int q = base + u * 32 + lane;
-                        const int r = row0 + (q >> lg), c = q & ((1 << lg) - 1);
-                        if (q < total && r < p.H && (r < cr0 || r >= cr1))
-                            v[u] = *reinterpret_cast<const uint4 *>(stage + r * C::STAGE_ROW + c * 16);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int q = base + u * 32 + lane;
-                        const int r = row0 + (q >> lg), c = q & ((1 << lg) - 1);
-                        if (q < total && r < p.H && (r < cr0 || r >= cr1))
-                            *reinterpret_cast<uint4 *>(dst0 + r * row_bytes + c * 16) = v[u];
-                    }
-                }
-            }
         }
         ptx::setmaxnreg_dec<kLaunchRegs>();
     }
@@ -952,6 +967,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, C::TMEM_COLS);
     }
+    // the staged rows leave (all warps); a fused split keeps its own combine rows
+    copy_out_rows<DC, C>(p, smem, tok, split, crank, tid);
+    if (tid == 0) SA_TRACE_POINT(3, 0, 7);
     if (p.fused) {
         // Every split of this token has published its partial rows and
         // log-sum-exp (release/acquire at cluster scope); all partner
