@@ -127,7 +127,8 @@ struct Cfg {
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
     static constexpr int OFF_RED = OFF_LIST + kMaxUnitTiles * 4 + 16;   // float [3][2][128]
     static constexpr int OFF_LSE = OFF_RED + 3 * 2 * kM * 4;             // float [8 splits][128]
-    static constexpr int OFF_BAR = OFF_LSE + 8 * kM * 4;
+    static constexpr int OFF_SINK = OFF_LSE + 8 * kM * 4;                // float [128]
+    static constexpr int OFF_BAR = OFF_SINK + kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
     // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar (spare) q_smem q_free
     static constexpr int NUM_BARS = 2 * NS + 18;
@@ -311,7 +312,7 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
         for (int u = 0; u < kB; ++u)
             if (rt + u * RP < cr1) pre[u] = __ldcg(src + u * pass_f4);
     }
-    const float sink_r = tid < nrows ? p.sink[cr0 + tid] : 0.f;
+    const float sink_r = tid < nrows ? reinterpret_cast<const float *>(smem + C::OFF_SINK)[cr0 + tid] : 0.f;
     if (tid == 0) SA_TRACE_POINT(1, 60, 0);
     // (pre holds passes 0..kB-1 of the first other split)
     if (tid < nrows) {
@@ -439,6 +440,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     constexpr int kWarpsAll = C::THREADS / 32;
     constexpr int kSteps = (kMaxUnitSlots / 32 + kWarpsAll - 1) / kWarpsAll;
     int32_t tv[kSteps];
+    float *sink_tab = reinterpret_cast<float *>(smem + C::OFF_SINK);
+    const float sink_t = tid < p.H ? __ldg(p.sink + tid) : 0.f;   // into sink_tab below
     {
         const int32_t *irow = p.idx + tok * p.K + slot0;
 #pragma unroll
@@ -495,6 +498,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             }
         }
     }
+    if (tid < kM) sink_tab[tid] = sink_t;
     if (tid == 0) SA_TRACE_POINT(3, 0, 11);
     __syncthreads();
     if (tid == 0) SA_TRACE_POINT(3, 0, 12);
@@ -508,11 +512,13 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         if (lane == 0) SA_TRACE_POINT(3, 0, 13);
     }
     ptx::tc_fence_before();
-    if constexpr (CL == 2) {
-        ptx::cluster_sync();  // partner barriers initialised before any remote access
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
+    // Other CTAs of the cluster must have initialised their barriers and be
+    // running before this CTA's first remote access: every thread arrives now
+    // and waits only just before its first remote access (the softmax warps)
+    // or before the teardown's cluster barrier (the others).
+    const bool clustered = CL == 2 || p.fused;
+    if (clustered) ptx::cluster_arrive_relaxed();
     ptx::tc_fence_after();
     if (tid == 0) SA_TRACE_POINT(3, 0, 14);
     const uint32_t tbase = *tslot;
@@ -624,6 +630,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 ptx::mma_commit(mma_done);
             }
         }
+        if (clustered) ptx::cluster_wait();
         // back to the launch allocation: the teardown below is common code
         ptx::setmaxnreg_inc<kLaunchRegs>();
     } else {
@@ -740,6 +747,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         const bool pos_scale = p.scale_log2 >= 0.f;
         float m_run = -INFINITY, l_run = 0.f;
         uint32_t cur[32], nxt[32];
+        if (clustered) ptx::cluster_wait();   // before the first remote access
         if (n_act > 0) ok = take(0, cur);
         int a = 0;
         for (; ok && a < n_act; ++a) {
@@ -887,7 +895,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             const bool split_out = p.num_splits > 1;
             float f = 0.f, lse = -INFINITY;
             if (!split_out) {
-                const float s2 = hv ? p.sink[h] * kLog2e : 0.f;
+                const float s2 = hv ? sink_tab[h] * kLog2e : 0.f;
                 if (n_act > 0 && s2 != INFINITY) {
                     const float M = fmaxf(m_run, s2);
                     const float e = exp2f(m_run - M);

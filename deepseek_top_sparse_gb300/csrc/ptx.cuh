@@ -98,6 +98,18 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// Split cluster barrier: arrive early, wait (acquire) just before the first
+// access that needs every CTA of the cluster to have passed its arrive.  Each
+// thread alternates arrive and wait; whole warps execute them.  The arrive is
+// relaxed: it publishes nothing by itself (mbarrier initialisation is
+// published by fence.mbarrier_init.release.cluster).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
