@@ -283,9 +283,10 @@ __device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *
 //      for the weights, its row's sink (the lse table was filled through
 //      distributed shared memory before the cluster barrier);
 //   2. per row the final weights w_i / den (the combine kernel's formula);
-//   3. weighted sums, 4 passes at a time: this split's own partial from
-//      shared memory, the others from L2 (the first batch of the first other
-//      split was loaded in step 1).
+//   3. weighted sums: the first other split's chunks (loaded in step 1) and
+//      this split's own partial from shared memory first, then any further
+//      splits from L2.  A split combines at most 64 rows (two or more
+//      splits), which is at most kB passes, so one batch covers them.
 template <int DC, typename C>
 __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int split,
                                              uint32_t crank, int tid) {
@@ -296,7 +297,8 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
     float *tab = reinterpret_cast<float *>(smem + C::OFF_LSE);   // [split][row]
     constexpr int CH = DC / 4;                 // float4 chunks per row
     constexpr int RP = C::THREADS / CH;        // rows per pass
-    constexpr int kB = 4;                      // passes per batch
+    constexpr int kB = 8;                      // passes: covers 64 rows for every DC
+    static_assert(kB * RP >= kM / 2, "one batch covers a split's rows");
     static_assert(C::THREADS % CH == 0 && kM <= C::THREADS, "thread -> (row, chunk) map");
     const int c = tid % CH;
     const int rt = cr0 + tid / CH;             // this thread's first row
@@ -340,48 +342,45 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
     if (tid == 0) SA_TRACE_POINT(1, 60, 1);
     __syncthreads();
     const uint8_t *own = smem + C::OFF_KV + rt * C::STAGE_ROW + c * 16;
-    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (tok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
-    const int64_t pass_u2 = int64_t(RP) * p.D / 4;
-    for (int k0 = 0; rt + k0 * RP < cr1; k0 += kB) {
-        float4 acc[kB];
+    float4 acc[kB];
 #pragma unroll
-        for (int u = 0; u < kB; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < ns; ++i) {
-            float4 v[kB];
-            if (i == first_other && k0 == 0) {
-#pragma unroll
-                for (int u = 0; u < kB; ++u) v[u] = pre[u];
-            } else if (i == split) {
-#pragma unroll
-                for (int u = 0; u < kB; ++u)
-                    if (rt + (k0 + u) * RP < cr1)
-                        v[u] = *reinterpret_cast<const float4 *>(own + (k0 + u) * RP * C::STAGE_ROW);
-            } else {
-                const float4 *src = part(i);
-#pragma unroll
-                for (int u = 0; u < kB; ++u)
-                    if (rt + (k0 + u) * RP < cr1) v[u] = __ldcg(src + (k0 + u) * pass_f4);
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int r = rt + (k0 + u) * RP;
-                if (r < cr1) {
-                    const float w = tab[i * kM + r];
-                    acc[u].x = fmaf(w, v[u].x, acc[u].x);
-                    acc[u].y = fmaf(w, v[u].y, acc[u].y);
-                    acc[u].z = fmaf(w, v[u].z, acc[u].z);
-                    acc[u].w = fmaf(w, v[u].w, acc[u].w);
-                }
-            }
+    for (int u = 0; u < kB; ++u) {
+        const int r = rt + u * RP;
+        if (r < cr1) {
+            const float wo = tab[first_other * kM + r], ws = tab[split * kM + r];
+            const float4 o4 = *reinterpret_cast<const float4 *>(own + u * RP * C::STAGE_ROW);
+            acc[u] = make_float4(fmaf(wo, pre[u].x, ws * o4.x), fmaf(wo, pre[u].y, ws * o4.y),
+                                 fmaf(wo, pre[u].z, ws * o4.z), fmaf(wo, pre[u].w, ws * o4.w));
         }
+    }
+    for (int i = 0; i < ns; ++i) {
+        if (i == split || i == first_other) continue;
+        const float4 *src = part(i);
+        float4 v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+            if (rt + u * RP < cr1) v[u] = __ldcg(src + u * pass_f4);
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
-            if (rt + (k0 + u) * RP < cr1) {
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-                dst[(k0 + u) * pass_u2] =
-                    make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+            const int r = rt + u * RP;
+            if (r < cr1) {
+                const float w = tab[i * kM + r];
+                acc[u].x = fmaf(w, v[u].x, acc[u].x);
+                acc[u].y = fmaf(w, v[u].y, acc[u].y);
+                acc[u].z = fmaf(w, v[u].z, acc[u].z);
+                acc[u].w = fmaf(w, v[u].w, acc[u].w);
             }
+        }
+    }
+    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (tok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
+    const int64_t pass_u2 = int64_t(RP) * p.D / 4;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+        if (rt + u * RP < cr1) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+            dst[u * pass_u2] =
+                make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
         }
     }
 }
