@@ -41,6 +41,7 @@
 
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "sa_internal.h"
@@ -385,7 +386,10 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
     }
 }
 
-template <int DC, int CL>
+// kPosScale: softmax_scale > 0 (the usual case).  A zero or negative scale
+// takes another instantiation whose softmax leaves invalid slots out
+// explicitly, so the usual one carries no code for it.
+template <int DC, int CL, bool kPosScale>
 __global__ void __launch_bounds__(Cfg<DC, CL>::THREADS, 1)
 attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     using C = Cfg<DC, CL>;
@@ -743,7 +747,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             return true;
         };
         bool ok = true;
-        const bool pos_scale = p.scale_log2 >= 0.f;
+        constexpr bool pos_scale = kPosScale;
         float m_run = -INFINITY, l_run = 0.f;
         uint32_t cur[32], nxt[32];
         if (clustered) ptx::cluster_wait();   // before the first remote access
@@ -786,18 +790,26 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             }
             // masked, scaled row max of this half (the scale is applied once,
             // to the max, when it is positive; invalid slots become -inf)
+            // Row max of scale * s over the valid slots.  With a positive scale
+            // (the usual case) invalid slots become -inf, the scale is applied
+            // once to the max, and 2^(scale * -inf - m) gives P = 0 below.  A
+            // zero or negative scale would turn -inf into NaN or +inf, so it
+            // takes a path that leaves invalid slots out of the max and
+            // selects P = 0 for them.
+            const bool full = vm == 0xFFFFFFFFu;
             float mloc = -INFINITY;
-            if (vm != 0xFFFFFFFFu) {
+            if constexpr (pos_scale) {
+                if (!full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = ((vm >> j) & 1u) ? s[j] : -INFINITY;
-            }
-            if (pos_scale) {
+                    for (int j = 0; j < 32; ++j) s[j] = ((vm >> j) & 1u) ? s[j] : -INFINITY;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) mloc = fmaxf(mloc, s[j]);
                 mloc *= p.scale_log2;
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) mloc = fmaxf(mloc, s[j] * p.scale_log2);
+                for (int j = 0; j < 32; ++j)
+                    if ((vm >> j) & 1u) mloc = fmaxf(mloc, s[j] * p.scale_log2);
             }
             // row max over both column halves
             if (tid == 0) SA_TRACE_POINT(2, a, 6);
@@ -849,17 +861,29 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 }
             }
             // P = 2^(scale*s - m) as bf16 pairs into TMEM (A operand of P.V);
-            // invalid slots hold -inf and give exactly 0
+            // invalid slots give exactly 0
             uint32_t pw[16];
             float lsum = 0.f;
             const float nm = -m_run;
+            // two copies of the loop keep the usual path free of selects
+            auto p_tile = [&](auto masked) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
-                const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
-                lsum += p0 + p1;
-                const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-                pw[c] = *reinterpret_cast<const uint32_t *>(&v);
+                for (int c = 0; c < 16; ++c) {
+                    float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
+                    float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
+                    if constexpr (decltype(masked)::value) {
+                        p0 = ((vm >> (2 * c)) & 1u) ? p0 : 0.f;
+                        p1 = ((vm >> (2 * c + 1)) & 1u) ? p1 : 0.f;
+                    }
+                    lsum += p0 + p1;
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                    pw[c] = *reinterpret_cast<const uint32_t *>(&v);
+                }
+            };
+            if (pos_scale || full) {
+                p_tile(std::false_type{});
+            } else if constexpr (!pos_scale) {
+                p_tile(std::true_type{});
             }
             ptx::tmem_st16(lane_addr + C::P_COL + (a & 1) * (kBN / 2) + half * 16, pw);
             ptx::tmem_wait_st();
@@ -1113,14 +1137,20 @@ cudaError_t prepare_kernel(int dev) {
     static cudaError_t attr_err[kMaxDev];
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [dev] {
-        attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
+        attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (attr_err[dev] == cudaSuccess)
+            attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         // The warpgroups' setmaxnreg split is drawn from the launch allocation;
         // a build that launched with fewer registers per thread could never
         // satisfy the softmax warpgroups' increase, so it is not launched.
         cudaFuncAttributes fa{};
-        if (attr_err[dev] == cudaSuccess) attr_err[dev] = cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL>);
-        if (attr_err[dev] == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err[dev] = cudaErrorInvalidConfiguration;
+        for (int k = 0; k < 2 && attr_err[dev] == cudaSuccess; ++k) {
+            attr_err[dev] = k == 0 ? cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, true>)
+                                   : cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, false>);
+            if (attr_err[dev] == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err[dev] = cudaErrorInvalidConfiguration;
+        }
     });
     return attr_err[dev];
 }
@@ -1149,7 +1179,7 @@ bool fused_combine(int dev, int ns) {
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL>, &q);
+        const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL, true>, &q);
         fits[dev][cs] = qe == cudaSuccess && n >= 1;
         (void)cudaGetLastError();   // a refused query is not a launch error
     });
@@ -1199,7 +1229,8 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     CUtensorMap qmap;
     e = encode_q_map(&qmap, a);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL>, p, qmap);
+    return a.scale > 0.f ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, true>, p, qmap)
+                         : cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, false>, p, qmap);
 }
 
 }  // namespace

@@ -89,6 +89,14 @@ def test_sink_limits():
     assert_close(o, run_oracle(inp), "sink=+-inf")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.05, -1.0, 1e-4])
+def test_zero_and_negative_scales_with_masked_slots(scale):
+    # masked slots weigh exactly 0 whatever the sign of the scale
+    inp = workloads.random_attn(2, 2, 128, 512, 500, 300, p_invalid=0.3, seed=41, scale=scale)
+    for ns in (1, 2):
+        assert_close(run_gpu(inp, num_splits=ns), run_oracle(inp), f"scale={scale} splits={ns}")
+
+
 def test_single_valid_slot_closed_form():
     # one valid slot: o = sigmoid(x - sink) * row, checked against the oracle
     inp = workloads.random_attn(1, 2, 128, 512, 64, 70, p_invalid=0.0, seed=6)
