@@ -28,7 +28,7 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
-           "sa_sparse_attn_launch_count")
+           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_build_topk_mask.restype = i32
         lib.sa_sparse_attn_fwd_static_ws.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p]
         lib.sa_sparse_attn_fwd_static_ws.restype = i32
+        lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_longlong]
+        lib.sa_selftest_wait_timeout.restype = i32
         lib.sa_device_error.argtypes = [i32]
         lib.sa_device_error.restype = i32
         _lib = lib
@@ -132,6 +134,10 @@ def sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K,
     shp = (ctypes.c_int64 * 3)(*[int(v) for v in mask_shape])
     return int(load().sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K, key_starts,
                                          mask, shp, stream))
+
+
+def sa_selftest_wait_timeout(max_cycles: int) -> int:
+    return int(load().sa_selftest_wait_timeout(int(max_cycles)))
 
 
 def sa_device_error(clear: bool = True) -> int:

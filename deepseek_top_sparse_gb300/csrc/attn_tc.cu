@@ -173,13 +173,13 @@ struct TcParams {
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
 template <bool kCluster = false>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long max_cycles = kWaitCycles) {
     auto poll = [&] { return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity); };
     if (poll()) return true;
     const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (poll()) return true;
-        if ((n & 1023u) == 0 && clock64() - t0 > kWaitCycles) {
+        if ((n & 1023u) == 0 && clock64() - t0 > max_cycles) {
             record_error(kErrWaitTimeout);
             return false;
         }
@@ -1308,6 +1308,24 @@ extern "C" int sa_trace_read_cta(unsigned long long *cta, unsigned long long *co
 }
 namespace sa {
 #endif
+
+// Self-test of the bounded wait: one warp waits, with the kernel's own wait
+// routine and a short cycle limit, on an mbarrier phase that nothing ever
+// completes.  The wait must give up, record kErrWaitTimeout and return.
+__global__ void wait_timeout_selftest_kernel(long long max_cycles) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    (void)wait_bar(ptx::smem_u32(&bar), 0, max_cycles);
+}
+
+cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(max_cycles);
+    return cudaGetLastError();
+}
 
 cudaError_t read_device_error(int *value, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();

@@ -223,6 +223,18 @@ sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32
     return SA_OK;
 }
 
+int sa_selftest_wait_timeout(long long max_cycles) {
+    if (max_cycles < 1 || max_cycles > (1ll << 28)) return -1;
+    DeviceInfo dev;
+    if (current_device(&dev) != SA_OK) return -1;
+    int before = 0;
+    if (sa::read_device_error(&before, true) != cudaSuccess) return -1;   // start from a clear word
+    if (sa::launch_wait_timeout_selftest(max_cycles, nullptr) != cudaSuccess) return -1;
+    int code = 0;
+    if (sa::read_device_error(&code, true) != cudaSuccess) return -1;
+    return code;
+}
+
 int sa_device_error(int clear) {
     int v = 0;
     if (sa::read_device_error(&v, clear != 0) != cudaSuccess) return -1;

@@ -19,6 +19,7 @@ enum DeviceError : int {
 // The device error word lives in attn_tc.cu; every kernel that can fail
 // records into it with atomicCAS(0 -> code) so the first failure sticks.
 cudaError_t read_device_error(int *value, bool clear);
+cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream);
 
 // ---- launchers (host side, enqueue only; arguments already validated) ----
 

@@ -178,6 +178,16 @@ sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32
  * Returns -1 if the word cannot be read. */
 int sa_device_error(int clear);
 
+/* Self-test of that mechanism, without any fault: launches one warp that
+ * waits, with the kernels' own bounded-wait routine and a limit of
+ * `max_cycles` SM clock cycles (1 .. 2^28, i.e. at most ~0.13 s), on a
+ * barrier phase that nothing completes.  Synchronises the current device and
+ * returns the code the wait recorded (1 = wait timed out, the expected
+ * result), leaving the word clear; -1 on a bad argument or a CUDA error.
+ * Any earlier code is cleared first.  The pages have no counterpart of this
+ * call: it exists to test failure detection on a shared GPU. */
+int sa_selftest_wait_timeout(long long max_cycles);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,6 +50,12 @@ def test_binding_exposes_c_names():
     assert set(binding.EXPORTS) == set(_declared_functions())
 
 
+def test_selftest_validates_its_limit_on_the_host():
+    # argument checks happen before any device work (no GPU needed)
+    assert binding.sa_selftest_wait_timeout(0) == -1
+    assert binding.sa_selftest_wait_timeout(-5) == -1
+
+
 def test_status_strings():
     assert binding.sa_status_string(0) == "SA_OK"
     assert binding.sa_status_string(4) == "SA_ERR_WORKSPACE"
