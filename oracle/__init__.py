@@ -58,10 +58,13 @@ def _load():
             lib.oracle_sparse_attn.argtypes = [p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, ctypes.c_int]
             lib.oracle_sparse_attn_tokens.argtypes = (
                 [p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
+            lib.oracle_sparse_attn_tokens_len.argtypes = (
+                [p, p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
             lib.oracle_masked_dense_attn.argtypes = [p, p, p, p, i64, i64, p, ctypes.c_double] + [i64] * 5 + [p]
             lib.oracle_topk_mask_shape.argtypes = [i64, i64, i64, ctypes.c_int, p]
             lib.oracle_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p]
-            for f in (lib.oracle_sparse_attn, lib.oracle_sparse_attn_tokens, lib.oracle_masked_dense_attn,
+            for f in (lib.oracle_sparse_attn, lib.oracle_sparse_attn_tokens, lib.oracle_sparse_attn_tokens_len,
+                      lib.oracle_masked_dense_attn,
                       lib.oracle_topk_mask_shape, lib.oracle_build_topk_mask):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -89,8 +92,11 @@ def _np(x, dtype):
     return np.ascontiguousarray(x.detach().cpu().numpy(), dtype=dtype)
 
 
-def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0):
-    """float64 o[B,S,H,D] (or o[len(tokens),H,D] for flat token ids b*S+s)."""
+def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0,
+                topk_length=None):
+    """float64 o[B,S,H,D] (or o[len(tokens),H,D] for flat token ids b*S+s).
+    topk_length: optional int32 [B,S]; slot j of token (b,s) counts only if
+    j < clamp(topk_length[b,s], 0, K)."""
     qb, kvb = _bf16_bits(q), _bf16_bits(kv)
     sink = _np(attn_sink, np.float32)
     idx = _np(topk_idxs, np.int32)
@@ -98,19 +104,17 @@ def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, 
     T = kvb.shape[1]
     K = idx.shape[-1]
     assert kvb.shape == (B, T, D) and idx.shape == (B, S, K) and sink.shape == (H,)
-    lib = _load()
-    if tokens is None:
-        o = np.zeros((B, S, H, D), dtype=np.float64)
-        rc = lib.oracle_sparse_attn(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), float(softmax_scale),
-                                    B, S, H, D, T, K, _ptr(o), int(nthreads))
-    else:
-        tok = np.ascontiguousarray(tokens, dtype=np.int64)
-        o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
-        rc = lib.oracle_sparse_attn_tokens(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), float(softmax_scale),
-                                           B, S, H, D, T, K, _ptr(tok), tok.shape[0], _ptr(o), int(nthreads))
+    lens = None
+    if topk_length is not None:
+        lens = _np(topk_length, np.int32).reshape(B, S)
+    tok = np.arange(B * S, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
+    rc = _load().oracle_sparse_attn_tokens_len(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                              float(softmax_scale), B, S, H, D, T, K, _ptr(tok), tok.shape[0],
+                                              _ptr(o), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn rejected its arguments (rc={rc})")
-    return o
+    return o.reshape(B, S, H, D) if tokens is None else o
 
 
 def masked_dense_attn(q, kv, attn_sink, mask, softmax_scale: float, key_offset=None):

@@ -56,6 +56,7 @@ typedef struct {
     const uint16_t *q, *kv;
     const float *sink;
     const int32_t *idx;
+    const int32_t *topk_len; /* [B*S] valid-prefix length per query token, or NULL */
     double scale;
     double *o;
     int64_t B, S, H, D, T, K;
@@ -67,6 +68,9 @@ typedef struct {
 
 /* One query token (b, s), every head h:
  *   logits_j = scale * q[b,s,h,:] . kv[b, idx_j, :]   for valid slots j,
+ *   a slot j being valid when 0 <= idx_j < T and, if a per-token topk_length
+ *   is given, j < min(max(topk_length[b,s], 0), K) (the "topk length per
+ *   sequence" variant of the FlashMLA kernels, [V4-5.3]);
  *   -inf for invalid ones; the sink logit attn_sink[h] is appended; softmax
  *   over the K+1 values; o = sum_{j<K} w_j * kv[b, idx_j, :] (the sink's
  *   weight is dropped).  [V4-5.2], [V4-5.5] */
@@ -74,6 +78,12 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
     const int64_t b = tok / J->S, s = tok % J->S;
     const int64_t H = J->H, D = J->D, T = J->T, K = J->K;
     const int32_t *idx = J->idx + (b * J->S + s) * K;
+    int64_t len = K;
+    if (J->topk_len) {
+        len = J->topk_len[b * J->S + s];
+        if (len < 0) len = 0;
+        if (len > K) len = K;
+    }
     double *logit = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
     for (int64_t h = 0; h < H; ++h) {
@@ -84,7 +94,7 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         /* logits of the K slots, -inf where the slot is invalid (R1) */
         for (int64_t j = 0; j < K; ++j) {
             int64_t t = idx[j];
-            if (t < 0 || t >= T) {
+            if (j >= len || t < 0 || t >= T) {
                 logit[j] = -INFINITY;
                 continue;
             }
@@ -135,16 +145,19 @@ static int resolve_threads(int nthreads) {
     return n > 0 ? (int)n : 1;
 }
 
-/* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D]. */
-int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
-                              const int32_t *topk_idxs, double softmax_scale, int64_t B,
-                              int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
-                              const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
+/* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D].
+ * topk_length: [B*S] int32 or NULL (every slot may count). */
+int oracle_sparse_attn_tokens_len(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                                  const int32_t *topk_idxs, const int32_t *topk_length,
+                                  double softmax_scale, int64_t B, int64_t S, int64_t H, int64_t D,
+                                  int64_t T, int64_t K, const int64_t *tokens, int64_t ntok, double *o,
+                                  int nthreads) {
     if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || K < 0 || ntok < 0) return ORACLE_EINVAL;
     for (int64_t i = 0; i < ntok; ++i)
         if (tokens[i] < 0 || tokens[i] >= B * S) return ORACLE_EINVAL;
     attn_job J;
-    J.q = q; J.kv = kv; J.sink = attn_sink; J.idx = topk_idxs; J.scale = softmax_scale;
+    J.q = q; J.kv = kv; J.sink = attn_sink; J.idx = topk_idxs; J.topk_len = topk_length;
+    J.scale = softmax_scale;
     J.o = o; J.B = B; J.S = S; J.H = H; J.D = D; J.T = T; J.K = K;
     J.tokens = tokens; J.ntok = ntok; J.next = 0;
     pthread_mutex_init(&J.mu, NULL);
@@ -156,6 +169,14 @@ int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float
     free(th);
     pthread_mutex_destroy(&J.mu);
     return ORACLE_OK;
+}
+
+int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                              const int32_t *topk_idxs, double softmax_scale, int64_t B,
+                              int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
+                              const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
+    return oracle_sparse_attn_tokens_len(q, kv, attn_sink, topk_idxs, NULL, softmax_scale, B, S, H, D, T,
+                                         K, tokens, ntok, o, nthreads);
 }
 
 /* Every token; o is [B,S,H,D]. */

@@ -309,3 +309,66 @@ def test_tiny_workload_shape_and_structure():
         assert len(set(v.tolist())) == len(v)
     assert 0 < int((idx < 0).sum()) < 64
     assert inp.softmax_scale == 0.125
+
+
+# --------------------------------------------------- per-token topk_length
+# A slot counts only below the token's length (clamped to [0, K]); these pins
+# tie the length path to the -1 path, to the closed forms and to the clamps.
+
+def _rand_case(seed, B=2, S=3, H=4, D=32, T=40, K=24, p_invalid=0.1):
+    return workloads.random_attn(B, S, H, D, T, K, p_invalid=p_invalid, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_topk_length_k_equals_no_length(seed):
+    inp = _rand_case(200 + seed)
+    B, S, K = inp.topk_idxs.shape
+    full = np.full((B, S), K, dtype=np.int32)
+    a = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    b = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=full)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_topk_length_equals_minus_one_padding(seed):
+    inp = _rand_case(210 + seed)
+    B, S, K = inp.topk_idxs.shape
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, K + 1, size=(B, S)).astype(np.int32)
+    padded = inp.topk_idxs.clone()
+    for b in range(B):
+        for s in range(S):
+            padded[b, s, lens[b, s]:] = -1
+    a = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens)
+    b_ = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, padded, inp.softmax_scale)
+    assert np.array_equal(a, b_)
+
+
+def test_topk_length_zero_gives_zero_and_one_gives_sigmoid_closed_form():
+    inp = _rand_case(220, p_invalid=0.0)
+    B, S, K = inp.topk_idxs.shape
+    zero = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                              topk_length=np.zeros((B, S), np.int32))
+    assert not zero.any()
+    one = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                             topk_length=np.ones((B, S), np.int32))
+    q = inp.q.double().numpy()
+    kv = inp.kv.double().numpy()
+    sink = inp.attn_sink.double().numpy()
+    for b in range(B):
+        for s in range(S):
+            row = kv[b, int(inp.topk_idxs[b, s, 0])]
+            x = inp.softmax_scale * q[b, s] @ row                      # [H]
+            w = 1.0 / (1.0 + np.exp(sink - x))                         # sigmoid(x - sink)
+            np.testing.assert_allclose(one[b, s], w[:, None] * row[None, :], rtol=1e-12, atol=1e-14)
+
+
+def test_topk_length_is_clamped_to_zero_and_k():
+    inp = _rand_case(230)
+    B, S, K = inp.topk_idxs.shape
+    neg = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                             topk_length=np.full((B, S), -7, np.int32))
+    assert not neg.any()
+    big = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                             topk_length=np.full((B, S), K + 100, np.int32))
+    assert np.array_equal(big, oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale))
