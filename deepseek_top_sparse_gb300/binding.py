@@ -28,7 +28,7 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
-           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout")
+           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +69,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_sparse_attn_fwd.restype = i32
         lib.sa_sparse_attn_fwd_splits.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p, sz, p]
         lib.sa_sparse_attn_fwd_splits.restype = i32
+        lib.sa_sparse_attn_fwd_topk_length.argtypes = [p, p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p, sz, p]
+        lib.sa_sparse_attn_fwd_topk_length.restype = i32
         lib.sa_topk_mask_shape.argtypes = [i64, i64, i64, i32, p]
         lib.sa_topk_mask_shape.restype = i32
         lib.sa_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p, p]
@@ -111,6 +113,13 @@ def sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, 
                               num_splits, workspace, workspace_bytes, stream) -> int:
     return int(load().sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T,
                                                  K, num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_sparse_attn_fwd_topk_length(q, kv, attn_sink, topk_idxs, topk_length, softmax_scale, o, B, S, H, D, T, K,
+                                   num_splits, workspace, workspace_bytes, stream) -> int:
+    return int(load().sa_sparse_attn_fwd_topk_length(q, kv, attn_sink, topk_idxs, topk_length, softmax_scale, o,
+                                                      B, S, H, D, T, K, num_splits, workspace, workspace_bytes,
+                                                      stream))
 
 
 def sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K, num_splits,
@@ -170,11 +179,12 @@ def workspace_for(B, S, H, D, K, num_splits=0, device=None) -> torch.Tensor | No
 
 def sparse_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk_idxs: torch.Tensor,
                 softmax_scale: float, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                num_splits: int = 0, stream=None) -> torch.Tensor:
+                num_splits: int = 0, stream=None, topk_length: torch.Tensor | None = None) -> torch.Tensor:
     """o = sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale) on the GPU.
 
     q bf16 [B,S,H,D], kv bf16 [B,T,D], attn_sink fp32 [H], topk_idxs int32
-    [B,S,K] (-1 = invalid), all contiguous on one CUDA device."""
+    [B,S,K] (-1 = invalid), all contiguous on one CUDA device.  topk_length:
+    optional int32 [B,S]; slot j counts only below clamp(topk_length, 0, K)."""
     for name, t, dt in (("q", q, torch.bfloat16), ("kv", kv, torch.bfloat16),
                         ("attn_sink", attn_sink, torch.float32), ("topk_idxs", topk_idxs, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -190,6 +200,15 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if topk_length is not None:
+        if topk_length.dtype != torch.int32 or not topk_length.is_cuda or not topk_length.is_contiguous() \
+                or topk_length.numel() != B * S:
+            raise ValueError("topk_length must be a contiguous CUDA int32 tensor with B*S elements")
+        rc = sa_sparse_attn_fwd_topk_length(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(topk_idxs),
+                                            _dptr(topk_length), float(softmax_scale), _dptr(out), B, S, H, D, T, K,
+                                            int(num_splits), _dptr(workspace), ws_bytes, _stream_ptr(stream))
+        _check("sa_sparse_attn_fwd_topk_length", rc)
+        return out
     rc = sa_sparse_attn_fwd_splits(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(topk_idxs), float(softmax_scale),
                                    _dptr(out), B, S, H, D, T, K, int(num_splits), _dptr(workspace), ws_bytes,
                                    _stream_ptr(stream))

@@ -160,6 +160,7 @@ struct TcParams {
     const __nv_bfloat16 *kv;  // [B, T, D]
     const float *sink;        // [H]
     const int32_t *idx;       // [tokens, K]
+    const int32_t *topk_len;  // [tokens] valid-prefix length per token, or nullptr
     __nv_bfloat16 *o;         // [tokens, H, D]
     float *ws_o;              // [tokens, splits, H, D]
     float *ws_lse;            // [tokens, splits, H]
@@ -445,6 +446,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     int32_t tv[kSteps];
     float *sink_tab = reinterpret_cast<float *>(smem + C::OFF_SINK);
     const float sink_t = tid < p.H ? __ldg(p.sink + tid) : 0.f;   // into sink_tab below
+    // slot j of this token counts only below its topk length (clamped to
+    // [0, K]); loaded beside the index list, applied when it is converted
+    const int32_t len_t = p.topk_len != nullptr ? __ldg(p.topk_len + tok) : int32_t(p.K);
     {
         const int32_t *irow = p.idx + tok * p.K + slot0;
 #pragma unroll
@@ -494,7 +498,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             const int ch = u * kWarpsAll + warp;
             if (ch < ntiles * 2) {
                 const int j = ch * 32 + lane;
-                const bool v = tv[u] >= 0 && int64_t(tv[u]) < p.T;
+                const bool v = tv[u] >= 0 && int64_t(tv[u]) < p.T && slot0 + j < int64_t(len_t);
                 rowc[j] = v ? int32_t(b * p.T + tv[u]) : -1;
                 const uint32_t m = __ballot_sync(0xffffffffu, v);
                 if (lane == 0) reinterpret_cast<uint32_t *>(vmask)[ch] = m;
@@ -1200,6 +1204,7 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
     p.sink = a.sink;
     p.idx = a.idx;
+    p.topk_len = a.topk_len;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.ws_o = a.ws_o;
     p.ws_lse = a.ws_lse;

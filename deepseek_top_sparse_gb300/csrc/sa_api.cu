@@ -130,11 +130,11 @@ int sa_sparse_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int6
     return sa::kernels_per_call(D, splits);
 }
 
-sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
-                                    const int32_t *topk_idxs, float softmax_scale, void *o,
-                                    int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
-                                    int64_t K, int num_splits, void *workspace,
-                                    size_t workspace_bytes, sa_stream_t stream) {
+sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const float *attn_sink,
+                                         const int32_t *topk_idxs, const int32_t *topk_length,
+                                         float softmax_scale, void *o, int64_t B, int64_t S, int64_t H,
+                                         int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
+                                         size_t workspace_bytes, sa_stream_t stream) {
     if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || K < 0) return SA_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
     if (num_splits > 64) return SA_ERR_INVALID_ARG;
@@ -144,7 +144,8 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
     if (B * S == 0) return SA_OK;
     if (!q || !kv || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return SA_ERR_ALIGNMENT;
-    if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3))
+    if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3) ||
+        (reinterpret_cast<uintptr_t>(topk_length) & 3))
         return SA_ERR_ALIGNMENT;
     DeviceInfo dev;
     const sa_status st = current_device(&dev);
@@ -156,7 +157,8 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
 
     sa::AttnArgs a{};
-    a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = topk_idxs; a.scale = softmax_scale; a.o = o;
+    a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = topk_idxs; a.topk_len = topk_length;
+    a.scale = softmax_scale; a.o = o;
     a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
     a.num_splits = splits;
     if (splits > 1) {
@@ -169,6 +171,15 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
     // the main kernel, then (for splits too many for one cluster) the combine
     if (sa::launch_sparse_attn(a, dev.sms, s) != cudaSuccess) return SA_ERR_CUDA;
     return SA_OK;
+}
+
+sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
+                                    const int32_t *topk_idxs, float softmax_scale, void *o,
+                                    int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                    int64_t K, int num_splits, void *workspace,
+                                    size_t workspace_bytes, sa_stream_t stream) {
+    return sa_sparse_attn_fwd_topk_length(q, kv, attn_sink, topk_idxs, nullptr, softmax_scale, o, B, S, H, D, T,
+                                          K, num_splits, workspace, workspace_bytes, stream);
 }
 
 sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_sink,

@@ -28,6 +28,7 @@ struct AttnArgs {
     const void *kv;         // bf16 [B,T,D]
     const float *sink;      // [H]
     const int32_t *idx;     // [B,S,K]
+    const int32_t *topk_len;  // [B,S] or nullptr
     float scale;
     void *o;                // bf16 [B,S,H,D]
     int64_t B, S, H, D, T, K;

@@ -117,6 +117,22 @@ sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *
                                     int64_t K, int num_splits, void *workspace,
                                     size_t workspace_bytes, sa_stream_t stream);
 
+/* sa_sparse_attn_fwd_splits with a per-token valid-prefix length:
+ *   topk_length  int32 [B,S] in device memory, 4-byte aligned, or NULL.
+ * Slot j of token (b,s) counts only if j < clamp(topk_length[b,s], 0, K)
+ * (and, as always, its index is in [0, T)); slots at or past the length are
+ * invalid whatever their index, so callers need not pad the tail with -1.
+ * NULL behaves as sa_sparse_attn_fwd_splits.  This is the "top-k length
+ * differs per sequence" variant of the FlashMLA kernels ("DeepSeek V4
+ * 源码剖析, 第5章", §5.3); the extra second KV source those kernels also
+ * accept is not supported.  Other arguments, workspace and errors as in
+ * sa_sparse_attn_fwd_splits. */
+sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const float *attn_sink,
+                                         const int32_t *topk_idxs, const int32_t *topk_length,
+                                         float softmax_scale, void *o, int64_t B, int64_t S, int64_t H,
+                                         int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
+                                         size_t workspace_bytes, sa_stream_t stream);
+
 /* Allocation-free variant of sa_sparse_attn_fwd_splits, for callers that
  * cannot supply device memory: a plain C host program with no device
  * allocator, or a serving loop that plans all memory up front and must not

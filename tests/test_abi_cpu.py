@@ -102,6 +102,16 @@ def test_attn_validation_happens_before_any_device_work():
     assert _fwd(S=0) == 0
 
 
+def test_topk_length_entry_validates_like_the_others():
+    f = binding.sa_sparse_attn_fwd_topk_length
+    base = dict(q=16, kv=16, attn_sink=16, topk_idxs=16, topk_length=16, softmax_scale=0.125, o=32, B=1, S=1,
+                H=8, D=64, T=10, K=4, num_splits=0, workspace=None, workspace_bytes=0, stream=None)
+    assert f(**dict(base, topk_length=2)) == 3      # not 4-byte aligned
+    assert f(**dict(base, D=96)) == 2
+    assert f(**dict(base, q=None)) == 1
+    assert f(**dict(base, B=0)) == 0
+
+
 def test_mask_validation_happens_before_any_device_work():
     f = binding.sa_build_topk_mask
     shape = binding.sa_topk_mask_shape(1, 1, 129, 0)

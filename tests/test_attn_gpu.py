@@ -217,3 +217,55 @@ def test_v4_prefill_sampled_tokens():
     # properties at every token: finite everywhere, and token 0 (one valid slot:
     # itself) equals sigmoid-weighted kv row 0 per head -- covered by the sample
     assert torch.isfinite(o.float()).all()
+
+
+# ------------------------------------------------------- per-token topk_length
+
+def run_gpu_len(inp, lens, num_splits=0):
+    d = inp.to("cuda")
+    L = torch.as_tensor(lens, dtype=torch.int32).cuda().contiguous()
+    o = binding.sparse_attn(d.q, d.kv, d.attn_sink, d.topk_idxs, d.softmax_scale, num_splits=num_splits,
+                            topk_length=L)
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    return o
+
+
+@pytest.mark.parametrize("H,D,K,T,ns", [
+    (128, 512, 1152, 2000, 0),
+    (128, 512, 700, 1500, 2),     # fused split combine
+    (100, 512, 700, 1500, 3),
+    (128, 512, 1152, 2000, 5),    # separate combine kernel
+    (16, 256, 300, 500, 1),
+    (64, 64, 200, 300, 2),
+])
+def test_topk_length_random(H, D, K, T, ns):
+    inp = workloads.random_attn(3, 2, H, D, T, K, p_invalid=0.1, seed=H + K + ns + 7)
+    rng = np.random.default_rng(K + ns)
+    lens = rng.integers(-2, K + 6, size=(3, 2)).astype(np.int32)
+    lens[0, 0], lens[0, 1], lens[1, 0] = 0, 1, K        # the edge values
+    ref = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens)
+    assert_close(run_gpu_len(inp, lens, ns), ref, f"topk_length H={H} D={D} K={K} splits={ns}")
+
+
+def test_topk_length_cuts_through_valid_slots():
+    inp = workloads.random_attn(2, 2, 128, 512, 800, 640, p_invalid=0.0, seed=77)
+    lens = np.array([[50, 64], [65, 639]], dtype=np.int32)   # inside a tile, at and just past a boundary
+    for ns in (1, 2):
+        ref = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens)
+        assert_close(run_gpu_len(inp, lens, ns), ref, f"cut lengths splits={ns}")
+
+
+def test_topk_length_of_the_valid_prefix_matches_minus_one_padding_exactly():
+    # ratio-4 decode: each token's slots are a valid prefix then -1; passing
+    # the prefix length runs the same tiles with the same arithmetic
+    inp = workloads.v4_ratio4_decode()
+    T = inp.kv.shape[1]
+    valid = (inp.topk_idxs >= 0) & (inp.topk_idxs < T)
+    lens = valid.sum(-1).to(torch.int32).numpy()
+    # the workload's valid slots form a prefix of every token's slot list
+    prefix = valid.int().cumprod(-1).sum(-1).numpy()
+    assert (prefix == lens).all()
+    a = run_gpu(inp)
+    b = run_gpu_len(inp, lens)
+    assert torch.equal(a, b)
