@@ -28,7 +28,8 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
-           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length")
+           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length",
+           "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_build_topk_mask.restype = i32
         lib.sa_sparse_attn_fwd_static_ws.argtypes = [p, p, p, p, ctypes.c_float, p] + [i64] * 6 + [i32, p]
         lib.sa_sparse_attn_fwd_static_ws.restype = i32
+        lib.sa_masked_dense_attn_fwd.argtypes = [p, p, p, p, i64, i64, i32, ctypes.c_float, p] + [i64] * 5 + \
+            [i32, p, sz, p]
+        lib.sa_masked_dense_attn_fwd.restype = i32
+        lib.sa_masked_dense_attn_workspace_size.argtypes = [i64] * 5 + [i32]
+        lib.sa_masked_dense_attn_workspace_size.restype = sz
+        lib.sa_masked_dense_attn_launch_count.argtypes = [i64] * 5 + [i32]
+        lib.sa_masked_dense_attn_launch_count.restype = i32
         lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_longlong]
         lib.sa_selftest_wait_timeout.restype = i32
         lib.sa_device_error.argtypes = [i32]
@@ -128,6 +136,21 @@ def sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, 
     arguments as sa_sparse_attn_fwd_splits without the workspace pair."""
     return int(load().sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
                                                    num_splits, stream))
+
+
+def sa_masked_dense_attn_workspace_size(B, S, H, D, T, num_splits=0) -> int:
+    return int(load().sa_masked_dense_attn_workspace_size(B, S, H, D, T, num_splits))
+
+
+def sa_masked_dense_attn_launch_count(B, S, H, D, T, num_splits=0) -> int:
+    return int(load().sa_masked_dense_attn_launch_count(B, S, H, D, T, num_splits))
+
+
+def sa_masked_dense_attn_fwd(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word, softmax_scale, o,
+                             B, S, H, D, T, num_splits, workspace, workspace_bytes, stream) -> int:
+    return int(load().sa_masked_dense_attn_fwd(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word,
+                                                softmax_scale, o, B, S, H, D, T, num_splits, workspace,
+                                                workspace_bytes, stream))
 
 
 def sa_topk_mask_shape(batch, max_query_len, max_key_len, reserve_key_starts_word) -> tuple[int, int, int]:
@@ -239,4 +262,33 @@ def build_topk_mask(topk: torch.Tensor, cu_q_lens: torch.Tensor, max_q_len: int,
     rc = sa_build_topk_mask(_dptr(tk), tk.shape[0], _dptr(cu_q_lens), B, max_q_len, max_key_len, tk.shape[1],
                             _dptr(key_starts), _dptr(out), shape, _stream_ptr(stream))
     _check("sa_build_topk_mask", rc)
+    return out
+
+
+def masked_dense_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, mask: torch.Tensor,
+                      softmax_scale: float, key_start_word: bool = False, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, num_splits: int = 0, stream=None) -> torch.Tensor:
+    """Attention of q bf16 [B,S,H,D] over the keys of kv bf16 [B,T,D] that the
+    bit-packed mask (32-bit words [B, rows >= S, words], as build_topk_mask
+    returns it) admits, with the per-head sink.  key_start_word: test bit
+    t + mask[b, 0, words-1] for key t (a context chunk at that offset)."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("kv", kv, torch.bfloat16), ("attn_sink", attn_sink, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if mask.element_size() != 4 or mask.dim() != 3 or not mask.is_cuda or not mask.is_contiguous():
+        raise ValueError("mask must be a contiguous CUDA 32-bit tensor [B, rows, words]")
+    B, S, H, D = q.shape
+    T = kv.shape[1]
+    if kv.shape != (B, T, D) or attn_sink.shape != (H,) or mask.shape[0] != B:
+        raise ValueError("shape mismatch among q, kv, attn_sink, mask")
+    if out is None:
+        out = torch.empty_like(q)
+    need = sa_masked_dense_attn_workspace_size(B, S, H, D, T, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = sa_masked_dense_attn_fwd(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(mask), mask.shape[1], mask.shape[2],
+                                  int(bool(key_start_word)), float(softmax_scale), _dptr(out), B, S, H, D, T,
+                                  int(num_splits), _dptr(workspace), ws_bytes, _stream_ptr(stream))
+    _check("sa_masked_dense_attn_fwd", rc)
     return out

@@ -169,6 +169,12 @@ struct TcParams {
     int fused;                // 1: the token's splits share a cluster and combine in-kernel
     int unit_slots;           // slots per split, a multiple of kBN, <= kMaxUnitSlots
     float scale_log2;         // softmax_scale * log2(e)
+    // Bit-mask mode (mask != nullptr, idx unused, K = T): slot j of a token is
+    // key j of its kv, admitted iff bit (j + key_start) of the token's mask
+    // row is set; each split compacts its admitted keys into full tiles.
+    const uint32_t *mask;     // [B, mask_rows, mask_words]
+    int64_t mask_rows, mask_words;
+    int key_start_word;       // 1: key_start = mask[b, 0, mask_words - 1] (int32), else 0
 };
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
@@ -410,7 +416,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     const int64_t slot0 = int64_t(split) * p.unit_slots;
     const int64_t left = p.K - slot0;
     const int nslots = left <= 0 ? 0 : int(left < p.unit_slots ? left : p.unit_slots);
-    const int ntiles = (nslots + kBN - 1) / kBN;
+    int ntiles = (nslots + kBN - 1) / kBN;
 
     int32_t *rowc = reinterpret_cast<int32_t *>(smem + C::OFF_IDX);
     uint64_t *vmask = reinterpret_cast<uint64_t *>(smem + C::OFF_VALID);
@@ -449,12 +455,28 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     // slot j of this token counts only below its topk length (clamped to
     // [0, K]); loaded beside the index list, applied when it is converted
     const int32_t len_t = p.topk_len != nullptr ? __ldg(p.topk_len + tok) : int32_t(p.K);
-    {
+    if (p.mask == nullptr) {
         const int32_t *irow = p.idx + tok * p.K + slot0;
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int j = (u * kWarpsAll + warp) * 32 + lane;
             tv[u] = j < nslots ? __ldg(irow + j) : -1;
+        }
+    } else {
+        // key t is admitted iff bit (t + key_start) & 31 of word
+        // (t + key_start) >> 5 of the token's mask row is set; positions
+        // outside the row admit nothing
+        const uint32_t *mrow = p.mask + (b * p.mask_rows + (tok - b * p.S)) * p.mask_words;
+        const int64_t key_start =
+            p.key_start_word ? int64_t(int32_t(__ldg(p.mask + b * p.mask_rows * p.mask_words + p.mask_words - 1)))
+                             : 0;
+        const int64_t row_bits = p.mask_words * 32;
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) {
+            const int j = (u * kWarpsAll + warp) * 32 + lane;
+            const int64_t key = slot0 + j + key_start;
+            const bool on = j < nslots && key >= 0 && key < row_bits && ((__ldg(mrow + (key >> 5)) >> (key & 31)) & 1u);
+            tv[u] = on ? int32_t(slot0 + j) : -1;
         }
     }
     if (warp == kMmaWarp) {
@@ -492,7 +514,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
     // mask per tile, 32 slots per warp step
-    {
+    if (p.mask == nullptr) {
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int ch = u * kWarpsAll + warp;
@@ -503,6 +525,35 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 const uint32_t m = __ballot_sync(0xffffffffu, v);
                 if (lane == 0) reinterpret_cast<uint32_t *>(vmask)[ch] = m;
             }
+        }
+    } else {
+        // bit-mask mode: the admitted keys, in key order, packed into the
+        // leading slots (a stream compaction over the 32-key chunks); only the
+        // last tile can be partial
+        static_assert(kSteps * kWarpsAll == kMaxUnitSlots / 32 && kMaxUnitSlots / 32 == 64, "one count per lane pair");
+        int *cnt = reinterpret_cast<int *>(red);   // [64] admitted keys per chunk (scratch until the softmax)
+        uint32_t mb[kSteps];
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) {
+            mb[u] = __ballot_sync(0xffffffffu, tv[u] >= 0);
+            if (lane == 0) cnt[u * kWarpsAll + warp] = __popc(mb[u]);
+        }
+        __syncthreads();
+        const int c0 = cnt[lane], c1 = cnt[lane + 32];
+        const int total = int(__reduce_add_sync(0xffffffffu, uint32_t(c0 + c1)));
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) {
+            const int ch = u * kWarpsAll + warp;
+            const int base =
+                int(__reduce_add_sync(0xffffffffu, uint32_t((lane < ch ? c0 : 0) + (lane + 32 < ch ? c1 : 0))));
+            if ((mb[u] >> lane) & 1u)
+                rowc[base + __popc(mb[u] & ((1u << lane) - 1u))] = int32_t(b * p.T + tv[u]);
+        }
+        ntiles = (total + kBN - 1) / kBN;
+        if (tid < ntiles * kBN - total) rowc[total + tid] = -1;
+        if (tid < ntiles) {
+            const int r = total - tid * kBN;
+            vmask[tid] = r >= kBN ? ~0ull : ((1ull << r) - 1ull);
         }
     }
     if (tid < kM) sink_tab[tid] = sink_t;
@@ -1216,6 +1267,10 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.fused = fused ? 1 : 0;
     *fused_out = fused;
     p.scale_log2 = a.scale * kLog2e;
+    p.mask = a.mask;
+    p.mask_rows = a.mask_rows;
+    p.mask_words = a.mask_words;
+    p.key_start_word = a.key_start_word;
     if (p.unit_slots > kMaxUnitSlots) return cudaErrorInvalidValue;
 
     const int64_t ctas = a.B * a.S * a.num_splits * CL;

@@ -190,6 +190,58 @@ sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_si
                                      K, 0, workspace, workspace_bytes, stream);
 }
 
+size_t sa_masked_dense_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                           int num_splits) {
+    // the T keys of a token play the part of its K slots
+    return sa_sparse_attn_workspace_size(B, S, H, D, T, num_splits);
+}
+
+int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int num_splits) {
+    return sa_sparse_attn_launch_count(B, S, H, D, T, num_splits);
+}
+
+sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *attn_sink,
+                                   const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                   int key_start_word, float softmax_scale, void *o, int64_t B, int64_t S,
+                                   int64_t H, int64_t D, int64_t T, int num_splits, void *workspace,
+                                   size_t workspace_bytes, sa_stream_t stream) {
+    if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || mask_rows < 0 || mask_words < 0) return SA_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
+    if (num_splits > 64 || (key_start_word != 0 && key_start_word != 1)) return SA_ERR_INVALID_ARG;
+    if (!attn_sizes_ok(B, S, H, D, T) || T < 1) return SA_ERR_SHAPE;
+    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (mask_rows < S || mask_words < 1 || (mask_words & 3)) return SA_ERR_SHAPE;
+    if (B * S == 0) return SA_OK;
+    if (!q || !kv || !attn_sink || !mask || !o) return SA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(mask)) return SA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(attn_sink) & 3) return SA_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const sa_status st = current_device(&dev);
+    if (st != SA_OK) return st;
+
+    const int splits = clamp_splits(T, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, T, dev.sms));
+    const size_t need = workspace_bytes_for(B, S, H, D, splits);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
+
+    sa::AttnArgs a{};
+    a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = nullptr; a.topk_len = nullptr;
+    a.scale = softmax_scale; a.o = o;
+    a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = T;
+    a.num_splits = splits;
+    a.mask = mask; a.mask_rows = mask_rows; a.mask_words = mask_words; a.key_start_word = key_start_word;
+    if (splits > 1) {
+        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
+        o_bytes = (o_bytes + 255) / 256 * 256;
+        a.ws_o = static_cast<float *>(workspace);
+        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    }
+    if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return SA_OK;
+}
+
 sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key_len,
                              int reserve_key_starts_word, int64_t out_shape[3]) {
     if (out_shape == nullptr || batch < 0 || max_query_len < 0 || max_key_len < 0)

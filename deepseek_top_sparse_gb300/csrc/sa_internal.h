@@ -35,6 +35,10 @@ struct AttnArgs {
     int num_splits;         // >= 1
     float *ws_o;            // fp32 [tokens, splits, H, D]   (splits > 1)
     float *ws_lse;          // fp32 [tokens, splits, H]      (splits > 1)
+    // bit-mask mode (idx == nullptr, K == T): keys admitted by a packed mask
+    const uint32_t *mask = nullptr;   // [B, mask_rows, mask_words]
+    int64_t mask_rows = 0, mask_words = 0;
+    int key_start_word = 0;           // 1: key offset read from mask[b, 0, mask_words - 1]
 };
 
 // Slots handled by one split (a multiple of the 64-row tile).

@@ -184,6 +184,49 @@ sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32
                              const int64_t mask_shape[3], sa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* consumer of the mask: dense attention over the admitted keys              */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for sa_masked_dense_attn_fwd with these sizes and split
+ * count (<= 0: the planned count); 0 when one split needs none or the sizes
+ * are unsupported.  The splits divide the T keys of each query. */
+size_t sa_masked_dense_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                           int num_splits);
+
+/* Kernels one sa_masked_dense_attn_fwd call enqueues (1 or 2), 0 on
+ * unsupported sizes. */
+int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
+                                      int num_splits);
+
+/* Attention of every query token over the keys its mask row admits: the
+ * consumer side of the bit-packed mask (`dense_mask_mod` and, with
+ * key_start_word = 1, `offset_dense_mask_mod` on the vLLM PR 48770 page;
+ * the 16-byte row contract of the PR 52217 page).
+ *   q, kv, attn_sink, o, B, S, H, D, T, softmax_scale: as in
+ *               sa_sparse_attn_fwd (kv[b] holds the T keys of request b).
+ *   mask        uint32 [B, mask_rows, mask_words] device, 16-byte aligned,
+ *               mask_words a multiple of 4 (the layout sa_topk_mask_shape
+ *               gives), mask_rows >= S.  Query s of request b reads row
+ *               mask[b, s, :].
+ *   key_start_word  0: key t tests bit t; 1: key t tests bit t + ks_b where
+ *               ks_b = (int32) mask[b, 0, mask_words - 1], the reserved word
+ *               sa_build_topk_mask writes (T keys of a context chunk that
+ *               starts at absolute position ks_b).
+ * Key t of request b is admitted iff 0 <= p < 32 * mask_words and bit p & 31
+ * of word p >> 5 of the row is set, p = t (+ ks_b); the result is then
+ * sa_sparse_attn_fwd's with the admitted keys as the token's slot list.
+ * num_splits: 1..64 key ranges per token (<= 0: planned); workspace as in
+ * sa_sparse_attn_fwd_splits, sized by sa_masked_dense_attn_workspace_size.
+ * Errors as sa_sparse_attn_fwd_splits, plus SA_ERR_SHAPE for mask_rows < S,
+ * mask_words < 1 or not a multiple of 4, and SA_ERR_ALIGNMENT for a mask
+ * that is not 16-byte aligned. */
+sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *attn_sink,
+                                   const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                   int key_start_word, float softmax_scale, void *o, int64_t B, int64_t S,
+                                   int64_t H, int64_t D, int64_t T, int num_splits, void *workspace,
+                                   size_t workspace_bytes, sa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* diagnostics                                                              */
 /* ------------------------------------------------------------------------ */
 

@@ -134,3 +134,25 @@ def test_workspace_size_is_zero_without_splits_and_for_bad_sizes():
     assert n == (o_bytes + 255) // 256 * 256 + 2 * 3 * 2 * 8 * 4
     # never more splits than 64-slot tiles
     assert binding.sa_sparse_attn_workspace_size(1, 1, 8, 64, 64, 8) == 0
+
+
+def test_masked_dense_entry_validates_before_any_device_work():
+    f = binding.sa_masked_dense_attn_fwd
+    base = dict(q=16, kv=16, attn_sink=16, mask=16, mask_rows=4, mask_words=8, key_start_word=0,
+                softmax_scale=0.125, o=32, B=1, S=2, H=8, D=64, T=200, num_splits=0, workspace=None,
+                workspace_bytes=0, stream=None)
+    assert f(**dict(base, mask_words=6)) == 2         # rows must be whole 16-byte vectors
+    assert f(**dict(base, mask_words=0)) == 2
+    assert f(**dict(base, mask_rows=1)) == 2          # fewer mask rows than queries
+    assert f(**dict(base, D=96)) == 2
+    assert f(**dict(base, T=0)) == 2
+    assert f(**dict(base, key_start_word=2)) == 1
+    assert f(**dict(base, softmax_scale=float("inf"))) == 1
+    assert f(**dict(base, mask=None)) == 1
+    assert f(**dict(base, mask=8)) == 3               # mask not 16-byte aligned
+    assert f(**dict(base, q=24)) == 3
+    assert f(**dict(base, B=0)) == 0
+    # the T keys of a token are split like K slots
+    assert binding.sa_masked_dense_attn_workspace_size(2, 3, 8, 64, 256, 2) == \
+        binding.sa_sparse_attn_workspace_size(2, 3, 8, 64, 256, 2)
+    assert binding.sa_masked_dense_attn_workspace_size(1, 1, 8, 96, 256, 2) == 0
