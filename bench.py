@@ -144,6 +144,9 @@ def _profile_traffic(kernel_tag: str, src_hash: str):
 KERNEL_SOURCES = ["deepseek_top_sparse_gb300/csrc/attn_tc.cu", "deepseek_top_sparse_gb300/csrc/ptx.cuh"]
 
 
+MASK_SOURCES = ["deepseek_top_sparse_gb300/csrc/mask_build.cu"]
+
+
 def _attn_kernel_sources():
     return [p for p in KERNEL_SOURCES if os.path.exists(os.path.join(ROOT, p))]
 
@@ -389,7 +392,54 @@ def run_gpu(args):
         mask_obj = {"workload": mi.name, "us_per_call": mms * 1e3, "gbs": m_gbs,
                     "algorithmic_bytes": m_bytes,
                     "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": hbm, "unit": "GB/s",
-                                 "frac": m_gbs / hbm, "peak_source": src}}
+                                 "frac": m_gbs / hbm, "peak_source": src,
+                                 "traffic": _profile_traffic("mask_build", _source_hash(MASK_SOURCES))}}
+
+        # ---- the mask's consumer: dense attention over the admitted keys of
+        # the same 4 x 2048 query rows (8 heads of 64, 8193 keys per request)
+        if not args.no_extra:
+            mstep()
+            torch.cuda.synchronize()
+            gq = torch.Generator().manual_seed(1005)
+            Hm, Dm, Tm = 8, 64, mi.max_key_len
+            qm = torch.randn(mi.batch, mi.max_q_len, Hm, Dm, generator=gq).to(torch.bfloat16).to(dev)
+            kvm = torch.randn(mi.batch, Tm, Dm, generator=gq).to(torch.bfloat16).to(dev)
+            sinkm = torch.randn(Hm, generator=gq).to(dev)
+            om = torch.empty_like(qm)
+            wsm_n = binding.sa_masked_dense_attn_workspace_size(mi.batch, mi.max_q_len, Hm, Dm, Tm)
+            wsm = torch.empty(max(wsm_n, 1), dtype=torch.uint8, device=dev)
+            tk = workloads.topk_mask().topk            # distinct indices per row
+            admitted = int(((tk >= 0) & (tk < Tm)).sum())
+
+            def dstep():
+                binding.masked_dense_attn(qm, kvm, sinkm, mbuf, Dm ** -0.5, out=om, workspace=wsm)
+
+            for _ in range(3):
+                flush.zero_()
+                dstep()
+            torch.cuda.synchronize()
+            d_ms = []
+            for _ in range(10):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                dstep()
+                b.record(stream)
+                b.synchronize()
+                d_ms.append(a.elapsed_time(b))
+            assert binding.sa_device_error(True) == 0
+            dms = sum(d_ms) / len(d_ms)
+            _, tf_m, _, _ = _peaks()
+            fl_m = 4.0 * Hm * Dm * admitted
+            gb_m = float(admitted) * Dm * 2
+            roof_m = max(fl_m / (tf_m * 1e12), gb_m / (hbm * 1e9))
+            mask_obj["consumer"] = {
+                "op": "masked_dense_attn", "us_per_call": dms * 1e3,
+                "value": mi.batch * mi.max_q_len / (dms * 1e-3), "unit": UNIT,
+                "admitted_keys": admitted, "gathered_kv_gbs": gb_m / (dms * 1e-3) / 1e9,
+                "roofline_frac": roof_m / (dms * 1e-3), "bound": "hbm" if gb_m / hbm >= fl_m / tf_m / 1e3 else "tensor",
+                "launches_per_call": binding.sa_masked_dense_attn_launch_count(mi.batch, mi.max_q_len, Hm, Dm, Tm),
+                "l2": "flushed between calls"}
 
     if rank != 0:
         if ws > 1:
