@@ -96,6 +96,81 @@ def random_attn(B, S, H, D, T, K, *, p_invalid=0.1, seed=0, distinct=True, scale
                       name=f"random B={B} S={S} H={H} D={D} T={T} K={K}")
 
 
+FP8_ROW_BYTES = 584      # one row of the FP8 kv cache: 448 codes + 64 bf16 + 8 scale bytes
+
+
+@dataclass
+class Fp8AttnInputs:
+    q: torch.Tensor          # [B,S,H,512] bf16
+    kv8: torch.Tensor        # [B,T,584]   uint8 rows of the FP8 kv format
+    attn_sink: torch.Tensor  # [H]         float32
+    topk_idxs: torch.Tensor  # [B,S,K]     int32, -1 = invalid slot
+    softmax_scale: float
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device):
+        return Fp8AttnInputs(self.q.to(device), self.kv8.to(device), self.attn_sink.to(device),
+                             self.topk_idxs.to(device), self.softmax_scale, self.name, dict(self.meta))
+
+
+def fp8_kv_rows(B: int, T: int, g) -> torch.Tensor:
+    """uint8 [B, T, 584]: bytes 0..447 are E4M3 codes with a random sign,
+    exponent field uniform in [4, 9] and mantissa uniform in [0, 7] (so never
+    the NaN pattern; magnitudes 2^-3 .. 7.5); bytes 448..575 are 64 N(0,1)
+    bf16 values, little-endian; bytes 576..582 are E8M0 scale bytes uniform in
+    [124, 127] (2^-3 .. 1); byte 583 is zero padding."""
+    sign = torch.randint(0, 2, (B, T, 448), generator=g, dtype=torch.int32)
+    expo = torch.randint(4, 10, (B, T, 448), generator=g, dtype=torch.int32)
+    mant = torch.randint(0, 8, (B, T, 448), generator=g, dtype=torch.int32)
+    codes = (sign * 128 + expo * 8 + mant).to(torch.uint8)
+    rope = _randn_bf16((B, T, 64), g).contiguous().view(torch.uint8).reshape(B, T, 128)
+    scales = torch.randint(124, 128, (B, T, 7), generator=g, dtype=torch.int32).to(torch.uint8)
+    pad = torch.zeros((B, T, 1), dtype=torch.uint8)
+    return torch.cat([codes, rope, scales, pad], dim=-1).contiguous()
+
+
+def random_attn_fp8(B, S, H, T, K, *, p_invalid=0.1, seed=0) -> Fp8AttnInputs:
+    """random_attn's index pattern over an FP8 kv cache (D = 512)."""
+    g = _gen(seed)
+    q = _randn_bf16((B, S, H, 512), g)
+    kv8 = fp8_kv_rows(B, T, g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.empty((B, S, K), dtype=torch.int32)
+    for b in range(B):
+        for s in range(S):
+            idx[b, s] = _distinct(T, K, g) if K <= T else torch.randint(0, T, (K,), generator=g, dtype=torch.int32)
+    if p_invalid > 0:
+        idx[torch.rand((B, S, K), generator=g) < p_invalid] = -1
+    return Fp8AttnInputs(q, kv8, sink, idx, 512 ** -0.5, name=f"random fp8 B={B} S={S} H={H} T={T} K={K}")
+
+
+def v4_ratio4_decode_fp8(seed=1006, B=32, H=128, window=128, topk=1024, ratio=4, long_ctx=65536, short_lo=128,
+                         short_hi=4096) -> Fp8AttnInputs:
+    """The ratio-4 decode batch (same context mix and slot structure as
+    v4_ratio4_decode) over an FP8 kv cache of 584-byte rows."""
+    g = _gen(seed)
+    n_comp = long_ctx // ratio
+    T = window + n_comp
+    K = window + topk
+    q = _randn_bf16((B, 1, H, 512), g)
+    kv8 = fp8_kv_rows(B, T, g)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.full((B, 1, K), -1, dtype=torch.int32)
+    ctx = []
+    for b in range(B):
+        L = long_ctx if b >= B // 2 else int(torch.randint(short_lo, short_hi, (1,), generator=g))
+        ctx.append(L)
+        nw = min(window, L)
+        idx[b, 0, :nw] = torch.arange(nw, dtype=torch.int32)
+        pool = L // ratio
+        nc = min(topk, pool)
+        idx[b, 0, window:window + nc] = window + _distinct(pool, nc, g)
+    return Fp8AttnInputs(q, kv8, sink, idx, 512 ** -0.5,
+                         name=f"V4 ratio-4 decode, FP8 kv B={B} S=1 H={H} D=512 T={T} K={K}",
+                         meta=dict(context=ctx))
+
+
 def tiny(seed=1000) -> AttnInputs:
     """B=1,S=4,H=8,D=64,T=256,K=64: the first 64 of a random permutation of
     [0,256) per token, each slot -1 with probability 0.1, scale = 1/8."""

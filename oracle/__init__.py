@@ -16,6 +16,11 @@ What each routine follows (page title and section):
 * ``masked_dense_attn`` -- the consumer semantics of the bit mask from the
   vLLM PR 48770 page (``dense_mask_mod`` / ``offset_dense_mask_mod``): key k
   is admitted iff bit k&31 of word k>>5 of its query row is set.
+* ``sparse_attn_fp8`` / ``decode_kv_fp8`` -- the same attention over an FP8
+  kv cache in the V4 (FlashMLA "MODEL1") row format of "DeepSeek V4 源码剖析,
+  第5章" §5.3 and §5.6: 448 nope dims as E4M3 codes with one E8M0 scale per
+  64-dim tile, 64 RoPE dims in bf16, 584 bytes a row (byte order: reading R22
+  in oracle.c).  Each gathered row is decoded to exact values first.
 * ``topk_mask_shape`` / ``build_topk_mask`` -- vLLM PR 52217 page
   (``_topk_mask_shape``, ``_build_topk_mask`` and the two alignment tests) and
   the PR 48770 page (bit order, reserved key_start word).
@@ -60,11 +65,18 @@ def _load():
                 [p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
             lib.oracle_sparse_attn_tokens_len.argtypes = (
                 [p, p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
+            lib.oracle_sparse_attn_fp8_tokens.argtypes = (
+                [p, p, p, p, p, ctypes.c_double] + [i64] * 5 + [p, i64, p, ctypes.c_int])
+            lib.oracle_decode_kv_fp8.argtypes = [p, i64, p]
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = ctypes.c_double
+            lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_to_double.restype = ctypes.c_double
             lib.oracle_masked_dense_attn.argtypes = [p, p, p, p, i64, i64, p, ctypes.c_double] + [i64] * 5 + [p]
             lib.oracle_topk_mask_shape.argtypes = [i64, i64, i64, ctypes.c_int, p]
             lib.oracle_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p]
             for f in (lib.oracle_sparse_attn, lib.oracle_sparse_attn_tokens, lib.oracle_sparse_attn_tokens_len,
-                      lib.oracle_masked_dense_attn,
+                      lib.oracle_masked_dense_attn, lib.oracle_sparse_attn_fp8_tokens, lib.oracle_decode_kv_fp8,
                       lib.oracle_topk_mask_shape, lib.oracle_build_topk_mask):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -114,6 +126,60 @@ def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, 
                                               _ptr(o), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn rejected its arguments (rc={rc})")
+    return o.reshape(B, S, H, D) if tokens is None else o
+
+
+FP8_ROW_BYTES = 584   # one kv row of the FP8 cache (R22)
+
+
+def _u8(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint8
+        return np.ascontiguousarray(x)
+    import torch
+
+    assert x.dtype == torch.uint8
+    return np.ascontiguousarray(x.detach().cpu().contiguous().numpy())
+
+
+def e4m3_to_float(code: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(code)))
+
+
+def e8m0_to_float(byte: int) -> float:
+    return float(_load().oracle_e8m0_to_double(int(byte)))
+
+
+def decode_kv_fp8(kv8) -> np.ndarray:
+    """float64 [..., 512] exact values of FP8 kv rows uint8 [..., 584]."""
+    a = _u8(kv8)
+    assert a.shape[-1] == FP8_ROW_BYTES
+    rows = int(np.prod(a.shape[:-1]))
+    out = np.zeros((rows, 512), dtype=np.float64)
+    rc = _load().oracle_decode_kv_fp8(_ptr(a), rows, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_decode_kv_fp8 rejected its arguments")
+    return out.reshape(*a.shape[:-1], 512)
+
+
+def sparse_attn_fp8(q, kv8, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0,
+                    topk_length=None):
+    """sparse_attn over an FP8 kv cache uint8 [B,T,584]; q bf16 [B,S,H,512]."""
+    qb, kb = _bf16_bits(q), _u8(kv8)
+    sink = _np(attn_sink, np.float32)
+    idx = _np(topk_idxs, np.int32)
+    B, S, H, D = qb.shape
+    T = kb.shape[1]
+    K = idx.shape[-1]
+    assert D == 512 and kb.shape == (B, T, FP8_ROW_BYTES) and idx.shape == (B, S, K) and sink.shape == (H,)
+    lens = None if topk_length is None else _np(topk_length, np.int32).reshape(B, S)
+    tok = np.arange(B * S, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
+    rc = _load().oracle_sparse_attn_fp8_tokens(_ptr(qb), _ptr(kb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                               float(softmax_scale), B, S, H, T, K, _ptr(tok), tok.shape[0],
+                                               _ptr(o), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_attn_fp8 rejected its arguments (rc={rc})")
     return o.reshape(B, S, H, D) if tokens is None else o
 
 

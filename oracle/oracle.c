@@ -18,6 +18,11 @@
  *   [MASK-BITS] vLLM PR 48770 page (masked MHA for sparse-MLA prefill), source
  *             excerpt `dense_mask_mod` / `offset_dense_mask_mod`: word kv>>5,
  *             bit kv&31, LSB first; the last word of row q=0 holds key_start.
+ *   [V4-5.3]  same chapter, §5.3: the MODEL1 (V4) constants of FlashMLA --
+ *             head dim 512 = 448 "nope" dims + 64 RoPE dims, FP8 quantisation
+ *             tiles of 64 dims, 8 scales per token (7 used), V carries the
+ *             RoPE dims too; §5.6: the nope part is stored quantised, the RoPE
+ *             part stays bf16, and the kernel dequantises what it gathers.
  *
  * Readings taken where the pages are silent (each one is tested):
  *   R1 a slot is valid iff 0 <= idx < T (the pages only define -1).
@@ -49,11 +54,63 @@ static double bf16_to_double(uint16_t bits) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 KV rows, [V4-5.3] / [V4-5.6]                                          */
+/* ------------------------------------------------------------------------ */
+/* Reading R22 (the pages give the parts and their sizes, not their order):
+ * one kv row is 584 bytes,
+ *   [0, 448)    dims 0..447 as FP8 E4M3 codes (OCP 8-bit floating point:
+ *               1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ *               infinities; S.1111.111 is NaN; exponent 0 is subnormal),
+ *   [448, 576)  dims 448..511 as bf16, little-endian,
+ *   [576, 584)  one scale byte per 64-dim tile of the nope dims (7 used, the
+ *               8th is padding), each an E8M0 exponent: 2^(byte - 127), 255 = NaN.
+ * value(d) = e4m3(code_d) * 2^(scale[d / 64] - 127) for d < 448, else bf16. */
+#define FP8_ROW_BYTES 584
+#define FP8_NOPE 448
+#define FP8_TILE 64
+#define FP8_ROPE_OFF 448
+#define FP8_SCALE_OFF 576
+#define FP8_DIM 512
+
+double oracle_e4m3_to_double(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6); /* subnormal: 0.mmm * 2^(1-7) */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+double oracle_e8m0_to_double(uint8_t s) {
+    if (s == 255) return NAN;
+    return ldexp(1.0, (int)s - 127);
+}
+
+/* one 584-byte row -> 512 doubles */
+static void fp8_row_decode(const uint8_t *row, double *out) {
+    for (int d = 0; d < FP8_NOPE; ++d)
+        out[d] = oracle_e4m3_to_double(row[d]) * oracle_e8m0_to_double(row[FP8_SCALE_OFF + d / FP8_TILE]);
+    for (int d = FP8_NOPE; d < FP8_DIM; ++d) {
+        const uint8_t *p = row + FP8_ROPE_OFF + 2 * (d - FP8_NOPE);
+        out[d] = bf16_to_double((uint16_t)(p[0] | (p[1] << 8)));
+    }
+}
+
+int oracle_decode_kv_fp8(const uint8_t *kv8, int64_t rows, double *out /* [rows, 512] */) {
+    if (rows < 0) return ORACLE_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) fp8_row_decode(kv8 + r * FP8_ROW_BYTES, out + r * FP8_DIM);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* sparse_attn, [V4-5.2]                                                     */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
     const uint16_t *q, *kv;
+    const uint8_t *kv8;    /* FP8 rows of 584 bytes instead of bf16 kv (D = 512), or NULL */
     const float *sink;
     const int32_t *idx;
     const int32_t *topk_len; /* [B*S] valid-prefix length per query token, or NULL */
@@ -65,6 +122,16 @@ typedef struct {
     int64_t next; /* work counter, guarded by mu */
     pthread_mutex_t mu;
 } attn_job;
+
+/* kv row `row` (= b*T + t) as D doubles, from bf16 or from the FP8 layout */
+static void load_kv_row(const attn_job *J, int64_t row, double *out) {
+    if (J->kv8) {
+        fp8_row_decode(J->kv8 + row * FP8_ROW_BYTES, out);
+        return;
+    }
+    const uint16_t *kr = J->kv + row * J->D;
+    for (int64_t d = 0; d < J->D; ++d) out[d] = bf16_to_double(kr[d]);
+}
 
 /* One query token (b, s), every head h:
  *   logits_j = scale * q[b,s,h,:] . kv[b, idx_j, :]   for valid slots j,
@@ -86,6 +153,7 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
     }
     double *logit = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+    double *krow = (double *)malloc(sizeof(double) * (size_t)D);
     for (int64_t h = 0; h < H; ++h) {
         double *orow = out + h * D;
         for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
@@ -98,9 +166,9 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
                 logit[j] = -INFINITY;
                 continue;
             }
-            const uint16_t *kr = J->kv + (b * T + t) * D;
+            load_kv_row(J, b * T + t, krow);
             double dot = 0.0;
-            for (int64_t d = 0; d < D; ++d) dot += qrow[d] * bf16_to_double(kr[d]);
+            for (int64_t d = 0; d < D; ++d) dot += qrow[d] * krow[d];
             logit[j] = dot * J->scale; /* R8: scale on q.k only */
         }
         const double sink = (double)J->sink[h];
@@ -119,12 +187,13 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         for (int64_t j = 0; j < K; ++j) {
             if (logit[j] == -INFINITY) continue; /* weight exactly 0 */
             const double w = exp(logit[j] - m) / denom;
-            const uint16_t *kr = J->kv + (b * T + idx[j]) * D;
-            for (int64_t d = 0; d < D; ++d) orow[d] += w * bf16_to_double(kr[d]);
+            load_kv_row(J, b * T + idx[j], krow);
+            for (int64_t d = 0; d < D; ++d) orow[d] += w * krow[d];
         }
     }
     free(logit);
     free(qrow);
+    free(krow);
 }
 
 static void *attn_worker(void *arg) {
@@ -145,18 +214,15 @@ static int resolve_threads(int nthreads) {
     return n > 0 ? (int)n : 1;
 }
 
-/* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D].
- * topk_length: [B*S] int32 or NULL (every slot may count). */
-int oracle_sparse_attn_tokens_len(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
-                                  const int32_t *topk_idxs, const int32_t *topk_length,
-                                  double softmax_scale, int64_t B, int64_t S, int64_t H, int64_t D,
-                                  int64_t T, int64_t K, const int64_t *tokens, int64_t ntok, double *o,
-                                  int nthreads) {
+static int run_attn_job(const uint16_t *q, const uint16_t *kv, const uint8_t *kv8, const float *attn_sink,
+                        const int32_t *topk_idxs, const int32_t *topk_length, double softmax_scale, int64_t B,
+                        int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, const int64_t *tokens, int64_t ntok,
+                        double *o, int nthreads) {
     if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || K < 0 || ntok < 0) return ORACLE_EINVAL;
     for (int64_t i = 0; i < ntok; ++i)
         if (tokens[i] < 0 || tokens[i] >= B * S) return ORACLE_EINVAL;
     attn_job J;
-    J.q = q; J.kv = kv; J.sink = attn_sink; J.idx = topk_idxs; J.topk_len = topk_length;
+    J.q = q; J.kv = kv; J.kv8 = kv8; J.sink = attn_sink; J.idx = topk_idxs; J.topk_len = topk_length;
     J.scale = softmax_scale;
     J.o = o; J.B = B; J.S = S; J.H = H; J.D = D; J.T = T; J.K = K;
     J.tokens = tokens; J.ntok = ntok; J.next = 0;
@@ -169,6 +235,28 @@ int oracle_sparse_attn_tokens_len(const uint16_t *q, const uint16_t *kv, const f
     free(th);
     pthread_mutex_destroy(&J.mu);
     return ORACLE_OK;
+}
+
+/* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D].
+ * topk_length: [B*S] int32 or NULL (every slot may count). */
+int oracle_sparse_attn_tokens_len(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                                  const int32_t *topk_idxs, const int32_t *topk_length,
+                                  double softmax_scale, int64_t B, int64_t S, int64_t H, int64_t D,
+                                  int64_t T, int64_t K, const int64_t *tokens, int64_t ntok, double *o,
+                                  int nthreads) {
+    return run_attn_job(q, kv, NULL, attn_sink, topk_idxs, topk_length, softmax_scale, B, S, H, D, T, K, tokens,
+                        ntok, o, nthreads);
+}
+
+/* The same attention over an FP8 kv cache (rows of 584 bytes, R22): every
+ * gathered row is decoded to its 512 exact values first; q and o keep D = 512. */
+int oracle_sparse_attn_fp8_tokens(const uint16_t *q, const uint8_t *kv8, const float *attn_sink,
+                                  const int32_t *topk_idxs, const int32_t *topk_length, double softmax_scale,
+                                  int64_t B, int64_t S, int64_t H, int64_t T, int64_t K, const int64_t *tokens,
+                                  int64_t ntok, double *o, int nthreads) {
+    if (kv8 == NULL) return ORACLE_EINVAL;
+    return run_attn_job(q, NULL, kv8, attn_sink, topk_idxs, topk_length, softmax_scale, B, S, H, FP8_DIM, T, K,
+                        tokens, ntok, o, nthreads);
 }
 
 int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,

@@ -372,3 +372,86 @@ def test_topk_length_is_clamped_to_zero_and_k():
     big = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
                              topk_length=np.full((B, S), K + 100, np.int32))
     assert np.array_equal(big, oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale))
+
+
+# ---------------------------------------------------------------- FP8 kv rows (V4 format)
+
+def test_e4m3_decode_matches_the_format_definition():
+    # OCP 8-bit floating point, E4M3: bias 7, 3 mantissa bits, subnormals at
+    # exponent 0, no infinities, S.1111.111 = NaN, largest finite 448
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+             0x40: 2.0, 0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0, 0x77: 240.0, 0x30: 0.5}
+    for code, want in cases.items():
+        assert oracle.e4m3_to_float(code) == want, hex(code)
+    assert math.copysign(1.0, oracle.e4m3_to_float(0x80)) == -1.0
+    assert math.isnan(oracle.e4m3_to_float(0x7F)) and math.isnan(oracle.e4m3_to_float(0xFF))
+
+
+def test_e4m3_decode_matches_torch_float8_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_to_float(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(lib))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], lib[~np.isnan(lib)])
+
+
+def test_e8m0_decode():
+    assert oracle.e8m0_to_float(127) == 1.0
+    assert oracle.e8m0_to_float(128) == 2.0
+    assert oracle.e8m0_to_float(0) == 2.0 ** -127
+    assert oracle.e8m0_to_float(254) == 2.0 ** 127
+    assert math.isnan(oracle.e8m0_to_float(255))
+
+
+def _hand_row():
+    row = np.zeros(oracle.FP8_ROW_BYTES, dtype=np.uint8)
+    row[576:583] = 127                     # every tile scale 2^0 ...
+    row[0] = 0x38                          # dim 0: 1.0
+    row[63] = 0xC0                         # dim 63: -2.0 (tile 0)
+    row[64] = 0x38                         # dim 64: 1.0 x 2^2 (tile 1)
+    row[577] = 129
+    row[447] = 0x30                        # dim 447: 0.5 x 2^-1 (tile 6)
+    row[582] = 126
+    row[448:450] = (0x80, 0x3F)            # dim 448: bf16 1.0, little-endian
+    row[574:576] = (0x00, 0xC0)            # dim 511: bf16 -2.0
+    row[583] = 0xFF                        # padding byte: ignored
+    want = np.zeros(512)
+    want[0], want[63], want[64], want[447], want[448], want[511] = 1.0, -2.0, 4.0, 0.25, 1.0, -2.0
+    return row, want
+
+
+def test_fp8_row_layout_hand_built():
+    row, want = _hand_row()
+    np.testing.assert_array_equal(oracle.decode_kv_fp8(row[None, :])[0], want)
+
+
+def test_fp8_attention_single_slot_closed_form():
+    # K = 1: o = sigmoid(x - sink) * kv_row, x = scale * q . kv_row
+    row, kv_row = _hand_row()
+    g = torch.Generator().manual_seed(41)
+    q = torch.randn(1, 1, 3, 512, generator=g).to(torch.bfloat16)
+    sink = torch.tensor([0.3, -1.0, 2.0])
+    kv8 = torch.from_numpy(np.stack([np.zeros_like(row), row])[None])     # [1, 2, 584]
+    idx = torch.tensor([[[1]]], dtype=torch.int32)
+    got = oracle.sparse_attn_fp8(q, kv8, sink, idx, 0.1)
+    qd = q.double().numpy()[0, 0]
+    for h in range(3):
+        x = 0.1 * float(qd[h] @ kv_row)
+        w = 1.0 / (1.0 + math.exp(-(x - float(sink[h]))))
+        np.testing.assert_allclose(got[0, 0, h], w * kv_row, rtol=1e-14, atol=1e-300)
+
+
+def test_fp8_attention_equals_bf16_attention_on_the_decoded_rows():
+    # the generated codes and scales decode to values that bf16 holds exactly,
+    # so attention over the FP8 rows must equal attention over those values
+    inp = workloads.random_attn_fp8(2, 3, 8, 90, 40, p_invalid=0.2, seed=43)
+    dec = oracle.decode_kv_fp8(inp.kv8)
+    kv_bf16 = torch.from_numpy(dec).to(torch.bfloat16)
+    np.testing.assert_array_equal(kv_bf16.double().numpy(), dec)       # exact in bf16
+    want = oracle.sparse_attn(inp.q, kv_bf16, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    got = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    np.testing.assert_array_equal(got, want)
+    lens = torch.tensor([[5, 40, 0], [17, -3, 60]], dtype=torch.int32)
+    np.testing.assert_array_equal(
+        oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens),
+        oracle.sparse_attn(inp.q, kv_bf16, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens))
