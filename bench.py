@@ -361,6 +361,47 @@ def run_gpu(args):
                            "l2": "flushed between calls"}
             assert binding.sa_device_error(True) == 0
 
+    # ---- the ratio-4 decode over an FP8 kv cache (584-byte rows), cold L2
+    if rank == 0 and not args.no_extra:
+        hbm_o, tf_o, _, _ = _peaks()
+        fc = workloads.v4_ratio4_decode_fp8()
+        fd = fc.to(dev)
+        Bf, Sf, Hf, _ = fd.q.shape
+        Tf, Kf = fd.kv8.shape[1], fd.topk_idxs.shape[-1]
+        vf = workloads.count_valid(fc.topk_idxs, Tf)
+        outf = torch.empty_like(fd.q)
+        wsf = binding.workspace_for(Bf, Sf, Hf, 512, Kf, device=dev)
+
+        def fstep():
+            binding.sparse_attn_fp8(fd.q, fd.kv8, fd.attn_sink, fd.topk_idxs, fd.softmax_scale, out=outf,
+                                    workspace=wsf)
+
+        for _ in range(3):
+            flush.zero_()
+            fstep()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(20):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fstep()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        assert binding.sa_device_error(True) == 0
+        ms_f = sum(ts) / len(ts)
+        fl = 4.0 * Hf * 512 * vf
+        gb = float(vf) * workloads.FP8_ROW_BYTES
+        roof = max(fl / (tf_o * 1e12), gb / (hbm_o * 1e9))
+        other["v4_ratio4_decode_fp8"] = {
+            "workload": fc.name, "us_per_call": ms_f * 1e3, "value": Bf * Sf / (ms_f * 1e-3), "unit": UNIT,
+            "tflops": fl / (ms_f * 1e-3) / 1e12, "valid_slots": vf, "gathered_bytes_per_row": workloads.FP8_ROW_BYTES,
+            "roofline_frac": roof / (ms_f * 1e-3), "compute_frac": fl / (tf_o * 1e12) / (ms_f * 1e-3),
+            "launches_per_call": binding.sa_sparse_attn_fp8_launch_count(Bf, Sf, Hf, Kf),
+            "l2": "flushed between calls"}
+        del fd, fc
+
     # ---- mask build on the mask workload (B=4, Q=2048, 8193 keys, K=2048)
     mask_obj = None
     if rank == 0 and not args.no_mask:

@@ -29,7 +29,8 @@ EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_work
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
            "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length",
-           "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count")
+           "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count",
+           "sa_sparse_attn_fwd_fp8", "sa_sparse_attn_fp8_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_masked_dense_attn_workspace_size.restype = sz
         lib.sa_masked_dense_attn_launch_count.argtypes = [i64] * 5 + [i32]
         lib.sa_masked_dense_attn_launch_count.restype = i32
+        lib.sa_sparse_attn_fwd_fp8.argtypes = [p, p, p, p, p, ctypes.c_float, p] + [i64] * 5 + [i32, p, sz, p]
+        lib.sa_sparse_attn_fwd_fp8.restype = i32
+        lib.sa_sparse_attn_fp8_launch_count.argtypes = [i64] * 4 + [i32]
+        lib.sa_sparse_attn_fp8_launch_count.restype = i32
         lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_longlong]
         lib.sa_selftest_wait_timeout.restype = i32
         lib.sa_device_error.argtypes = [i32]
@@ -136,6 +141,16 @@ def sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, 
     arguments as sa_sparse_attn_fwd_splits without the workspace pair."""
     return int(load().sa_sparse_attn_fwd_static_ws(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
                                                    num_splits, stream))
+
+
+def sa_sparse_attn_fwd_fp8(q, kv_fp8, attn_sink, topk_idxs, topk_length, softmax_scale, o, B, S, H, T, K,
+                           num_splits, workspace, workspace_bytes, stream) -> int:
+    return int(load().sa_sparse_attn_fwd_fp8(q, kv_fp8, attn_sink, topk_idxs, topk_length, softmax_scale, o, B, S, H,
+                                              T, K, num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_sparse_attn_fp8_launch_count(B, S, H, K, num_splits=0) -> int:
+    return int(load().sa_sparse_attn_fp8_launch_count(B, S, H, K, num_splits))
 
 
 def sa_masked_dense_attn_workspace_size(B, S, H, D, T, num_splits=0) -> int:
@@ -291,4 +306,38 @@ def masked_dense_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor
                                   int(bool(key_start_word)), float(softmax_scale), _dptr(out), B, S, H, D, T,
                                   int(num_splits), _dptr(workspace), ws_bytes, _stream_ptr(stream))
     _check("sa_masked_dense_attn_fwd", rc)
+    return out
+
+
+FP8_ROW_BYTES = 584
+
+
+def sparse_attn_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, attn_sink: torch.Tensor, topk_idxs: torch.Tensor,
+                    softmax_scale: float, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    num_splits: int = 0, stream=None, topk_length: torch.Tensor | None = None) -> torch.Tensor:
+    """sparse_attn over an FP8 kv cache: q bf16 [B,S,H,512], kv_fp8 uint8
+    [B,T,584] (448 E4M3 codes, 64 bf16 RoPE dims, 8 E8M0 tile-scale bytes per
+    row), attn_sink fp32 [H], topk_idxs int32 [B,S,K]; o bf16 [B,S,H,512]."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("kv_fp8", kv_fp8, torch.uint8),
+                        ("attn_sink", attn_sink, torch.float32), ("topk_idxs", topk_idxs, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    B, S, H, D = q.shape
+    T = kv_fp8.shape[1]
+    K = topk_idxs.shape[-1]
+    if D != 512 or kv_fp8.shape != (B, T, FP8_ROW_BYTES) or topk_idxs.shape != (B, S, K) or attn_sink.shape != (H,):
+        raise ValueError("shape mismatch among q, kv_fp8, attn_sink, topk_idxs")
+    if topk_length is not None and (topk_length.dtype != torch.int32 or not topk_length.is_cuda
+                                    or not topk_length.is_contiguous() or topk_length.numel() != B * S):
+        raise ValueError("topk_length must be a contiguous CUDA int32 tensor with B*S elements")
+    if out is None:
+        out = torch.empty_like(q)
+    need = sa_sparse_attn_workspace_size(B, S, H, 512, K, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = sa_sparse_attn_fwd_fp8(_dptr(q), _dptr(kv_fp8), _dptr(attn_sink), _dptr(topk_idxs), _dptr(topk_length),
+                                float(softmax_scale), _dptr(out), B, S, H, T, K, int(num_splits), _dptr(workspace),
+                                ws_bytes, _stream_ptr(stream))
+    _check("sa_sparse_attn_fwd_fp8", rc)
     return out

@@ -38,6 +38,8 @@
 // wait is bounded by the global timer: a wait that runs out records an error
 // code and the kernel drains and returns instead of hanging.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -107,11 +109,28 @@ constexpr int kLaunchRegs = 128;
 constexpr int kSoftmaxRegs = 160;
 constexpr int kOtherRegs = 96;
 
-template <int DC, int CL>
+// FP8 kv rows (the V4 cache format): 448 dims as E4M3 codes, then 64 RoPE
+// dims as bf16, then one E8M0 scale byte per 64-dim tile of the codes (7 used,
+// 1 pad): 584 bytes, so a row starts on an 8-byte boundary only.
+constexpr int kF8Row = 584;
+constexpr int kF8RopeOff = 448;
+constexpr int kF8ScaleOff = 576;
+
+template <int DC, int CL, bool F8 = false>
 struct Cfg {
     static_assert(DC == 64 || DC == 128 || DC == 256, "per-CTA head-dim slice");
+    static_assert(!F8 || (DC == 256 && CL == 2), "FP8 rows only at D = 512 (two 256-column halves)");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
-    static constexpr int NS = CL == 2 ? 5 : 4;            // kv ring depth
+    static constexpr int NS = F8 ? 4 : (CL == 2 ? 5 : 4);  // kv ring depth (bf16 stages the MMA reads)
+    // FP8: the raw bytes of a tile land in one of NF staging buffers (one
+    // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
+    // values at [0, 320), its scale bytes at 320) and are widened to bf16
+    // into a kv stage by the gather warps
+    static constexpr int NF = F8 ? 2 : 0;
+    static constexpr int STG_ROW = 336;
+    static constexpr int STG_SCALE = 320;
+    static constexpr int STG_BYTES = kBN * STG_ROW;
+    static_assert(STG_SCALE + 8 <= STG_ROW && STG_ROW % 16 == 0, "staging row: 320 data bytes, 8 scale bytes");
     static constexpr int THREADS = (kFirstGatherWarp + kGatherWarps) * 32;
     static_assert(THREADS == 512, "four warpgroups");
     static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
@@ -122,7 +141,9 @@ struct Cfg {
     static constexpr int X_BYTES = XQ_BYTES + 2 * kM * 4; // + 1 KB of steps
     static_assert(X_BYTES % 1024 == 0, "receive buffers keep 1 KB alignment");
     static constexpr int OFF_KV = 0;
-    static constexpr int OFF_X = OFF_KV + NS * STAGE_BYTES;
+    static constexpr int OFF_STG = OFF_KV + NS * STAGE_BYTES;
+    static constexpr int OFF_X = OFF_STG + NF * STG_BYTES;
+    static_assert(OFF_X % 1024 == 0, "receive buffers keep 1 KB alignment");
     static constexpr int OFF_IDX = OFF_X + (CL == 2 ? 2 * X_BYTES : 0);
     static constexpr int OFF_VALID = OFF_IDX + kMaxUnitSlots * 4;
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
@@ -393,13 +414,30 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
     }
 }
 
+// E8M0 scale byte -> 2^(byte - 127) as a float (255 -> NaN; 0 -> 2^-127, a
+// subnormal float).
+__device__ __forceinline__ float e8m0_scale(uint32_t b) {
+    if (b == 255u) return __int_as_float(0x7fc00000);
+    return b == 0u ? __int_as_float(0x00400000) : __int_as_float(int(b << 23));
+}
+
+// two E4M3 codes -> two bf16 values (code * scale), packed low = first code.
+// E4M3 -> f16 is exact, so is f16 -> f32 and the power-of-two scale (barring
+// overflow or results below the bf16 range); the bf16 rounding is then exact.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint16_t codes, float sc) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
 // kPosScale: softmax_scale > 0 (the usual case).  A zero or negative scale
 // takes another instantiation whose softmax leaves invalid slots out
 // explicitly, so the usual one carries no code for it.
-template <int DC, int CL, bool kPosScale>
-__global__ void __launch_bounds__(Cfg<DC, CL>::THREADS, 1)
+template <int DC, int CL, bool kPosScale, bool kFp8>
+__global__ void __launch_bounds__(Cfg<DC, CL, kFp8>::THREADS, 1)
 attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
-    using C = Cfg<DC, CL>;
+    using C = Cfg<DC, CL, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -587,6 +625,88 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // MMA and gather warpgroups: a small register budget
         ptx::setmaxnreg_dec<kOtherRegs>();
         if (warp >= kFirstGatherWarp) {
+          if constexpr (kFp8) {
+            // ------------------------------------------------- gather, FP8 rows
+            // Warp g handles rows g, g + 7, ... of every tile, one row per step,
+            // lane l owning 16 bytes of bf16 output (8 dims): dims 8l.. of this
+            // CTA's half.  Half 0 = dims 0..255 (codes, tiles 0-3); half 1 =
+            // dims 256..447 (codes, tiles 4-6, lanes 0-23) and the 64 RoPE dims
+            // (bf16, lanes 24-31).  A lane copies its own source bytes with
+            // 8-byte cp.async (rows are only 8-byte aligned) into the staging
+            // buffer, lane 0 also the row's 8 scale bytes; one tile later, once
+            // its own copies have landed, the lane widens them to bf16 into the
+            // 128B-swizzled kv stage the MMA reads.  Tile a+1's copies are in
+            // flight while tile a is widened.
+            constexpr int ITERS = (kBN + kGatherWarps - 1) / kGatherWarps;
+            const int g = warp - kFirstGatherWarp;
+            const bool rope = crank == 1 && lane >= 24;
+            const int src_off = crank == 0 ? 8 * lane : (lane < 24 ? 256 + 8 * lane : kF8RopeOff + 16 * (lane - 24));
+            const int stg_off = rope ? 192 + 16 * (lane - 24) : 8 * lane;
+            const int sc_idx = crank == 0 ? (lane >> 3) : 4 + (lane >> 3);   // scale byte of the lane's tile
+            const uint32_t dst_col = uint32_t(lane >> 3) * (kBN * 128);
+            const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
+            auto issue = [&](int a) {
+                const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + (a % C::NF) * C::STG_BYTES);
+                const int32_t *rc = rowc + act[a] * kBN;
+#pragma unroll 2
+                for (int i = 0; i < ITERS; ++i) {
+                    const int r = i * kGatherWarps + g;
+                    if (r >= kBN) break;
+                    const int32_t row = rc[r];
+                    const uint8_t *src = kv8 + (row >= 0 ? int64_t(row) : 0) * kF8Row;
+                    const uint32_t n = row >= 0 ? 8u : 0u;
+                    const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
+                    ptx::cp_async_8(d + stg_off, src + src_off, n);
+                    if (rope) ptx::cp_async_8(d + stg_off + 8, src + src_off + 8, n);
+                    if (lane == 0) ptx::cp_async_8(d + C::STG_SCALE, src + kF8ScaleOff, n);
+                }
+                ptx::cp_async_commit();
+            };
+            if (n_act > 0) issue(0);
+            int a = 0;
+            for (; a < n_act; ++a) {
+                const int s = a % C::NS, f = a / C::NS;
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
+                if (a + 1 < n_act)
+                    issue(a + 1);
+                else
+                    ptx::cp_async_commit();   // an empty group keeps the count uniform
+                ptx::cp_async_wait_group<1>();  // this lane's copies of tile a have landed
+                __syncwarp();                   // ... and lane 0's scale bytes for every lane
+                if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) break;
+                // the last two stages hold Q_c until the softmax warps copied it
+                if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
+                const uint8_t *stg = smem + C::OFF_STG + (a % C::NF) * C::STG_BYTES;
+                uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
+                for (int i = 0; i < ITERS; ++i) {
+                    const int r = i * kGatherWarps + g;
+                    if (r >= kBN) break;
+                    const uint8_t *srow = stg + r * C::STG_ROW;
+                    uint4 out;
+                    if (rope) {
+                        // two 8-byte copies of bf16 values: already the output
+                        const uint2 lo = *reinterpret_cast<const uint2 *>(srow + stg_off);
+                        const uint2 hi = *reinterpret_cast<const uint2 *>(srow + stg_off + 8);
+                        out = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    } else {
+                        const uint2 codes = *reinterpret_cast<const uint2 *>(srow + stg_off);
+                        const float sc = e8m0_scale(srow[C::STG_SCALE + sc_idx]);
+                        out.x = e4m3x2_scaled_bf16x2(uint16_t(codes.x & 0xffffu), sc);
+                        out.y = e4m3x2_scaled_bf16x2(uint16_t(codes.x >> 16), sc);
+                        out.z = e4m3x2_scaled_bf16x2(uint16_t(codes.y & 0xffffu), sc);
+                        out.w = e4m3x2_scaled_bf16x2(uint16_t(codes.y >> 16), sc);
+                    }
+                    *reinterpret_cast<uint4 *>(stage + dst_col + uint32_t(r) * 128u +
+                                               uint32_t((lane & 7) ^ (r & 7)) * 16u) = out;
+                }
+                ptx::fence_proxy_async_smem();   // generic-proxy stores -> MMA reads
+                ptx::mbar_arrive(kv_full(s));
+                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
+                __syncwarp();                    // every lane done with the staging row before it is refilled
+            }
+            ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
+          } else {
             // ------------------------------------------------------------ gather
             // every gather warp copies its share of the rows of every tile; each
             // lane's copies arrive on the stage's mbarrier when they land, so a
@@ -633,6 +753,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             }
             ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
             (void)ok;
+          }
         } else {
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
@@ -1185,25 +1306,25 @@ cudaError_t encode_q_map(CUtensorMap *m, const AttnArgs &a) {
 }
 
 // Opt the kernel into its dynamic shared memory once per device.
-template <int DC, int CL>
+template <int DC, int CL, bool F8>
 cudaError_t prepare_kernel(int dev) {
-    using C = Cfg<DC, CL>;
+    using C = Cfg<DC, CL, F8>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [dev] {
-        attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, true>,
+        attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, true, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (attr_err[dev] == cudaSuccess)
-            attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, false>,
+            attr_err[dev] = cudaFuncSetAttribute(attn_tc_kernel<DC, CL, false, F8>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         // The warpgroups' setmaxnreg split is drawn from the launch allocation;
         // a build that launched with fewer registers per thread could never
         // satisfy the softmax warpgroups' increase, so it is not launched.
         cudaFuncAttributes fa{};
         for (int k = 0; k < 2 && attr_err[dev] == cudaSuccess; ++k) {
-            attr_err[dev] = k == 0 ? cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, true>)
-                                   : cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, false>);
+            attr_err[dev] = k == 0 ? cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, true, F8>)
+                                   : cudaFuncGetAttributes(&fa, attn_tc_kernel<DC, CL, false, F8>);
             if (attr_err[dev] == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err[dev] = cudaErrorInvalidConfiguration;
         }
     });
@@ -1213,14 +1334,14 @@ cudaError_t prepare_kernel(int dev) {
 // Whether a token's ns splits are combined inside the kernel: they must fit
 // one portable cluster together with their head-dim halves, and such a
 // cluster must be placeable on this device (asked once per cluster size).
-template <int DC, int CL>
+template <int DC, int CL, bool F8>
 bool fused_combine(int dev, int ns) {
-    using C = Cfg<DC, CL>;
+    using C = Cfg<DC, CL, F8>;
     static std::once_flag fit_once[kMaxDev][kMaxFusedCluster + 1];
     static bool fits[kMaxDev][kMaxFusedCluster + 1];
     const int cs = CL * ns;
     if (ns < 2 || cs > kMaxFusedCluster || dev < 0 || dev >= kMaxDev) return false;
-    if (prepare_kernel<DC, CL>(dev) != cudaSuccess) return false;
+    if (prepare_kernel<DC, CL, F8>(dev) != cudaSuccess) return false;
     std::call_once(fit_once[dev][cs], [dev, cs] {
         cudaLaunchConfig_t q{};
         q.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
@@ -1234,20 +1355,20 @@ bool fused_combine(int dev, int ns) {
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL, true>, &q);
+        const cudaError_t qe = cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<DC, CL, true, F8>, &q);
         fits[dev][cs] = qe == cudaSuccess && n >= 1;
         (void)cudaGetLastError();   // a refused query is not a launch error
     });
     return fits[dev][cs];
 }
 
-template <int DC, int CL>
+template <int DC, int CL, bool F8>
 cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
-    using C = Cfg<DC, CL>;
+    using C = Cfg<DC, CL, F8>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = prepare_kernel<DC, CL>(dev);
+    e = prepare_kernel<DC, CL, F8>(dev);
     if (e != cudaSuccess) return e;
 
     TcParams p{};
@@ -1263,7 +1384,7 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.num_splits = a.num_splits;
     p.unit_slots = int(split_slots(a.K, a.num_splits));
     const int cs_fused = CL * a.num_splits;
-    const bool fused = fused_combine<DC, CL>(dev, a.num_splits);
+    const bool fused = fused_combine<DC, CL, F8>(dev, a.num_splits);
     p.fused = fused ? 1 : 0;
     *fused_out = fused;
     p.scale_log2 = a.scale * kLog2e;
@@ -1289,8 +1410,8 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     CUtensorMap qmap;
     e = encode_q_map(&qmap, a);
     if (e != cudaSuccess) return e;
-    return a.scale > 0.f ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, true>, p, qmap)
-                         : cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, false>, p, qmap);
+    return a.scale > 0.f ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, true, F8>, p, qmap)
+                         : cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, false, F8>, p, qmap);
 }
 
 }  // namespace
@@ -1308,12 +1429,17 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stre
     if (a.B * a.S == 0) return cudaSuccess;
     cudaError_t e;
     bool fused = false;
-    switch (a.D) {
-        case 64: e = launch_tc<64, 1>(a, stream, &fused); break;
-        case 128: e = launch_tc<128, 1>(a, stream, &fused); break;
-        case 256: e = launch_tc<256, 1>(a, stream, &fused); break;
-        case 512: e = launch_tc<256, 2>(a, stream, &fused); break;
-        default: return cudaErrorInvalidValue;
+    if (a.kv_fp8) {
+        if (a.D != 512) return cudaErrorInvalidValue;
+        e = launch_tc<256, 2, true>(a, stream, &fused);
+    } else {
+        switch (a.D) {
+            case 64: e = launch_tc<64, 1, false>(a, stream, &fused); break;
+            case 128: e = launch_tc<128, 1, false>(a, stream, &fused); break;
+            case 256: e = launch_tc<256, 1, false>(a, stream, &fused); break;
+            case 512: e = launch_tc<256, 2, false>(a, stream, &fused); break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
@@ -1322,17 +1448,22 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stre
     return cudaSuccess;
 }
 
-int kernels_per_call(int64_t D, int num_splits) {
+int kernels_per_call(int64_t D, int num_splits, bool kv_fp8) {
     if (num_splits <= 1) return 1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     bool fused = false;
-    switch (D) {
-        case 64: fused = fused_combine<64, 1>(dev, num_splits); break;
-        case 128: fused = fused_combine<128, 1>(dev, num_splits); break;
-        case 256: fused = fused_combine<256, 1>(dev, num_splits); break;
-        case 512: fused = fused_combine<256, 2>(dev, num_splits); break;
-        default: return 0;
+    if (kv_fp8) {
+        if (D != 512) return 0;
+        fused = fused_combine<256, 2, true>(dev, num_splits);
+    } else {
+        switch (D) {
+            case 64: fused = fused_combine<64, 1, false>(dev, num_splits); break;
+            case 128: fused = fused_combine<128, 1, false>(dev, num_splits); break;
+            case 256: fused = fused_combine<256, 1, false>(dev, num_splits); break;
+            case 512: fused = fused_combine<256, 2, false>(dev, num_splits); break;
+            default: return 0;
+        }
     }
     return fused ? 1 : 2;
 }

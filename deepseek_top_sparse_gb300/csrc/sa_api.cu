@@ -173,6 +173,57 @@ sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const fl
     return SA_OK;
 }
 
+int sa_sparse_attn_fp8_launch_count(int64_t B, int64_t S, int64_t H, int64_t K, int num_splits) {
+    if (!attn_sizes_ok(B, S, H, 512, K) || num_splits > 64) return 0;
+    if (B * S == 0) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev) != SA_OK) return 0;
+    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, 512, K, dev.sms));
+    return sa::kernels_per_call(512, splits, true);
+}
+
+sa_status sa_sparse_attn_fwd_fp8(const void *q, const uint8_t *kv_fp8, const float *attn_sink,
+                                 const int32_t *topk_idxs, const int32_t *topk_length, float softmax_scale,
+                                 void *o, int64_t B, int64_t S, int64_t H, int64_t T, int64_t K, int num_splits,
+                                 void *workspace, size_t workspace_bytes, sa_stream_t stream) {
+    constexpr int64_t D = 512;
+    if (B < 0 || S < 0 || H < 0 || T < 0 || K < 0) return SA_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
+    if (num_splits > 64) return SA_ERR_INVALID_ARG;
+    if (!attn_sizes_ok(B, S, H, D, K) || T < 1) return SA_ERR_SHAPE;
+    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S == 0) return SA_OK;
+    if (!q || !kv_fp8 || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_fp8) || !aligned16(o)) return SA_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3) ||
+        (reinterpret_cast<uintptr_t>(topk_length) & 3))
+        return SA_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const sa_status st = current_device(&dev);
+    if (st != SA_OK) return st;
+
+    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms));
+    const size_t need = workspace_bytes_for(B, S, H, D, splits);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
+
+    sa::AttnArgs a{};
+    a.q = q; a.kv = kv_fp8; a.kv_fp8 = true; a.sink = attn_sink; a.idx = topk_idxs; a.topk_len = topk_length;
+    a.scale = softmax_scale; a.o = o;
+    a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
+    a.num_splits = splits;
+    if (splits > 1) {
+        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
+        o_bytes = (o_bytes + 255) / 256 * 256;
+        a.ws_o = static_cast<float *>(workspace);
+        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    }
+    if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return SA_OK;
+}
+
 sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
                                     const int32_t *topk_idxs, float softmax_scale, void *o,
                                     int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,

@@ -25,7 +25,7 @@ cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stre
 
 struct AttnArgs {
     const void *q;          // bf16 [B,S,H,D]
-    const void *kv;         // bf16 [B,T,D]
+    const void *kv;         // bf16 [B,T,D], or uint8 [B,T,584] FP8 rows when kv_fp8
     const float *sink;      // [H]
     const int32_t *idx;     // [B,S,K]
     const int32_t *topk_len;  // [B,S] or nullptr
@@ -39,6 +39,7 @@ struct AttnArgs {
     const uint32_t *mask = nullptr;   // [B, mask_rows, mask_words]
     int64_t mask_rows = 0, mask_words = 0;
     int key_start_word = 0;           // 1: key offset read from mask[b, 0, mask_words - 1]
+    bool kv_fp8 = false;              // kv rows in the FP8 format (D = 512)
 };
 
 // Slots handled by one split (a multiple of the 64-row tile).
@@ -50,7 +51,7 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t stre
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream);
 // Kernels one sparse_attn call enqueues on the current device: 1, or 2 when
 // the splits are too many to combine inside the main kernel (0 on error).
-int kernels_per_call(int64_t D, int num_splits);
+int kernels_per_call(int64_t D, int num_splits, bool kv_fp8 = false);
 
 struct MaskArgs {
     const int32_t *topk;

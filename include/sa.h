@@ -133,6 +133,30 @@ sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const fl
                                          int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
                                          size_t workspace_bytes, sa_stream_t stream);
 
+/* sa_sparse_attn_fwd_topk_length over an FP8 kv cache, D = 512 (the V4 /
+ * FlashMLA "MODEL1" cache: "DeepSeek V4 源码剖析, 第5章", §5.3 head dims
+ * 448 + 64, quantisation tiles of 64, 8 scales a token, V with the RoPE
+ * dims; §5.6 codes dequantised where they are gathered).
+ *   kv_fp8  uint8 [B, T, 584] device, 16-byte aligned; row t of request b:
+ *           bytes [0, 448)   dims 0..447 as FP8 E4M3 codes (OCP: bias 7,
+ *                            subnormals, 0x7F/0xFF NaN, max 448),
+ *           bytes [448, 576) dims 448..511 as bf16, little-endian,
+ *           bytes [576, 583) one E8M0 scale per 64-dim tile of the codes,
+ *                            2^(byte - 127) (255 = NaN); byte 583 unused.
+ *   value of dim d < 448 = e4m3(code) * scale[d / 64]; the rows are widened
+ *   to bf16 on chip (exact unless a value falls below bf16's range) and the
+ *   attention is then that of sa_sparse_attn_fwd_topk_length with D = 512.
+ * q and o are bf16 [B,S,H,512]; workspace as sa_sparse_attn_workspace_size
+ * (B,S,H,512,K,num_splits).  Errors as sa_sparse_attn_fwd_topk_length. */
+sa_status sa_sparse_attn_fwd_fp8(const void *q, const uint8_t *kv_fp8, const float *attn_sink,
+                                 const int32_t *topk_idxs, const int32_t *topk_length, float softmax_scale,
+                                 void *o, int64_t B, int64_t S, int64_t H, int64_t T, int64_t K, int num_splits,
+                                 void *workspace, size_t workspace_bytes, sa_stream_t stream);
+
+/* Kernels one sa_sparse_attn_fwd_fp8 call enqueues (1 or 2); 0 on
+ * unsupported sizes. */
+int sa_sparse_attn_fp8_launch_count(int64_t B, int64_t S, int64_t H, int64_t K, int num_splits);
+
 /* Allocation-free variant of sa_sparse_attn_fwd_splits, for callers that
  * cannot supply device memory: a plain C host program with no device
  * allocator, or a serving loop that plans all memory up front and must not

@@ -153,7 +153,13 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
     }
     double *logit = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
-    double *krow = (double *)malloc(sizeof(double) * (size_t)D);
+    /* the gathered rows of the token's valid slots, widened once (shared by
+     * every head: kv is one head shared by all query heads) */
+    double *krows = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)D);
+    for (int64_t j = 0; j < K; ++j) {
+        const int64_t t = idx[j];
+        if (j < len && t >= 0 && t < T) load_kv_row(J, b * T + t, krows + j * D);
+    }
     for (int64_t h = 0; h < H; ++h) {
         double *orow = out + h * D;
         for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
@@ -166,7 +172,7 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
                 logit[j] = -INFINITY;
                 continue;
             }
-            load_kv_row(J, b * T + t, krow);
+            const double *krow = krows + j * D;
             double dot = 0.0;
             for (int64_t d = 0; d < D; ++d) dot += qrow[d] * krow[d];
             logit[j] = dot * J->scale; /* R8: scale on q.k only */
@@ -187,13 +193,13 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         for (int64_t j = 0; j < K; ++j) {
             if (logit[j] == -INFINITY) continue; /* weight exactly 0 */
             const double w = exp(logit[j] - m) / denom;
-            load_kv_row(J, b * T + idx[j], krow);
+            const double *krow = krows + j * D;
             for (int64_t d = 0; d < D; ++d) orow[d] += w * krow[d];
         }
     }
     free(logit);
     free(qrow);
-    free(krow);
+    free(krows);
 }
 
 static void *attn_worker(void *arg) {

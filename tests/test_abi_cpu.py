@@ -156,3 +156,18 @@ def test_masked_dense_entry_validates_before_any_device_work():
     assert binding.sa_masked_dense_attn_workspace_size(2, 3, 8, 64, 256, 2) == \
         binding.sa_sparse_attn_workspace_size(2, 3, 8, 64, 256, 2)
     assert binding.sa_masked_dense_attn_workspace_size(1, 1, 8, 96, 256, 2) == 0
+
+
+def test_fp8_entry_validates_before_any_device_work():
+    f = binding.sa_sparse_attn_fwd_fp8
+    base = dict(q=16, kv_fp8=16, attn_sink=16, topk_idxs=16, topk_length=None, softmax_scale=0.05, o=32, B=1, S=1,
+                H=128, T=10, K=4, num_splits=0, workspace=None, workspace_bytes=0, stream=None)
+    assert f(**dict(base, H=129)) == 2
+    assert f(**dict(base, K=0)) == 2
+    assert f(**dict(base, T=0)) == 2
+    assert f(**dict(base, kv_fp8=None)) == 1
+    assert f(**dict(base, kv_fp8=8)) == 3          # not 16-byte aligned
+    assert f(**dict(base, topk_length=2)) == 3
+    assert f(**dict(base, softmax_scale=float("nan"))) == 1
+    assert f(**dict(base, B=0)) == 0
+    assert binding.sa_sparse_attn_fp8_launch_count(1, 1, 128, 0, 0) == 0

@@ -1,0 +1,103 @@
+"""GPU parity of sparse_attn over an FP8 kv cache (584-byte V4 rows: E4M3
+codes with E8M0 tile scales, bf16 RoPE dims) against the CPU oracle's
+``sparse_attn_fp8``, which decodes every row exactly.
+
+Bar, element by element: |gpu - oracle| <= 1e-2 + 1e-2 |oracle| (the rows
+widen to bf16 exactly, so the bf16 path's tolerance carries over)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_top_sparse_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def assert_close(gpu: torch.Tensor, ref: np.ndarray, what=""):
+    g = gpu.float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    bad = np.abs(g - ref) > ATOL + RTOL * np.abs(ref)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; first at "
+                             f"{tuple(i)}: gpu={g[tuple(i)]} oracle={ref[tuple(i)]}")
+
+
+def _run(inp: workloads.Fp8AttnInputs, num_splits=0, topk_length=None, sink=None, scale=None):
+    d = inp.to("cuda")
+    s = d.attn_sink if sink is None else sink.cuda()
+    o = binding.sparse_attn_fp8(d.q, d.kv8, s, d.topk_idxs, inp.softmax_scale if scale is None else scale,
+                                num_splits=num_splits,
+                                topk_length=None if topk_length is None else topk_length.cuda())
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    return o
+
+
+@pytest.mark.parametrize("B,S,H,T,K,p,splits", [
+    (1, 2, 8, 100, 64, 0.1, 0),
+    (2, 3, 128, 700, 200, 0.2, 0),
+    (1, 4, 64, 3000, 1152, 0.05, 0),
+    (2, 2, 128, 5000, 1152, 0.3, 2),
+    (1, 1, 128, 9000, 2000, 0.0, 5),     # more splits than fit one cluster: separate combine
+    (3, 1, 16, 300, 129, 0.5, 1),        # ragged last tile, one split
+])
+def test_random_fp8_cases(B, S, H, T, K, p, splits):
+    inp = workloads.random_attn_fp8(B, S, H, T, K, p_invalid=p, seed=B * 97 + T)
+    o = _run(inp, num_splits=splits)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    assert_close(o, want, f"B{B} S{S} H{H} T{T} K{K}")
+
+
+def test_split_count_invariance():
+    inp = workloads.random_attn_fp8(1, 2, 128, 4000, 1152, p_invalid=0.1, seed=5)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    for ns in (1, 2, 3, 4, 9):
+        assert_close(_run(inp, num_splits=ns), want, f"splits={ns}")
+
+
+def test_topk_length():
+    inp = workloads.random_attn_fp8(2, 3, 32, 800, 300, p_invalid=0.1, seed=7)
+    lens = torch.tensor([[0, 1, 300], [65, -4, 1000]], dtype=torch.int32)
+    o = _run(inp, topk_length=lens)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens)
+    assert_close(o, want, "topk_length")
+
+
+def test_edges_all_invalid_sinks_and_scales():
+    inp = workloads.random_attn_fp8(1, 3, 8, 200, 70, p_invalid=0.2, seed=9)
+    inp.topk_idxs[0, 1] = -1                         # a token with no valid slot: o = 0
+    sink = torch.tensor([0.0, float("inf"), float("-inf"), 1.5, -2.0, float("inf"), 0.3, float("-inf")])
+    for scale in (inp.softmax_scale, 0.0, -0.05):
+        o = _run(inp, sink=sink, scale=scale)
+        want = oracle.sparse_attn_fp8(inp.q, inp.kv8, sink, inp.topk_idxs, scale)
+        assert_close(o, want, f"scale={scale}")
+        assert float(o[0, 1].float().abs().max()) == 0.0
+
+
+def test_subnormal_codes_and_extreme_scales():
+    # codes of every class (subnormal, normal, max 448, both signs) under
+    # scales from 2^-40 to 2^10; all values stay inside bf16's normal range
+    g = torch.Generator().manual_seed(11)
+    inp = workloads.random_attn_fp8(1, 2, 8, 64, 64, p_invalid=0.0, seed=11)
+    kv8 = inp.kv8.clone()
+    codes = torch.tensor([0x01, 0x07, 0x08, 0x7E, 0x81, 0xFE, 0x00, 0x80], dtype=torch.uint8)
+    kv8[0, :, :448] = codes[torch.randint(0, 8, (64, 448), generator=g)]
+    kv8[0, :, 576:583] = torch.tensor([87, 100, 127, 137, 110, 120, 127], dtype=torch.uint8)
+    inp.kv8 = kv8
+    o = _run(inp)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    assert_close(o, want, "extreme codes")
+
+
+def test_full_v4_fp8_decode_every_token():
+    inp = workloads.v4_ratio4_decode_fp8()
+    o = _run(inp)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    assert_close(o, want, "V4 ratio-4 decode, FP8 kv")
+    assert binding.sa_sparse_attn_fp8_launch_count(32, 1, 128, 1152) == 1
