@@ -38,8 +38,6 @@
 // wait is bounded by the global timer: a wait that runs out records an error
 // code and the kernel drains and returns instead of hanging.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -113,7 +111,10 @@ constexpr int kOtherRegs = 96;
 // dims as bf16, then one E8M0 scale byte per 64-dim tile of the codes (7 used,
 // 1 pad): 584 bytes, so a row starts on an 8-byte boundary only.
 constexpr int kF8Row = 584;
-constexpr int kF8RopeOff = 448;
+// FP8 gather roles: of the 7 gather warps, the first copy raw rows into the
+// staging ring and the others widen them into the kv stages
+constexpr int kF8CopyWarps = 3;
+constexpr int kF8WidenWarps = kGatherWarps - kF8CopyWarps;
 constexpr int kF8ScaleOff = 576;
 
 template <int DC, int CL, bool F8 = false>
@@ -121,16 +122,16 @@ struct Cfg {
     static_assert(DC == 64 || DC == 128 || DC == 256, "per-CTA head-dim slice");
     static_assert(!F8 || (DC == 256 && CL == 2), "FP8 rows only at D = 512 (two 256-column halves)");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
-    static constexpr int NS = F8 ? 4 : (CL == 2 ? 5 : 4);  // kv ring depth (bf16 stages the MMA reads)
+    static constexpr int NS = F8 ? 3 : (CL == 2 ? 5 : 4);  // kv ring depth (bf16 stages the MMA reads)
     // FP8: the raw bytes of a tile land in one of NF staging buffers (one
     // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
     // values at [0, 320), its scale bytes at 320) and are widened to bf16
     // into a kv stage by the gather warps
-    static constexpr int NF = F8 ? 2 : 0;
+    static constexpr int NF = F8 ? 3 : 0;
     static constexpr int STG_ROW = 336;
     static constexpr int STG_SCALE = 320;
     static constexpr int STG_BYTES = kBN * STG_ROW;
-    static_assert(STG_SCALE + 8 <= STG_ROW && STG_ROW % 16 == 0, "staging row: 320 data bytes, 8 scale bytes");
+    static_assert(STG_SCALE + 16 <= STG_ROW && STG_ROW % 16 == 0, "staging row: 320 data bytes, one 16-byte scale window");
     static constexpr int THREADS = (kFirstGatherWarp + kGatherWarps) * 32;
     static_assert(THREADS == 512, "four warpgroups");
     static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
@@ -153,7 +154,8 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_SINK + kM * 4;
     // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
     // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar (spare) q_smem q_free
-    static constexpr int NUM_BARS = 2 * NS + 18;
+    // FP8: + stg_full[NF] stg_empty[NF]
+    static constexpr int NUM_BARS = 2 * NS + 18 + 2 * NF;
     // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
     // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
     static constexpr int OFF_QS = OFF_KV + (NS - 2) * STAGE_BYTES;
@@ -421,14 +423,47 @@ __device__ __forceinline__ float e8m0_scale(uint32_t b) {
     return b == 0u ? __int_as_float(0x00400000) : __int_as_float(int(b << 23));
 }
 
-// two E4M3 codes -> two bf16 values (code * scale), packed low = first code.
-// E4M3 -> f16 is exact, so is f16 -> f32 and the power-of-two scale (barring
-// overflow or results below the bf16 range); the bf16 rounding is then exact.
-__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint16_t codes, float sc) {
-    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-    return *reinterpret_cast<const uint32_t *>(&b);
+// two E4M3 codes (low byte first) -> two bf16 values code * sc, packed low =
+// first.  E4M3 -> f16 is exact (cvt.rn.f16x2.e4m3x2), so are f16 -> f32 and
+// the power-of-two scale (barring overflow or results below the bf16 range);
+// the bf16 rounding is then exact too.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t codes, float sc) {
+    uint32_t h2, out;
+    float a, b;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(codes)));
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(a), "=f"(b) : "r"(h2));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(b * sc), "f"(a * sc));
+    return out;
+}
+
+// Four E4M3 codes (one word, byte i = code i) -> two bf16x2 words (lo =
+// codes 0,1; hi = codes 2,3), each value code * 2^(sbyte - 127), given
+// s2 = 2^(sbyte - 7) as bf16 in both halves (sbyte <= 134).  Each code's
+// sign goes to bit 15 of a 16-bit lane and its 7 exponent/mantissa bits to
+// bits 10..4: read as bf16 the lane then holds exactly code * 2^-120 (for
+// zero, subnormal and normal codes alike: bf16 has E4M3's mantissa bits and
+// f32's exponent range), and one bf16 multiply by s2, a power of two, makes
+// it code * 2^(sbyte - 127) without rounding unless the result leaves bf16's
+// normal range.  The NaN codes (S.1111.111) need the exact path.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t c, uint32_t s2, uint32_t &lo, uint32_t &hi) {
+    // byte permutes that sign-extend each code to its 16-bit lane (selector
+    // nibbles 8-11 replicate the sign bit of bytes 0-3), then one shift puts
+    // the 7 exponent/mantissa bits at 10..4 with a sign copy at bit 15
+    // (prmt's generic mode; the __byte_perm intrinsic ignores the sign bit of
+    // a selector nibble)
+    uint32_t x0, x1;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(x0) : "r"(c));   // [c0, sign(c0), c1, sign(c1)]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(x1) : "r"(c));   // [c2, sign(c2), c3, sign(c3)]
+    const uint32_t t0 = (x0 << 4) & 0x87F087F0u;
+    const uint32_t t1 = (x1 << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(s2));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(s2));
+}
+
+// nonzero iff one of the four codes is a NaN pattern (low 7 bits all ones)
+__device__ __forceinline__ uint32_t e4m3x4_has_nan(uint32_t c) {
+    return ((c & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
 }
 
 // kPosScale: softmax_scale > 0 (the usual case).  A zero or negative scale
@@ -478,6 +513,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     const uint32_t l_bar = bar(2 * C::NS + 14);
     const uint32_t q_smem = bar(2 * C::NS + 16);   // Q_c landed in shared memory
     const uint32_t q_free = bar(2 * C::NS + 17);   // Q_c copied to TMEM: its stages are free
+    auto stg_full = [&](int f) { return bar(2 * C::NS + 18 + f); };           // FP8: staging f landed
+    auto stg_empty = [&](int f) { return bar(2 * C::NS + 18 + C::NF + f); };  // FP8: staging f widened
 
     // ---------------------------------------------------------------- prologue
     if (tid == 0) SA_TRACE_POINT(3, 0, 0);
@@ -523,7 +560,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     }
     if (tid == 0) {
         for (int s = 0; s < C::NS; ++s) {
-            ptx::mbar_init(kv_full(s), 32 * kGatherWarps);
+            ptx::mbar_init(kv_full(s), kFp8 ? 32 * kF8WidenWarps : 32 * kGatherWarps);
             ptx::mbar_init(kv_empty(s), 1);
         }
         ptx::mbar_init(s_full, 1);
@@ -541,6 +578,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         ptx::mbar_init(l_bar, kSoftmaxThreads);
         ptx::mbar_init(q_smem, 1);
         ptx::mbar_init(q_free, kSoftmaxThreads);
+        for (int f = 0; f < C::NF; ++f) {
+            ptx::mbar_init(stg_full(f), 32 * kF8CopyWarps);
+            ptx::mbar_init(stg_empty(f), kF8WidenWarps);
+        }
         ptx::fence_mbar_init();
         // Q_c of this unit: DC / 64 boxes of 128 head rows x 64 columns
         ptx::mbar_arrive_expect_tx(q_smem, C::Q_BYTES);
@@ -627,83 +668,156 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         if (warp >= kFirstGatherWarp) {
           if constexpr (kFp8) {
             // ------------------------------------------------- gather, FP8 rows
-            // Warp g handles rows g, g + 7, ... of every tile, one row per step,
-            // lane l owning 16 bytes of bf16 output (8 dims): dims 8l.. of this
-            // CTA's half.  Half 0 = dims 0..255 (codes, tiles 0-3); half 1 =
-            // dims 256..447 (codes, tiles 4-6, lanes 0-23) and the 64 RoPE dims
-            // (bf16, lanes 24-31).  A lane copies its own source bytes with
-            // 8-byte cp.async (rows are only 8-byte aligned) into the staging
-            // buffer, lane 0 also the row's 8 scale bytes; one tile later, once
-            // its own copies have landed, the lane widens them to bf16 into the
-            // 128B-swizzled kv stage the MMA reads.  Tile a+1's copies are in
-            // flight while tile a is widened.
-            constexpr int ITERS = (kBN + kGatherWarps - 1) / kGatherWarps;
-            const int g = warp - kFirstGatherWarp;
-            const bool rope = crank == 1 && lane >= 24;
-            const int src_off = crank == 0 ? 8 * lane : (lane < 24 ? 256 + 8 * lane : kF8RopeOff + 16 * (lane - 24));
-            const int stg_off = rope ? 192 + 16 * (lane - 24) : 8 * lane;
-            const int sc_idx = crank == 0 ? (lane >> 3) : 4 + (lane >> 3);   // scale byte of the lane's tile
-            const uint32_t dst_col = uint32_t(lane >> 3) * (kBN * 128);
+            // This CTA needs bytes [0, 256) of a row (half 0: codes of dims
+            // 0..255) or [256, 576) (half 1: codes of dims 256..447, then the
+            // 64 RoPE dims in bf16), plus the scale bytes [576, 584).  A row
+            // starts 8 bytes past a 16-byte boundary when its index is odd, so
+            // the copies are the 16-byte-aligned windows covering those bytes
+            // (16-byte cp.async, L2 only): an odd row's first window starts 8
+            // bytes early, inside the previous row, and for half 1 its last
+            // window holds the scale bytes; otherwise one more window brings
+            // them.  In a staging row the wanted bytes then start at `shift`
+            // (0 for an even row, 8 for an odd one) and the scale bytes sit at
+            // STG_SCALE + shift.
+            //
+            // Copy warps: a tile is W copy items a row (windows, then the scale
+            // copy; W = 18 for half 0, 21 for half 1), 32 consecutive items per
+            // instruction, instructions dealt round-robin to the copy warps;
+            // every lane's copies arrive on stg_full when they land, so the
+            // copy warps run NF tiles ahead.  Widen warps: lane l turns 8 dims
+            // (8l.. of this half; lanes 24-31 of half 1 pass the RoPE dims
+            // through) of rows w, w + 3, ... into bf16 in the 128B-swizzled kv
+            // stage the MMA reads, then free the staging buffer.
             const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
-            auto issue = [&](int a) {
-                const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + (a % C::NF) * C::STG_BYTES);
-                const int32_t *rc = rowc + act[a] * kBN;
-#pragma unroll 2
-                for (int i = 0; i < ITERS; ++i) {
-                    const int r = i * kGatherWarps + g;
-                    if (r >= kBN) break;
-                    const int32_t row = rc[r];
-                    const uint8_t *src = kv8 + (row >= 0 ? int64_t(row) : 0) * kF8Row;
-                    const uint32_t n = row >= 0 ? 8u : 0u;
-                    const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
-                    ptx::cp_async_8(d + stg_off, src + src_off, n);
-                    if (rope) ptx::cp_async_8(d + stg_off + 8, src + src_off + 8, n);
-                    if (lane == 0) ptx::cp_async_8(d + C::STG_SCALE, src + kF8ScaleOff, n);
-                }
-                ptx::cp_async_commit();
-            };
-            if (n_act > 0) issue(0);
-            int a = 0;
-            for (; a < n_act; ++a) {
-                const int s = a % C::NS, f = a / C::NS;
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
-                if (a + 1 < n_act)
-                    issue(a + 1);
-                else
-                    ptx::cp_async_commit();   // an empty group keeps the count uniform
-                ptx::cp_async_wait_group<1>();  // this lane's copies of tile a have landed
-                __syncwarp();                   // ... and lane 0's scale bytes for every lane
-                if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) break;
-                // the last two stages hold Q_c until the softmax warps copied it
-                if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
-                const uint8_t *stg = smem + C::OFF_STG + (a % C::NF) * C::STG_BYTES;
-                uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
-                for (int i = 0; i < ITERS; ++i) {
-                    const int r = i * kGatherWarps + g;
-                    if (r >= kBN) break;
-                    const uint8_t *srow = stg + r * C::STG_ROW;
-                    uint4 out;
-                    if (rope) {
-                        // two 8-byte copies of bf16 values: already the output
-                        const uint2 lo = *reinterpret_cast<const uint2 *>(srow + stg_off);
-                        const uint2 hi = *reinterpret_cast<const uint2 *>(srow + stg_off + 8);
-                        out = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                    } else {
-                        const uint2 codes = *reinterpret_cast<const uint2 *>(srow + stg_off);
-                        const float sc = e8m0_scale(srow[C::STG_SCALE + sc_idx]);
-                        out.x = e4m3x2_scaled_bf16x2(uint16_t(codes.x & 0xffffu), sc);
-                        out.y = e4m3x2_scaled_bf16x2(uint16_t(codes.x >> 16), sc);
-                        out.z = e4m3x2_scaled_bf16x2(uint16_t(codes.y & 0xffffu), sc);
-                        out.w = e4m3x2_scaled_bf16x2(uint16_t(codes.y >> 16), sc);
+            const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
+            const int nwin = crank == 0 ? 16 : 20;            // windows of an even row
+            if (warp < kFirstGatherWarp + kF8CopyWarps) {
+                const int cw = warp - kFirstGatherWarp;
+                const int W = crank == 0 ? 18 : 21;           // copy items per row
+                const int n_instr = (kBN * W + 31) / 32;
+                bool ok = true;
+                for (int a = 0; a < n_act && ok; ++a) {
+                    const int f = a % C::NF;
+                    if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
-                    *reinterpret_cast<uint4 *>(stage + dst_col + uint32_t(r) * 128u +
-                                               uint32_t((lane & 7) ^ (r & 7)) * 16u) = out;
+                    if (cw == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
+                    const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
+                    const int32_t *rc = rowc + act[a] * kBN;
+                    for (int j = cw; j < n_instr; j += kF8CopyWarps) {
+                        const int it = j * 32 + lane;
+                        const int r = it / W, w = it - r * W;
+                        if (r >= kBN) continue;
+                        const int32_t row = rc[r];
+                        const int64_t rr = row >= 0 ? int64_t(row) : 0;
+                        const uint32_t n = row >= 0 ? 16u : 0u;
+                        const int shift = int(rr & 1) * 8;
+                        const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
+                        const int nw = nwin + (shift >> 3);
+                        // one 16-byte copy per item, the same instruction for
+                        // every lane: a window, or the scale window (an even
+                        // row's [576, 592) reads only its 8 scale bytes, the
+                        // rest is zero-filled; half 0 of an odd row takes
+                        // [568, 584); half 1 of an odd row has it as its last
+                        // window), or nothing
+                        const bool win = w < nw;
+                        const bool scl = w == nw && (!shift || crank == 0);
+                        const uint8_t *src = kv8 + rr * kF8Row + (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
+                        const uint32_t dst = d + (win ? 16u * uint32_t(w) : uint32_t(C::STG_SCALE));
+                        if (win || scl) ptx::cp_async_16(dst, src, win || shift ? n : (n >> 1));
+                    }
+                    ptx::cp_async_arrive_noinc(stg_full(f));
                 }
-                ptx::fence_proxy_async_smem();   // generic-proxy stores -> MMA reads
-                ptx::mbar_arrive(kv_full(s));
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
-                __syncwarp();                    // every lane done with the staging row before it is refilled
+            } else {
+                // widen warps: half-warp h of warp ww takes rows 2 (ww + W i) + h;
+                // lane u of the half-warp owns 16 dims (16u.. of this half): 16
+                // codes, or for u >= 12 of half 1 the RoPE dims 448 + 16 (u - 12)
+                // as bf16, and stores them as two 16-byte chunks, odd chunk
+                // first in every other 64-dim block so each 8-lane store phase
+                // covers eight distinct bank groups
+                const int ww = warp - kFirstGatherWarp - kF8CopyWarps;
+                const int h = lane >> 4, u = lane & 15;
+                constexpr int IT = kBN / (2 * kF8WidenWarps) + (kBN % (2 * kF8WidenWarps) ? 1 : 0);
+                constexpr int CB = 4;                                            // row pairs per load batch
+                const bool rope = crank == 1 && u >= 12;
+                const int sc_idx = crank == 0 ? (u >> 2) : 4 + (u >> 2);         // scale byte of the lane's tile
+                const int off = rope ? 192 + 32 * (u - 12) : 16 * u;             // lane's bytes in a staging row
+                const uint32_t blk = uint32_t(u >> 2);                           // 64-dim block of the stage
+                const uint32_t c_first = 2u * uint32_t(u & 3) + (blk & 1u);      // chunk stored first
+                for (int a = 0; a < n_act; ++a) {
+                    const int s = a % C::NS, fs = a / C::NS, f = a % C::NF;
+                    if (!wait_all(stg_full(f), (a / C::NF) & 1)) break;
+                    if (fs >= 1 && !wait_all(kv_empty(s), (fs - 1) & 1)) break;
+                    // the last two stages hold Q_c until the softmax warps copied it
+                    if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
+                    if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
+                    const uint8_t *stg = smem + C::OFF_STG + f * C::STG_BYTES;
+                    uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
+                    const int32_t *rc = rowc + act[a] * kBN;
+#pragma unroll
+                    for (int i0 = 0; i0 < IT; i0 += CB) {
+                        // every load of the batch before the first conversion
+                        uint2 v[CB][2], w[CB][2];
+                        uint32_t sb[CB];
+#pragma unroll
+                        for (int k = 0; k < CB; ++k) {
+                            const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
+                            if (i0 + k >= IT || r >= kBN) break;
+                            const int32_t row = rc[r];
+                            const int shift = row > 0 ? (row & 1) * 8 : 0;   // as copied (an invalid row came as row 0)
+                            const uint8_t *srow = stg + r * C::STG_ROW;
+                            const uint8_t *src = srow + shift + off;
+                            v[k][0] = *reinterpret_cast<const uint2 *>(src);
+                            v[k][1] = *reinterpret_cast<const uint2 *>(src + 8);
+                            if (rope) {
+                                w[k][0] = *reinterpret_cast<const uint2 *>(src + 16);
+                                w[k][1] = *reinterpret_cast<const uint2 *>(src + 24);
+                            }
+                            sb[k] = srow[C::STG_SCALE + shift + sc_idx];
+                        }
+#pragma unroll
+                        for (int k = 0; k < CB; ++k) {
+                            const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
+                            if (i0 + k >= IT || r >= kBN) break;
+                            uint4 o0, o1;   // dims 0-7 and 8-15 of the lane's 16
+                            if (rope) {
+                                o0 = make_uint4(v[k][0].x, v[k][0].y, v[k][1].x, v[k][1].y);
+                                o1 = make_uint4(w[k][0].x, w[k][0].y, w[k][1].x, w[k][1].y);
+                            } else {
+                                const uint32_t nan = e4m3x4_has_nan(v[k][0].x) | e4m3x4_has_nan(v[k][0].y) |
+                                                     e4m3x4_has_nan(v[k][1].x) | e4m3x4_has_nan(v[k][1].y);
+                                if (sb[k] <= 134u && !nan) {
+                                    const uint32_t s2 = ((sb[k] + 120u) << 7) * 0x00010001u;   // 2^(sb - 7), bf16 x2
+                                    e4m3x4_to_bf16x4(v[k][0].x, s2, o0.x, o0.y);
+                                    e4m3x4_to_bf16x4(v[k][0].y, s2, o0.z, o0.w);
+                                    e4m3x4_to_bf16x4(v[k][1].x, s2, o1.x, o1.y);
+                                    e4m3x4_to_bf16x4(v[k][1].y, s2, o1.z, o1.w);
+                                } else {   // NaN codes or a scale above 2^7: exact conversions
+                                    const float sc = e8m0_scale(sb[k]);
+                                    o0.x = e4m3x2_scaled_bf16x2(v[k][0].x & 0xffffu, sc);
+                                    o0.y = e4m3x2_scaled_bf16x2(v[k][0].x >> 16, sc);
+                                    o0.z = e4m3x2_scaled_bf16x2(v[k][0].y & 0xffffu, sc);
+                                    o0.w = e4m3x2_scaled_bf16x2(v[k][0].y >> 16, sc);
+                                    o1.x = e4m3x2_scaled_bf16x2(v[k][1].x & 0xffffu, sc);
+                                    o1.y = e4m3x2_scaled_bf16x2(v[k][1].x >> 16, sc);
+                                    o1.z = e4m3x2_scaled_bf16x2(v[k][1].y & 0xffffu, sc);
+                                    o1.w = e4m3x2_scaled_bf16x2(v[k][1].y >> 16, sc);
+                                }
+                            }
+                            uint8_t *line = stage + blk * (kBN * 128) + uint32_t(r) * 128u;
+                            const uint32_t c0 = c_first, c1 = c_first ^ 1u;   // chunk of dims 0-7 is 2(u&3)
+                            const uint4 first = (c0 & 1u) ? o1 : o0, second = (c0 & 1u) ? o0 : o1;
+                            *reinterpret_cast<uint4 *>(line + ((c0 ^ uint32_t(r & 7)) << 4)) = first;
+                            *reinterpret_cast<uint4 *>(line + ((c1 ^ uint32_t(r & 7)) << 4)) = second;
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();   // generic-proxy stores -> MMA reads
+                    ptx::mbar_arrive(kv_full(s));
+                    __syncwarp();                    // every lane done with the staging rows ...
+                    if (lane == 0) ptx::mbar_arrive(stg_empty(f));   // ... before they are refilled
+                    if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
+                }
             }
             ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
           } else {

@@ -101,3 +101,23 @@ def test_full_v4_fp8_decode_every_token():
     want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
     assert_close(o, want, "V4 ratio-4 decode, FP8 kv")
     assert binding.sa_sparse_attn_fp8_launch_count(32, 1, 128, 1152) == 1
+
+
+@pytest.mark.parametrize("scale_byte", [134, 127, 135, 150])
+def test_zero_and_subnormal_codes_at_the_fast_and_exact_paths(scale_byte):
+    # only zero and subnormal codes (m * 2^-9) under one scale: at 2^7 the
+    # values are m / 4, so a flushed subnormal would show; scale bytes above
+    # 134 take the exact conversion path
+    g = torch.Generator().manual_seed(scale_byte)
+    inp = workloads.random_attn_fp8(1, 2, 16, 64, 64, p_invalid=0.0, seed=13)
+    kv8 = inp.kv8.clone()
+    sub = torch.tensor([0x00, 0x01, 0x02, 0x03, 0x04, 0x05, 0x06, 0x07,
+                        0x80, 0x81, 0x82, 0x83, 0x84, 0x85, 0x86, 0x87], dtype=torch.uint8)
+    kv8[0, :, :448] = sub[torch.randint(0, 16, (64, 448), generator=g)]
+    kv8[0, :, 576:583] = scale_byte
+    inp.kv8 = kv8
+    dec = oracle.decode_kv_fp8(kv8)
+    assert np.abs(dec[..., :448]).max() > 0
+    o = _run(inp, scale=0.02)
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, 0.02)
+    assert_close(o, want, f"subnormal codes, scale byte {scale_byte}")
