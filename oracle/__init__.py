@@ -72,7 +72,9 @@ def _load():
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
             lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_e8m0_to_double.restype = ctypes.c_double
-            lib.oracle_masked_dense_attn.argtypes = [p, p, p, p, i64, i64, p, ctypes.c_double] + [i64] * 5 + [p]
+            lib.oracle_masked_dense_attn.argtypes = [p, p, p, p, i64, i64, p, p, ctypes.c_double] + [i64] * 5 + [p]
+            lib.oracle_build_topk_mask_window.argtypes = [p, i64, p, i64, i64, i64, i64, i64, p, p, p, p]
+            lib.oracle_build_topk_mask_window.restype = ctypes.c_int
             lib.oracle_topk_mask_shape.argtypes = [i64, i64, i64, ctypes.c_int, p]
             lib.oracle_build_topk_mask.argtypes = [p, i64, p, i64, i64, i64, i64, p, p, p]
             for f in (lib.oracle_sparse_attn, lib.oracle_sparse_attn_tokens, lib.oracle_sparse_attn_tokens_len,
@@ -183,8 +185,9 @@ def sparse_attn_fp8(q, kv8, attn_sink, topk_idxs, softmax_scale: float, tokens=N
     return o.reshape(B, S, H, D) if tokens is None else o
 
 
-def masked_dense_attn(q, kv, attn_sink, mask, softmax_scale: float, key_offset=None):
-    """float64 o[B,S,H,D]: dense attention over the keys the bit mask admits."""
+def masked_dense_attn(q, kv, attn_sink, mask, softmax_scale: float, key_offset=None, key_ends=None):
+    """float64 o[B,S,H,D]: dense attention over the keys the bit mask admits
+    (key_ends: per-request live end in mask positions, or None)."""
     qb, kvb = _bf16_bits(q), _bf16_bits(kv)
     sink = _np(attn_sink, np.float32)
     m = _np(mask, np.int64).astype(np.uint32) if not isinstance(mask, np.ndarray) or mask.dtype != np.uint32 \
@@ -193,9 +196,10 @@ def masked_dense_attn(q, kv, attn_sink, mask, softmax_scale: float, key_offset=N
     T = kvb.shape[1]
     assert m.shape[0] == B and m.shape[1] >= S
     off = None if key_offset is None else np.ascontiguousarray(key_offset, dtype=np.int64)
+    ends = None if key_ends is None else np.ascontiguousarray(_np(key_ends, np.int64))
     o = np.zeros((B, S, H, D), dtype=np.float64)
     rc = _load().oracle_masked_dense_attn(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(m), m.shape[1], m.shape[2],
-                                          _ptr(off), float(softmax_scale), B, S, H, D, T, _ptr(o))
+                                          _ptr(off), _ptr(ends), float(softmax_scale), B, S, H, D, T, _ptr(o))
     if rc != 0:
         raise ValueError(f"oracle_masked_dense_attn rejected its arguments (rc={rc})")
     return o
@@ -230,4 +234,28 @@ def build_topk_mask(topk, cu_q_lens, batch: int, max_q_len: int, max_key_len: in
                                         tk.shape[1], _ptr(ks), _ptr(out), _ptr(shp))
     if rc != 0:
         raise ValueError(f"oracle_build_topk_mask rejected its arguments (rc={rc})")
+    return out
+
+
+def build_topk_mask_window(topk, cu_q_lens, batch: int, q0: int, q_rows: int, max_key_len: int, key_starts=None,
+                           key_ends=None, out: np.ndarray | None = None) -> np.ndarray:
+    """uint32 mask [B, padded(q_rows), W] whose row i is query q0 + i of each
+    request; only words below each request's live end (key_ends, or
+    max_key_len) are written."""
+    tk = _np(topk, np.int32)
+    if tk.ndim == 1:
+        tk = tk.reshape(-1, 1)
+    cu = _np(cu_q_lens, np.int32)
+    assert cu.shape == (batch + 1,)
+    ks = None if key_starts is None else _np(key_starts, np.int32)
+    ke = None if key_ends is None else _np(key_ends, np.int32)
+    shape = topk_mask_shape(batch, q_rows, max_key_len, ks is not None)
+    if out is None:
+        out = np.zeros(shape, dtype=np.uint32)
+    assert out.dtype == np.uint32 and out.ndim == 3 and out.flags.c_contiguous
+    shp = np.asarray(out.shape, dtype=np.int64)
+    rc = _load().oracle_build_topk_mask_window(_ptr(tk), tk.shape[0], _ptr(cu), batch, q0, q_rows, max_key_len,
+                                               tk.shape[1], _ptr(ks), _ptr(ke), _ptr(out), _ptr(shp))
+    if rc != 0:
+        raise ValueError(f"oracle_build_topk_mask_window rejected its arguments (rc={rc})")
     return out

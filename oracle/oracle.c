@@ -18,6 +18,13 @@
  *   [MASK-BITS] vLLM PR 48770 page (masked MHA for sparse-MLA prefill), source
  *             excerpt `dense_mask_mod` / `offset_dense_mask_mod`: word kv>>5,
  *             bit kv&31, LSB first; the last word of row q=0 holds key_start.
+ *   [MASK-CAP] same page, review notes: the global mask grows with batch x
+ *             query length x key length, so above a 64 MiB cap the chunked
+ *             mask path takes over.
+ *   [MASK-END] vLLM PR 56628 page: the strided mask kernel stops at each
+ *             row's live end, so its cost follows the live context rather
+ *             than the workspace width, and leaves the columns past the end
+ *             untouched.
  *   [V4-5.3]  same chapter, §5.3: the MODEL1 (V4) constants of FlashMLA --
  *             head dim 512 = 448 "nope" dims + 64 RoPE dims, FP8 quantisation
  *             tiles of 64 dims, 8 scales per token (7 used), V carries the
@@ -293,11 +300,13 @@ int oracle_sparse_attn(const uint16_t *q, const uint16_t *kv, const float *attn_
 /* mask[b, s, :] is set.  Same softmax-with-sink as above over the admitted  */
 /* keys.  key_offset may be NULL (all zero, `dense_mask_mod`); a non-NULL    */
 /* offset is the chunked-context reading (`offset_dense_mask_mod`).          */
+/* key_ends (or NULL): a key at or past request b's live end key_ends[b]     */
+/* (in mask positions, i.e. after the offset) is never admitted (R24).       */
 /* ------------------------------------------------------------------------ */
 int oracle_masked_dense_attn(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
                              const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
-                             const int64_t *key_offset, double softmax_scale, int64_t B,
-                             int64_t S, int64_t H, int64_t D, int64_t T, double *o) {
+                             const int64_t *key_offset, const int64_t *key_ends, double softmax_scale,
+                             int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, double *o) {
     if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || mask_rows < S || mask_words < 0)
         return ORACLE_EINVAL;
     double *logit = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
@@ -312,6 +321,7 @@ int oracle_masked_dense_attn(const uint16_t *q, const uint16_t *kv, const float 
                 for (int64_t t = 0; t < T; ++t) {
                     int64_t key = t + off;
                     int on = key >= 0 && (key >> 5) < mask_words &&
+                             (key_ends == NULL || key < key_ends[b]) &&
                              ((row[key >> 5] >> (key & 31)) & 1u);
                     if (!on) {
                         logit[t] = -INFINITY;
@@ -377,28 +387,39 @@ int oracle_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key
  * cu_q_lens[b] + q with 0 <= k < max_key_len (R14).  Live words are cleared
  * first.  When key_starts is non-NULL, word W-1 of row (b, 0) receives the
  * raw bits of key_starts[b] (R16).  Nothing else is written (R15). */
-int oracle_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
-                           int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
-                           const int32_t *key_starts, uint32_t *mask,
-                           const int64_t mask_shape[3]) {
+/* A window of the mask (reading R24, the chunked fallback of [MASK-CAP]):
+ * row i of `mask` is query q0 + i of each request, for the q_rows queries of
+ * the window; key_ends (or NULL) gives each request's live key end, and only
+ * the words below min(end, max_key_len) of a live row are written (the
+ * strided build that stops at the row's end, [MASK-END]).  Everything else --
+ * words past the end, padding words, rows past a request's query count and
+ * padding rows -- keeps its contents.  The reserved key_start word goes to
+ * row 0 of each request, where the consumer reads it. */
+int oracle_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                                  int64_t B, int64_t q0, int64_t q_rows, int64_t max_key_len, int64_t K,
+                                  const int32_t *key_starts, const int32_t *key_ends, uint32_t *mask,
+                                  const int64_t mask_shape[3]) {
     int64_t want[3];
-    if (oracle_topk_mask_shape(B, max_q_len, max_key_len, key_starts != NULL, want))
+    if (q0 < 0 || oracle_topk_mask_shape(B, q_rows, max_key_len, key_starts != NULL, want))
         return ORACLE_EINVAL;
     if (mask_shape[0] != want[0] || mask_shape[1] != want[1] || mask_shape[2] != want[2])
         return ORACLE_EINVAL;
     const int64_t R = want[1], W = want[2];
-    const int64_t live_words = cdiv64(max_key_len, 32);
     for (int64_t b = 0; b < B; ++b) {
-        int64_t q_len = (int64_t)cu_q_lens[b + 1] - (int64_t)cu_q_lens[b];
-        if (q_len > max_q_len) q_len = max_q_len;
-        for (int64_t qi = 0; qi < q_len; ++qi) {
+        int64_t end = max_key_len;
+        if (key_ends != NULL && (int64_t)key_ends[b] < end) end = key_ends[b] < 0 ? 0 : key_ends[b];
+        const int64_t live_words = cdiv64(end, 32);
+        const int64_t q_len = (int64_t)cu_q_lens[b + 1] - (int64_t)cu_q_lens[b];
+        for (int64_t i = 0; i < q_rows; ++i) {
+            const int64_t qi = q0 + i;
+            if (qi >= q_len) break;
             const int64_t src = (int64_t)cu_q_lens[b] + qi;
             if (src < 0 || src >= topk_rows) continue;
-            uint32_t *row = mask + (b * R + qi) * W;
+            uint32_t *row = mask + (b * R + i) * W;
             for (int64_t w = 0; w < live_words; ++w) row[w] = 0u;
             for (int64_t j = 0; j < K; ++j) {
                 const int64_t k = topk[src * K + j];
-                if (k < 0 || k >= max_key_len) continue;
+                if (k < 0 || k >= end) continue;
                 row[k >> 5] |= 1u << (k & 31);
             }
         }
@@ -406,4 +427,13 @@ int oracle_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t
             mask[(b * R + 0) * W + (W - 1)] = (uint32_t)key_starts[b];
     }
     return ORACLE_OK;
+}
+
+/* The whole mask: the window of every query, no live ends. */
+int oracle_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                           int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
+                           const int32_t *key_starts, uint32_t *mask,
+                           const int64_t mask_shape[3]) {
+    return oracle_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, 0, max_q_len, max_key_len, K, key_starts,
+                                         NULL, mask, mask_shape);
 }

@@ -455,3 +455,73 @@ def test_fp8_attention_equals_bf16_attention_on_the_decoded_rows():
     np.testing.assert_array_equal(
         oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens),
         oracle.sparse_attn(inp.q, kv_bf16, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, topk_length=lens))
+
+
+# ---------------------------------------------------------------- mask windows and live ends
+
+def _mask_case(seed, B=3, max_q=300, keys=700, K=40):
+    rng = np.random.default_rng(seed)
+    q_lens = [int(rng.integers(0, max_q + 1)) for _ in range(B)]
+    topk = rng.integers(-3, keys + 3, size=(sum(q_lens), K)).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    return rng, q_lens, topk, cu
+
+
+def test_mask_window_of_every_query_is_the_whole_mask():
+    _, q_lens, topk, cu = _mask_case(61)
+    full = oracle.build_topk_mask(topk, cu, 3, 300, 700, key_starts=np.array([5, 0, 9], np.int32))
+    win = oracle.build_topk_mask_window(topk, cu, 3, 0, 300, 700, key_starts=np.array([5, 0, 9], np.int32))
+    np.testing.assert_array_equal(win, full)
+
+
+def test_mask_windows_tile_the_whole_mask():
+    # windows of 128 queries, stacked, give the live rows of the whole mask;
+    # each window carries the reserved word in its own row 0
+    _, q_lens, topk, cu = _mask_case(62)
+    ks = np.array([7, 1, 2], np.int32)
+    full = oracle.build_topk_mask(topk, cu, 3, 300, 700, key_starts=ks)
+    W = full.shape[2]
+    for q0 in range(0, 300, 128):
+        win = oracle.build_topk_mask_window(topk, cu, 3, q0, 128, 700, key_starts=ks)
+        assert win.shape == (3, 128, W)
+        for b in range(3):
+            assert win[b, 0, W - 1] == np.uint32(ks[b])
+            for i in range(128):
+                q = q0 + i
+                if q < q_lens[b]:
+                    lw = (700 + 31) // 32
+                    np.testing.assert_array_equal(win[b, i, :lw], full[b, q, :lw])
+
+
+def test_mask_live_end_brute_force():
+    # only the words below each request's live end are written; they hold the
+    # bits of the indices below the end; every other word keeps the sentinel
+    rng, q_lens, topk, cu = _mask_case(63, keys=500)
+    ends = np.array([0, 77, 1000], np.int32)          # empty, ragged, past max_key_len
+    shape = oracle.topk_mask_shape(3, 300, 500)
+    out = np.full(shape, 0xA5A5A5A5, dtype=np.uint32)
+    oracle.build_topk_mask_window(topk, cu, 3, 0, 300, 500, key_ends=ends, out=out)
+    for b in range(3):
+        end = min(int(ends[b]), 500)
+        lw = (end + 31) // 32
+        for q in range(shape[1]):
+            row = out[b, q]
+            if q >= q_lens[b]:
+                assert (row == 0xA5A5A5A5).all()
+                continue
+            want = set(int(k) for k in topk[cu[b] + q] if 0 <= k < end)
+            got = {w * 32 + j for w in range(lw) for j in range(32) if (int(row[w]) >> j) & 1}
+            assert got == want
+            assert (row[lw:] == 0xA5A5A5A5).all()
+
+
+def test_masked_dense_live_end_drops_the_keys_past_it():
+    inp = workloads.random_attn(2, 3, 4, 16, 90, 30, p_invalid=0.1, seed=64)
+    cu = np.array([0, 3, 6], np.int32)
+    m = oracle.build_topk_mask(inp.topk_idxs.reshape(6, -1).numpy(), cu, 2, 3, 90)
+    ends = np.array([41, 90], np.int64)
+    got = oracle.masked_dense_attn(inp.q, inp.kv, inp.attn_sink, m, inp.softmax_scale, key_ends=ends)
+    idx = inp.topk_idxs.clone()
+    idx[0][idx[0] >= 41] = -1
+    want = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, idx, inp.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
