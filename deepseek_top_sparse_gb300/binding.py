@@ -30,7 +30,9 @@ EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_work
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
            "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length",
            "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count",
-           "sa_sparse_attn_fwd_fp8", "sa_sparse_attn_fp8_launch_count")
+           "sa_sparse_attn_fwd_fp8", "sa_sparse_attn_fp8_launch_count", "sa_build_topk_mask_window",
+           "sa_masked_dense_attn_fwd_window", "sa_topk_mask_chunk_rows", "sa_topk_masked_attn_fwd",
+           "sa_topk_masked_attn_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -90,6 +92,18 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_sparse_attn_fwd_fp8.restype = i32
         lib.sa_sparse_attn_fp8_launch_count.argtypes = [i64] * 4 + [i32]
         lib.sa_sparse_attn_fp8_launch_count.restype = i32
+        lib.sa_build_topk_mask_window.argtypes = [p, i64, p, i64, i64, i64, i64, i64, p, p, p, p, p]
+        lib.sa_build_topk_mask_window.restype = i32
+        lib.sa_masked_dense_attn_fwd_window.argtypes = [p, p, p, p, i64, i64, i32, p, ctypes.c_float, p] + \
+            [i64] * 7 + [i32, p, sz, p]
+        lib.sa_masked_dense_attn_fwd_window.restype = i32
+        lib.sa_topk_mask_chunk_rows.argtypes = [i64, i64, i64, i32, i64]
+        lib.sa_topk_mask_chunk_rows.restype = i64
+        lib.sa_topk_masked_attn_fwd.argtypes = [p, p, p, p, i64, p, p, p, ctypes.c_float, p] + [i64] * 8 + \
+            [p, sz, p, sz, p]
+        lib.sa_topk_masked_attn_fwd.restype = i32
+        lib.sa_topk_masked_attn_workspace_size.argtypes = [i64] * 6 + [i32, i64]
+        lib.sa_topk_masked_attn_workspace_size.restype = sz
         lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_longlong]
         lib.sa_selftest_wait_timeout.restype = i32
         lib.sa_device_error.argtypes = [i32]
@@ -181,6 +195,40 @@ def sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K,
     shp = (ctypes.c_int64 * 3)(*[int(v) for v in mask_shape])
     return int(load().sa_build_topk_mask(topk, topk_rows, cu_q_lens, B, max_q_len, max_key_len, K, key_starts,
                                          mask, shp, stream))
+
+
+def sa_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, q0, q_rows, max_key_len, K, key_starts, key_ends,
+                              mask, mask_shape, stream) -> int:
+    shp = (ctypes.c_int64 * 3)(*[int(v) for v in mask_shape])
+    return int(load().sa_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, q0, q_rows, max_key_len, K,
+                                                 key_starts, key_ends, mask, shp, stream))
+
+
+def sa_masked_dense_attn_fwd_window(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word, key_ends,
+                                    softmax_scale, o, B, S_total, q0, S, H, D, T, num_splits, workspace,
+                                    workspace_bytes, stream) -> int:
+    return int(load().sa_masked_dense_attn_fwd_window(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word,
+                                                       key_ends, softmax_scale, o, B, S_total, q0, S, H, D, T,
+                                                       num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_topk_mask_chunk_rows(batch, max_query_len, max_key_len, reserve_key_starts_word, cap_bytes=0) -> int:
+    return int(load().sa_topk_mask_chunk_rows(batch, max_query_len, max_key_len, int(bool(reserve_key_starts_word)),
+                                              cap_bytes))
+
+
+def sa_topk_masked_attn_fwd(q, kv, attn_sink, topk, topk_rows, cu_q_lens, key_starts, key_ends, softmax_scale, o, B,
+                            max_q_len, H, D, T, max_key_len, K, cap_bytes, mask_buf, mask_buf_bytes, workspace,
+                            workspace_bytes, stream) -> int:
+    return int(load().sa_topk_masked_attn_fwd(q, kv, attn_sink, topk, topk_rows, cu_q_lens, key_starts, key_ends,
+                                               softmax_scale, o, B, max_q_len, H, D, T, max_key_len, K, cap_bytes,
+                                               mask_buf, mask_buf_bytes, workspace, workspace_bytes, stream))
+
+
+def sa_topk_masked_attn_workspace_size(B, max_q_len, H, D, T, max_key_len, reserve_key_starts_word,
+                                       cap_bytes=0) -> int:
+    return int(load().sa_topk_masked_attn_workspace_size(B, max_q_len, H, D, T, max_key_len,
+                                                          int(bool(reserve_key_starts_word)), cap_bytes))
 
 
 def sa_selftest_wait_timeout(max_cycles: int) -> int:
@@ -340,4 +388,51 @@ def sparse_attn_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, attn_sink: torch.Tens
                                 float(softmax_scale), _dptr(out), B, S, H, T, K, int(num_splits), _dptr(workspace),
                                 ws_bytes, _stream_ptr(stream))
     _check("sa_sparse_attn_fwd_fp8", rc)
+    return out
+
+
+def build_topk_mask_window(topk: torch.Tensor, cu_q_lens: torch.Tensor, q0: int, q_rows: int, max_key_len: int,
+                           key_starts: torch.Tensor | None = None, key_ends: torch.Tensor | None = None,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Mask window [B, rows, words]: row i is query q0 + i of each request;
+    only the words below each request's live key end are written."""
+    B = cu_q_lens.numel() - 1
+    shape = topk_mask_shape(B, q_rows, max_key_len, key_starts is not None)
+    if out is None:
+        out = torch.zeros(shape, dtype=torch.int32, device=topk.device)
+    if tuple(out.shape) != shape or out.element_size() != 4 or not out.is_contiguous():
+        raise ValueError(f"mask buffer must be a contiguous 32-bit tensor of shape {shape}")
+    tk = topk if topk.dim() == 2 else topk.reshape(-1, topk.shape[-1] if topk.dim() else 1)
+    rc = sa_build_topk_mask_window(_dptr(tk), tk.shape[0], _dptr(cu_q_lens), B, q0, q_rows, max_key_len, tk.shape[1],
+                                   _dptr(key_starts), _dptr(key_ends), _dptr(out), shape, _stream_ptr(stream))
+    _check("sa_build_topk_mask_window", rc)
+    return out
+
+
+def topk_masked_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk: torch.Tensor,
+                     cu_q_lens: torch.Tensor, softmax_scale: float, max_key_len: int,
+                     key_starts: torch.Tensor | None = None, key_ends: torch.Tensor | None = None,
+                     cap_bytes: int = 0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Attention of q bf16 [B, max_q_len, H, D] over the keys its top-k rows
+    select, through the bit-packed mask built and consumed in windows of
+    query rows that fit cap_bytes (0: 64 MiB).  Rows past a request's query
+    count are left unspecified."""
+    B, Q, H, D = q.shape
+    T = kv.shape[1]
+    tk = topk if topk.dim() == 2 else topk.reshape(-1, topk.shape[-1])
+    reserve = key_starts is not None
+    qc = sa_topk_mask_chunk_rows(B, Q, max_key_len, reserve, cap_bytes)
+    if qc < 1:
+        raise ValueError("no window of query rows fits the mask cap")
+    shape = topk_mask_shape(B, qc, max_key_len, reserve)
+    mbuf = torch.empty(shape, dtype=torch.int32, device=q.device)
+    nws = sa_topk_masked_attn_workspace_size(B, Q, H, D, T, max_key_len, reserve, cap_bytes)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    rc = sa_topk_masked_attn_fwd(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(tk), tk.shape[0], _dptr(cu_q_lens),
+                                 _dptr(key_starts), _dptr(key_ends), float(softmax_scale), _dptr(out), B, Q, H, D, T,
+                                 max_key_len, tk.shape[1], int(cap_bytes), _dptr(mbuf), mbuf.numel() * 4, _dptr(ws),
+                                 nws, _stream_ptr(stream))
+    _check("sa_topk_masked_attn_fwd", rc)
     return out

@@ -198,7 +198,13 @@ struct TcParams {
     const uint32_t *mask;     // [B, mask_rows, mask_words]
     int64_t mask_rows, mask_words;
     int key_start_word;       // 1: key_start = mask[b, 0, mask_words - 1] (int32), else 0
+    const int32_t *key_ends;  // [B] live key end (mask positions) per request, or nullptr
+    // q and o rows: token (b, s) of the call is row b * io_S + io_s0 + s of
+    // q and o (a window of io_S query rows per request; io_S = S, io_s0 = 0
+    // for a whole batch)
+    int64_t io_S, io_s0;
 };
+
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
@@ -274,8 +280,8 @@ __device__ __forceinline__ void combine_range(const TcParams &p, int split, int 
 // itself.  (One TMA bulk store per row measured slower: ~60 cycles per bulk
 // operation.)
 template <int DC, typename C>
-__device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *smem, int64_t tok, int split,
-                                              uint32_t crank, int tid) {
+__device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *smem, int64_t tok, int64_t iotok,
+                                              int split, uint32_t crank, int tid) {
     const bool split_out = p.num_splits > 1;
     int cr0 = 0, cr1 = 0;
     if (p.fused) combine_range(p, split, cr0, cr1);
@@ -286,7 +292,7 @@ __device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *
     const int64_t row_bytes = split_out ? p.D * 4 : p.D * 2;
     char *dst = split_out
         ? reinterpret_cast<char *>(p.ws_o + ((tok * p.num_splits + split) * p.H) * p.D + int64_t(crank) * DC)
-        : reinterpret_cast<char *>(p.o + (tok * p.H) * p.D + int64_t(crank) * DC);
+        : reinterpret_cast<char *>(p.o + (iotok * p.H) * p.D + int64_t(crank) * DC);
     dst += c * 16;
     const uint8_t *src = smem + C::OFF_KV + c * 16;
     constexpr int kBatch = 8;
@@ -319,7 +325,8 @@ __device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *
 //      splits from L2.  A split combines at most 64 rows (two or more
 //      splits), which is at most kB passes, so one batch covers them.
 template <int DC, typename C>
-__device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int split,
+__device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int64_t iotok,
+                                             int split,
                                              uint32_t crank, int tid) {
     const int ns = p.num_splits;
     int cr0, cr1;
@@ -403,7 +410,7 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
             }
         }
     }
-    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (tok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
+    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (iotok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
     const int64_t pass_u2 = int64_t(RP) * p.D / 4;
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
@@ -486,6 +493,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     const int64_t tok = unit / p.num_splits;
     const int split = int(unit % p.num_splits);
     const int64_t b = tok / p.S;
+    const int64_t iotok = b * p.io_S + p.io_s0 + (tok - b * p.S);   // this token's row of q and o
     const int64_t slot0 = int64_t(split) * p.unit_slots;
     const int64_t left = p.K - slot0;
     const int nslots = left <= 0 ? 0 : int(left < p.unit_slots ? left : p.unit_slots);
@@ -546,11 +554,13 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             p.key_start_word ? int64_t(int32_t(__ldg(p.mask + b * p.mask_rows * p.mask_words + p.mask_words - 1)))
                              : 0;
         const int64_t row_bits = p.mask_words * 32;
+        const int64_t key_end = p.key_ends != nullptr ? int64_t(__ldg(p.key_ends + b)) : row_bits;
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int j = (u * kWarpsAll + warp) * 32 + lane;
             const int64_t key = slot0 + j + key_start;
-            const bool on = j < nslots && key >= 0 && key < row_bits && ((__ldg(mrow + (key >> 5)) >> (key & 31)) & 1u);
+            const bool on = j < nslots && key >= 0 && key < row_bits && key < key_end &&
+                            ((__ldg(mrow + (key >> 5)) >> (key & 31)) & 1u);
             tv[u] = on ? int32_t(slot0 + j) : -1;
         }
     }
@@ -588,7 +598,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
 #pragma unroll
         for (int c = 0; c < DC / 64; ++c)
             ptx::tma_load_2d(ptx::smem_u32(smem + C::OFF_QS + c * (kM * 128)), &qmap, int32_t(crank) * DC + c * 64,
-                             int32_t(tok * p.H), q_smem);
+                             int32_t(iotok * p.H), q_smem);
         SA_TRACE_POINT(3, 0, 10);
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
@@ -1289,7 +1299,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         ptx::tmem_dealloc(tbase, C::TMEM_COLS);
     }
     // the staged rows leave (all warps); a fused split keeps its own combine rows
-    copy_out_rows<DC, C>(p, smem, tok, split, crank, tid);
+    copy_out_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
     if (tid == 0) SA_TRACE_POINT(3, 0, 7);
     if (p.fused) {
         // Every split of this token has published its partial rows and
@@ -1299,7 +1309,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // others' from L2, in the log-sum-exp form with the sink added once.
         ptx::cluster_sync();
         if (tid == 0) SA_TRACE_POINT(3, 0, 15);
-        combine_rows<DC, C>(p, smem, tok, split, crank, tid);
+        combine_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
     } else if constexpr (CL == 2) {
         ptx::cluster_sync();  // no remote access outlives the partner
     }
@@ -1315,7 +1325,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
 template <int D>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, const float *__restrict__ sink,
-                    __nv_bfloat16 *__restrict__ o, int64_t rows, int64_t H, int ns) {
+                    __nv_bfloat16 *__restrict__ o, int64_t rows, int64_t H, int ns, int64_t S, int64_t io_S,
+                    int64_t io_s0) {
     constexpr int E = D / 32;              // columns per lane
     constexpr int V = E >= 4 ? 4 : 2;      // columns per vector access
     constexpr int G = E / V;               // vectors per lane
@@ -1364,7 +1375,8 @@ attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws
     }
     const float f = zero ? 0.f : 1.f / den;
     const float fn = isnan(s2) ? NAN : f;
-    __nv_bfloat16 *dst = o + row * D + lane * V;
+    const int64_t bq = tok / S;   // o row of token tok: a window of io_S query rows per request
+    __nv_bfloat16 *dst = o + ((bq * io_S + io_s0 + (tok - bq * S)) * H + h) * D + lane * V;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[V * g] * fn, acc[V * g + 1] * fn);
@@ -1409,7 +1421,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 cudaError_t encode_q_map(CUtensorMap *m, const AttnArgs &a) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.B * a.S * a.H)};
+    const int64_t io_S = a.io_S > 0 ? a.io_S : a.S;
+    cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.B * io_S * a.H)};
     cuuint64_t strides[1] = {cuuint64_t(a.D) * 2};
     cuuint32_t box[2] = {64, cuuint32_t(kM)};
     cuuint32_t estr[2] = {1, 1};
@@ -1506,6 +1519,9 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.mask_rows = a.mask_rows;
     p.mask_words = a.mask_words;
     p.key_start_word = a.key_start_word;
+    p.key_ends = a.key_ends;
+    p.io_S = a.io_S > 0 ? a.io_S : a.S;
+    p.io_s0 = a.io_s0;
     if (p.unit_slots > kMaxUnitSlots) return cudaErrorInvalidValue;
 
     const int64_t ctas = a.B * a.S * a.num_splits * CL;
@@ -1584,13 +1600,14 @@ int kernels_per_call(int64_t D, int num_splits, bool kv_fp8) {
 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
     const int64_t rows = a.B * a.S * a.H;
+    const int64_t io_S = a.io_S > 0 ? a.io_S : a.S;   // 0: o holds exactly the call's S rows per request
     if (rows == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
     switch (a.D) {
-        case 64: attn_combine_kernel<64><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits); break;
-        case 128: attn_combine_kernel<128><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits); break;
-        case 256: attn_combine_kernel<256><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits); break;
-        case 512: attn_combine_kernel<512><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits); break;
+        case 64: attn_combine_kernel<64><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 128: attn_combine_kernel<128><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 256: attn_combine_kernel<256><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 512: attn_combine_kernel<512><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -34,6 +34,14 @@ constexpr int64_t kWarpRowWords = 2048;  // 8 KB image per warp: up to 65536 key
 // loads per lane in flight instead.
 constexpr int64_t kSmallRowWords = 768;
 
+// Live key end of request b: max_key_len, or its entry of key_ends clamped to
+// [0, max_key_len] (the build then stops at that row's end).
+__device__ __forceinline__ uint32_t live_end(const int32_t *key_ends, int64_t b, uint32_t max_key) {
+    if (key_ends == nullptr) return max_key;
+    const int32_t e = key_ends[b];
+    return e <= 0 ? 0u : (uint32_t(e) < max_key ? uint32_t(e) : max_key);
+}
+
 __device__ __forceinline__ void or_bit(uint32_t *img, int32_t k, uint32_t key_limit) {
     // (uint32_t)k < key_limit rejects negative and too-large indices at once
     if (static_cast<uint32_t>(k) < key_limit) atomicOr(&img[k >> 5], 1u << (k & 31));
@@ -58,9 +66,9 @@ __device__ __forceinline__ void scatter_row(const int32_t *__restrict__ row, int
 }
 
 __global__ void __launch_bounds__(kMaskThreads)
-build_topk_mask_kernel(MaskArgs a, int64_t live_words, int smem_path) {
+build_topk_mask_kernel(MaskArgs a, int smem_path) {
     extern __shared__ __align__(16) uint32_t row_img[];
-    const uint32_t key_limit = static_cast<uint32_t>(a.max_key_len);
+    const uint32_t max_key = static_cast<uint32_t>(a.max_key_len);
 
     // reserved key_start word of row (b, 0), for every request b
     if (a.key_starts != nullptr && a.rows > 0) {
@@ -72,13 +80,15 @@ build_topk_mask_kernel(MaskArgs a, int64_t live_words, int smem_path) {
     const int64_t n_slots = a.B * a.max_q_len;
     for (int64_t r = blockIdx.x; r < n_slots; r += gridDim.x) {
         // everything below is uniform across the CTA
-        const int64_t b = r / a.max_q_len, q = r % a.max_q_len;
+        const int64_t b = r / a.max_q_len, i = r % a.max_q_len, q = a.q0 + i;
         const int64_t c0 = a.cu_q_lens[b], c1 = a.cu_q_lens[b + 1];
         if (q >= c1 - c0) continue;
         const int64_t src = c0 + q;
         if (src < 0 || src >= a.topk_rows) continue;
         const int32_t *row = a.topk + src * a.K;
-        uint32_t *dst = a.mask + (b * a.rows + q) * a.words;
+        uint32_t *dst = a.mask + (b * a.rows + i) * a.words;
+        const uint32_t key_limit = live_end(a.key_ends, b, max_key);
+        const int64_t live_words = (int64_t(key_limit) + 31) / 32;
 
         if (smem_path) {
             for (int64_t w = threadIdx.x; w < live_words; w += blockDim.x) row_img[w] = 0u;
@@ -107,7 +117,8 @@ struct WarpMaskArgs {
     const int32_t *cu_q_lens;
     const int32_t *key_starts;
     uint32_t *mask;
-    int topk_rows, B, max_q_len, K, rows, words, live_words;
+    const int32_t *key_ends;   // [B] or nullptr
+    int topk_rows, B, max_q_len, K, rows, words, live_words, q0;
     uint32_t key_limit;
 };
 
@@ -127,13 +138,15 @@ build_topk_mask_warp_kernel(WarpMaskArgs a) {
     const int n_slots = a.B * a.max_q_len;
     for (int r = blockIdx.x * kMaskWarps + warp; r < n_slots; r += gridDim.x * kMaskWarps) {
         // everything below is uniform across the warp
-        const int b = r / a.max_q_len, q = r - b * a.max_q_len;
+        const int b = r / a.max_q_len, i = r - b * a.max_q_len, q = a.q0 + i;
         const int c0 = a.cu_q_lens[b], c1 = a.cu_q_lens[b + 1];
         if (q >= c1 - c0) continue;
         const int64_t src = int64_t(c0) + q;
         if (src < 0 || src >= a.topk_rows) continue;
         const int32_t *row = a.topk + src * a.K;
-        uint32_t *dst = a.mask + (int64_t(b) * a.rows + q) * a.words;
+        uint32_t *dst = a.mask + (int64_t(b) * a.rows + i) * a.words;
+        const uint32_t key_limit = live_end(a.key_ends, b, a.key_limit);
+        const int live_words = int((key_limit + 31u) / 32u);
 
         for (int w = lane; w < img_words; w += 32) img[w] = 0u;
         __syncwarp();
@@ -149,21 +162,21 @@ build_topk_mask_warp_kernel(WarpMaskArgs a) {
                 }
 #pragma unroll
                 for (int u = 0; u < kLoadsInFlight; ++u) {
-                    or_bit(img, x[u].x, a.key_limit);
-                    or_bit(img, x[u].y, a.key_limit);
-                    or_bit(img, x[u].z, a.key_limit);
-                    or_bit(img, x[u].w, a.key_limit);
+                    or_bit(img, x[u].x, key_limit);
+                    or_bit(img, x[u].y, key_limit);
+                    or_bit(img, x[u].z, key_limit);
+                    or_bit(img, x[u].w, key_limit);
                 }
             }
         } else {
-            for (int j = lane; j < a.K; j += 32) or_bit(img, __ldcs(row + j), a.key_limit);
+            for (int j = lane; j < a.K; j += 32) or_bit(img, __ldcs(row + j), key_limit);
         }
         __syncwarp();
-        const int nvec = a.live_words / 4;
+        const int nvec = live_words / 4;
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);  // rows start on 16 B (words % 4 == 0)
         const uint4 *s4 = reinterpret_cast<const uint4 *>(img);
         for (int v = lane; v < nvec; v += 32) d4[v] = s4[v];
-        for (int w = nvec * 4 + lane; w < a.live_words; w += 32) dst[w] = img[w];
+        for (int w = nvec * 4 + lane; w < live_words; w += 32) dst[w] = img[w];
         __syncwarp();  // the image is reused by the warp's next row
     }
 }
@@ -178,9 +191,10 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
     const int64_t cap = int64_t(num_sms) * 8;
     const int64_t lim31 = int64_t(1) << 31;
     if (live_words <= kWarpRowWords && a.K < lim31 && a.topk_rows < lim31 && n_slots < lim31 &&
-        a.B + 1 < lim31 && a.rows < lim31 && a.words < lim31) {
+        a.B + 1 < lim31 && a.rows < lim31 && a.words < lim31 && a.q0 + a.max_q_len < lim31) {
         WarpMaskArgs w;
         w.topk = a.topk; w.cu_q_lens = a.cu_q_lens; w.key_starts = a.key_starts; w.mask = a.mask;
+        w.key_ends = a.key_ends; w.q0 = int(a.q0);
         w.topk_rows = int(a.topk_rows); w.B = int(a.B); w.max_q_len = int(a.max_q_len); w.K = int(a.K);
         w.rows = int(a.rows); w.words = int(a.words); w.live_words = int(live_words);
         w.key_limit = static_cast<uint32_t>(a.max_key_len);
@@ -206,8 +220,7 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
     int64_t grid = n_slots;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    build_topk_mask_kernel<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(a, live_words,
-                                                                                       smem_path);
+    build_topk_mask_kernel<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(a, smem_path);
     return cudaGetLastError();
 }
 

@@ -10,6 +10,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Above this size the whole (global) top-k mask is not built at once: it is
+// built and consumed one window of query rows at a time (vLLM PR 48770 page,
+// review notes: GLOBAL_TOPK_MASK_MAX_BYTES = 64 MiB).
+constexpr int64_t kGlobalTopkMaskMaxBytes = int64_t(64) << 20;
+
 struct DeviceInfo {
     int sms = 0;
     int major = 0, minor = 0;
@@ -251,22 +256,26 @@ int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D
     return sa_sparse_attn_launch_count(B, S, H, D, T, num_splits);
 }
 
-sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *attn_sink,
-                                   const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
-                                   int key_start_word, float softmax_scale, void *o, int64_t B, int64_t S,
-                                   int64_t H, int64_t D, int64_t T, int num_splits, void *workspace,
-                                   size_t workspace_bytes, sa_stream_t stream) {
-    if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || mask_rows < 0 || mask_words < 0) return SA_ERR_INVALID_ARG;
+sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const float *attn_sink,
+                                          const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                          int key_start_word, const int32_t *key_ends, float softmax_scale, void *o,
+                                          int64_t B, int64_t S_total, int64_t q0, int64_t S, int64_t H, int64_t D,
+                                          int64_t T, int num_splits, void *workspace, size_t workspace_bytes,
+                                          sa_stream_t stream) {
+    if (B < 0 || S < 0 || S_total < 0 || q0 < 0 || H < 0 || D < 0 || T < 0 || mask_rows < 0 || mask_words < 0)
+        return SA_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
     if (num_splits > 64 || (key_start_word != 0 && key_start_word != 1)) return SA_ERR_INVALID_ARG;
     if (!attn_sizes_ok(B, S, H, D, T) || T < 1) return SA_ERR_SHAPE;
+    if (q0 + S > S_total) return SA_ERR_SHAPE;
     if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
-    if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * S_total * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
     if (mask_rows < S || mask_words < 1 || (mask_words & 3)) return SA_ERR_SHAPE;
     if (B * S == 0) return SA_OK;
     if (!q || !kv || !attn_sink || !mask || !o) return SA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(mask)) return SA_ERR_ALIGNMENT;
-    if (reinterpret_cast<uintptr_t>(attn_sink) & 3) return SA_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(attn_sink) & 3) || (reinterpret_cast<uintptr_t>(key_ends) & 3))
+        return SA_ERR_ALIGNMENT;
     DeviceInfo dev;
     const sa_status st = current_device(&dev);
     if (st != SA_OK) return st;
@@ -280,8 +289,10 @@ sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *a
     a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = nullptr; a.topk_len = nullptr;
     a.scale = softmax_scale; a.o = o;
     a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = T;
+    a.io_S = S_total; a.io_s0 = q0;
     a.num_splits = splits;
     a.mask = mask; a.mask_rows = mask_rows; a.mask_words = mask_words; a.key_start_word = key_start_word;
+    a.key_ends = key_ends;
     if (splits > 1) {
         size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
         o_bytes = (o_bytes + 255) / 256 * 256;
@@ -291,6 +302,75 @@ sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *a
     if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
+}
+
+sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *attn_sink,
+                                   const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                   int key_start_word, float softmax_scale, void *o, int64_t B, int64_t S,
+                                   int64_t H, int64_t D, int64_t T, int num_splits, void *workspace,
+                                   size_t workspace_bytes, sa_stream_t stream) {
+    return sa_masked_dense_attn_fwd_window(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word, nullptr,
+                                           softmax_scale, o, B, S, 0, S, H, D, T, num_splits, workspace,
+                                           workspace_bytes, stream);
+}
+
+int64_t sa_topk_mask_chunk_rows(int64_t batch, int64_t max_query_len, int64_t max_key_len,
+                                int reserve_key_starts_word, int64_t cap_bytes) {
+    if (batch < 1 || max_query_len < 1 || max_key_len < 0) return 0;
+    if (cap_bytes <= 0) cap_bytes = kGlobalTopkMaskMaxBytes;
+    auto bytes = [&](int64_t rows) {
+        int64_t shp[3];
+        sa_topk_mask_shape(batch, rows, max_key_len, reserve_key_starts_word, shp);
+        return shp[0] * shp[1] * shp[2] * 4;
+    };
+    if (bytes(max_query_len) <= cap_bytes) return max_query_len;   // the whole (global) mask
+    // windows past 128 rows pad to multiples of 256
+    const int64_t per256 = bytes(256);
+    int64_t k = per256 > 0 ? cap_bytes / per256 : 0;
+    if (k * 256 >= max_query_len) k = (max_query_len - 1) / 256;
+    if (k >= 1) return k * 256;
+    return bytes(128) <= cap_bytes ? 128 : 0;
+}
+
+sa_status sa_topk_masked_attn_fwd(const void *q, const void *kv, const float *attn_sink, const int32_t *topk,
+                                  int64_t topk_rows, const int32_t *cu_q_lens, const int32_t *key_starts,
+                                  const int32_t *key_ends, float softmax_scale, void *o, int64_t B,
+                                  int64_t max_q_len, int64_t H, int64_t D, int64_t T, int64_t max_key_len, int64_t K,
+                                  int64_t cap_bytes, uint32_t *mask_buf, size_t mask_buf_bytes, void *workspace,
+                                  size_t workspace_bytes, sa_stream_t stream) {
+    if (B < 0 || max_q_len < 0 || H < 0 || D < 0 || T < 0 || max_key_len < 0 || K < 0 || topk_rows < 0)
+        return SA_ERR_INVALID_ARG;
+    if (B * max_q_len == 0) return SA_OK;
+    const int64_t qc = sa_topk_mask_chunk_rows(B, max_q_len, max_key_len, key_starts != nullptr, cap_bytes);
+    if (qc < 1) return SA_ERR_SHAPE;
+    int64_t shp[3];
+    sa_topk_mask_shape(B, qc, max_key_len, key_starts != nullptr, shp);
+    if (mask_buf == nullptr || mask_buf_bytes < size_t(shp[0] * shp[1] * shp[2] * 4)) return SA_ERR_WORKSPACE;
+    const int key_start_word = key_starts != nullptr ? 1 : 0;
+    for (int64_t q0 = 0; q0 < max_q_len; q0 += qc) {
+        const int64_t rows = max_q_len - q0 < qc ? max_q_len - q0 : qc;
+        int64_t ws[3];
+        sa_topk_mask_shape(B, rows, max_key_len, key_starts != nullptr, ws);
+        sa_status st = sa_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, q0, rows, max_key_len, K, key_starts,
+                                                 key_ends, mask_buf, ws, stream);
+        if (st != SA_OK) return st;
+        st = sa_masked_dense_attn_fwd_window(q, kv, attn_sink, mask_buf, ws[1], ws[2], key_start_word, key_ends,
+                                             softmax_scale, o, B, max_q_len, q0, rows, H, D, T, 0, workspace,
+                                             workspace_bytes, stream);
+        if (st != SA_OK) return st;
+    }
+    return SA_OK;
+}
+
+size_t sa_topk_masked_attn_workspace_size(int64_t B, int64_t max_q_len, int64_t H, int64_t D, int64_t T,
+                                          int64_t max_key_len, int reserve_key_starts_word, int64_t cap_bytes) {
+    const int64_t qc = sa_topk_mask_chunk_rows(B, max_q_len, max_key_len, reserve_key_starts_word, cap_bytes);
+    if (qc < 1) return 0;
+    // every window but the last has qc rows; a short last window may plan more splits
+    const int64_t last = max_q_len - (max_q_len - 1) / qc * qc;
+    const size_t a = sa_masked_dense_attn_workspace_size(B, qc, H, D, T, 0);
+    const size_t b = sa_masked_dense_attn_workspace_size(B, last, H, D, T, 0);
+    return a > b ? a : b;
 }
 
 sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_key_len,
@@ -304,37 +384,47 @@ sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_k
     return SA_OK;
 }
 
-sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
-                             int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
-                             const int32_t *key_starts, uint32_t *mask,
-                             const int64_t mask_shape[3], sa_stream_t stream) {
-    if (mask_shape == nullptr || B < 0 || max_q_len < 0 || max_key_len < 0 || K < 0 || topk_rows < 0)
+sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B,
+                                    int64_t q0, int64_t q_rows, int64_t max_key_len, int64_t K,
+                                    const int32_t *key_starts, const int32_t *key_ends, uint32_t *mask,
+                                    const int64_t mask_shape[3], sa_stream_t stream) {
+    if (mask_shape == nullptr || B < 0 || q0 < 0 || q_rows < 0 || max_key_len < 0 || K < 0 || topk_rows < 0)
         return SA_ERR_INVALID_ARG;
-    if (max_key_len > INT32_MAX) return SA_ERR_SHAPE;
+    if (max_key_len > INT32_MAX || q0 > INT32_MAX - q_rows) return SA_ERR_SHAPE;
     int64_t want[3];
-    sa_status st = sa_topk_mask_shape(B, max_q_len, max_key_len, key_starts != nullptr, want);
+    sa_status st = sa_topk_mask_shape(B, q_rows, max_key_len, key_starts != nullptr, want);
     if (st != SA_OK) return st;
     if (mask_shape[0] != want[0] || mask_shape[1] != want[1] || mask_shape[2] != want[2])
         return SA_ERR_SHAPE;
-    const bool any_rows = B * max_q_len > 0 && topk_rows > 0;
+    const bool any_rows = B * q_rows > 0 && topk_rows > 0;
     const bool any_ks = key_starts != nullptr && want[1] > 0 && B > 0;
     if (!any_rows && !any_ks) return SA_OK;
     if (mask == nullptr || cu_q_lens == nullptr) return SA_ERR_INVALID_ARG;
     if (any_rows && K > 0 && topk == nullptr) return SA_ERR_INVALID_ARG;
     if (!aligned16(mask)) return SA_ERR_ALIGNMENT;
-    if ((reinterpret_cast<uintptr_t>(cu_q_lens) & 3) || (reinterpret_cast<uintptr_t>(topk) & 3))
+    if ((reinterpret_cast<uintptr_t>(cu_q_lens) & 3) || (reinterpret_cast<uintptr_t>(topk) & 3) ||
+        (reinterpret_cast<uintptr_t>(key_starts) & 3) || (reinterpret_cast<uintptr_t>(key_ends) & 3))
         return SA_ERR_ALIGNMENT;
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != SA_OK) return st;
     sa::MaskArgs a{};
     a.topk = topk; a.topk_rows = topk_rows; a.cu_q_lens = cu_q_lens;
-    a.B = B; a.max_q_len = max_q_len; a.max_key_len = max_key_len; a.K = K;
+    a.B = B; a.max_q_len = q_rows; a.max_key_len = max_key_len; a.K = K;
     a.key_starts = key_starts; a.mask = mask; a.rows = want[1]; a.words = want[2];
+    a.q0 = q0; a.key_ends = key_ends;
     if (!any_rows) a.max_q_len = 0;  // only the reserved words remain to write
     if (sa::launch_build_topk_mask(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
+}
+
+sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,
+                             int64_t B, int64_t max_q_len, int64_t max_key_len, int64_t K,
+                             const int32_t *key_starts, uint32_t *mask,
+                             const int64_t mask_shape[3], sa_stream_t stream) {
+    return sa_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, 0, max_q_len, max_key_len, K, key_starts,
+                                     nullptr, mask, mask_shape, stream);
 }
 
 int sa_selftest_wait_timeout(long long max_cycles) {

@@ -40,6 +40,10 @@ struct AttnArgs {
     int64_t mask_rows = 0, mask_words = 0;
     int key_start_word = 0;           // 1: key offset read from mask[b, 0, mask_words - 1]
     bool kv_fp8 = false;              // kv rows in the FP8 format (D = 512)
+    const int32_t *key_ends = nullptr;  // bit-mask mode: [B] live key end per request, or nullptr
+    // q / o hold io_S query rows per request and the call covers rows
+    // io_s0 .. io_s0 + S - 1 of each (io_S = 0: io_S = S, io_s0 = 0)
+    int64_t io_S = 0, io_s0 = 0;
 };
 
 // Slots handled by one split (a multiple of the 64-row tile).
@@ -61,6 +65,8 @@ struct MaskArgs {
     const int32_t *key_starts;
     uint32_t *mask;
     int64_t rows, words;    // mask shape [B, rows, words]
+    int64_t q0 = 0;                    // mask row i is query q0 + i of each request
+    const int32_t *key_ends = nullptr; // [B] live key end per request, or nullptr
 };
 cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t stream);
 

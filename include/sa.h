@@ -250,6 +250,70 @@ sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *a
                                    int64_t H, int64_t D, int64_t T, int num_splits, void *workspace,
                                    size_t workspace_bytes, sa_stream_t stream);
 
+/* Builds one window of the mask: row i of `mask` is query q0 + i of each
+ * request (i < q_rows), so a mask larger than a memory budget can be built
+ * and consumed a window at a time (the chunked fallback above the 64 MiB
+ * global-mask cap, vLLM PR 48770 page).  key_ends: int32 [B] device or NULL;
+ * request b's rows get only the words below its live key end
+ * min(max(key_ends[b], 0), max_key_len) written, and indices at or past it are
+ * dropped -- the build stops at each row's live end (vLLM PR 56628 page), so
+ * its cost follows the live context, not the mask width.  mask_shape must
+ * equal sa_topk_mask_shape(B, q_rows, max_key_len, key_starts != NULL); the
+ * reserved key_start word goes to row 0 of each request.  Everything not
+ * written keeps its contents.  Other arguments and errors as
+ * sa_build_topk_mask, which is this call with q0 = 0, q_rows = max_q_len and
+ * key_ends = NULL. */
+sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B,
+                                    int64_t q0, int64_t q_rows, int64_t max_key_len, int64_t K,
+                                    const int32_t *key_starts, const int32_t *key_ends, uint32_t *mask,
+                                    const int64_t mask_shape[3], sa_stream_t stream);
+
+/* sa_masked_dense_attn_fwd for the query rows q0 .. q0 + S - 1 of each
+ * request: q and o are [B, S_total, H, D] (S_total >= q0 + S), mask row s is
+ * query q0 + s (a window from sa_build_topk_mask_window), and key_ends (int32
+ * [B] device, or NULL) admits no key whose mask position (t, plus key_start
+ * with key_start_word) is at or past request b's live end.  Workspace as
+ * sa_masked_dense_attn_workspace_size(B, S, H, D, T, num_splits).  Errors as
+ * sa_masked_dense_attn_fwd, plus SA_ERR_SHAPE for q0 + S > S_total. */
+sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const float *attn_sink,
+                                          const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                          int key_start_word, const int32_t *key_ends, float softmax_scale, void *o,
+                                          int64_t B, int64_t S_total, int64_t q0, int64_t S, int64_t H, int64_t D,
+                                          int64_t T, int num_splits, void *workspace, size_t workspace_bytes,
+                                          sa_stream_t stream);
+
+/* Host-only.  Query rows per window so that one window's mask,
+ * sa_topk_mask_shape(batch, rows, max_key_len, reserve) words of 4 bytes,
+ * fits cap_bytes (<= 0: 64 MiB, the pages' global-mask cap): max_query_len
+ * when the whole mask fits, else the largest multiple of 256 (or 128) that
+ * fits; 0 if not even 128 rows fit. */
+int64_t sa_topk_mask_chunk_rows(int64_t batch, int64_t max_query_len, int64_t max_key_len,
+                                int reserve_key_starts_word, int64_t cap_bytes);
+
+/* Attention of every query over the keys its top-k row selects, through the
+ * bit-packed mask: for each window of sa_topk_mask_chunk_rows(...) query
+ * rows, sa_build_topk_mask_window into mask_buf, then
+ * sa_masked_dense_attn_fwd_window, all enqueued on `stream`.  One window
+ * when the whole mask fits cap_bytes (the global mask), several otherwise
+ * (the chunked fallback).  q, o: bf16 [B, max_q_len, H, D]; kv: bf16
+ * [B, T, D], key t of kv[b] at mask position t + key_starts[b] (0 without
+ * key_starts); topk, cu_q_lens, key_starts, key_ends as in
+ * sa_build_topk_mask_window.  mask_buf: device, 16-byte aligned, at least
+ * one window's mask; workspace: sa_topk_masked_attn_workspace_size bytes.
+ * Rows q >= q_len_b of o are left unspecified.  Returns SA_ERR_SHAPE when no
+ * window fits the cap, SA_ERR_WORKSPACE when mask_buf or the workspace is too
+ * small, else the first error of the calls it makes. */
+sa_status sa_topk_masked_attn_fwd(const void *q, const void *kv, const float *attn_sink, const int32_t *topk,
+                                  int64_t topk_rows, const int32_t *cu_q_lens, const int32_t *key_starts,
+                                  const int32_t *key_ends, float softmax_scale, void *o, int64_t B,
+                                  int64_t max_q_len, int64_t H, int64_t D, int64_t T, int64_t max_key_len, int64_t K,
+                                  int64_t cap_bytes, uint32_t *mask_buf, size_t mask_buf_bytes, void *workspace,
+                                  size_t workspace_bytes, sa_stream_t stream);
+
+/* Workspace bytes sa_topk_masked_attn_fwd needs for these sizes and cap. */
+size_t sa_topk_masked_attn_workspace_size(int64_t B, int64_t max_q_len, int64_t H, int64_t D, int64_t T,
+                                          int64_t max_key_len, int reserve_key_starts_word, int64_t cap_bytes);
+
 /* ------------------------------------------------------------------------ */
 /* diagnostics                                                              */
 /* ------------------------------------------------------------------------ */

@@ -171,3 +171,31 @@ def test_fp8_entry_validates_before_any_device_work():
     assert f(**dict(base, softmax_scale=float("nan"))) == 1
     assert f(**dict(base, B=0)) == 0
     assert binding.sa_sparse_attn_fp8_launch_count(1, 1, 128, 0, 0) == 0
+
+
+def test_mask_chunk_rows_plan():
+    # the whole mask when it fits the 64 MiB cap; else the largest window of
+    # 256-row multiples (or 128 rows) whose mask fits
+    f = binding.sa_topk_mask_chunk_rows
+    assert f(4, 2048, 8193, 1, 0) == 2048                    # 8.5 MB: global mask
+    assert f(4, 2048, 8193, 1, 1 << 20) == 128               # 256 rows would be 1.06 MB
+    assert f(4, 2048, 8193, 1, 100000) == 0                  # not even 128 rows fit
+    assert f(1, 100000, 1 << 20, 0, 0) == 512                # 32 MiB per 256 rows of 2^15 words
+    assert f(2, 300, 700, 0, 60000) == 256
+    assert f(0, 300, 700, 0, 0) == 0
+
+
+def test_window_entries_validate_before_any_device_work():
+    f = binding.sa_masked_dense_attn_fwd_window
+    base = dict(q=16, kv=16, attn_sink=16, mask=16, mask_rows=128, mask_words=8, key_start_word=0, key_ends=None,
+                softmax_scale=0.1, o=32, B=1, S_total=10, q0=4, S=4, H=8, D=64, T=200, num_splits=0,
+                workspace=None, workspace_bytes=0, stream=None)
+    assert f(**dict(base, q0=7)) == 2                        # q0 + S > S_total
+    assert f(**dict(base, q0=-1)) == 1
+    assert f(**dict(base, key_ends=2)) == 3
+    assert f(**dict(base, B=0)) == 0
+    g = binding.sa_build_topk_mask_window
+    shape = binding.sa_topk_mask_shape(2, 16, 100, 0)
+    assert g(16, 4, 16, 2, -1, 16, 100, 8, None, None, 16, shape, None) == 1
+    assert g(16, 4, 16, 2, 0, 16, 100, 8, None, None, 16, (2, 128, 8), None) == 2   # wrong shape
+    assert g(16, 4, 16, 2, 0, 16, 100, 8, None, 6, 16, shape, None) == 3             # key_ends misaligned
