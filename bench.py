@@ -528,6 +528,50 @@ def run_gpu(args):
     return 0
 
 
+def run_profile(args):
+    """STEPS calls of one kernel's workload, each after a 256 MB L2 flush, and
+    nothing else (a profiler's launch filter then sees only these calls)."""
+    from deepseek_top_sparse_gb300 import binding, workloads
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.profile in ("decode", "decode_fp8"):
+        fp8 = args.profile == "decode_fp8"
+        inp = (workloads.v4_ratio4_decode_fp8() if fp8 else workloads.v4_ratio4_decode()).to(dev)
+        B, S, H, D = inp.q.shape
+        K = inp.topk_idxs.shape[-1]
+        out = torch.empty_like(inp.q)
+        ws = binding.workspace_for(B, S, H, D, K, device=dev)
+        if fp8:
+            call = lambda: binding.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                                                   out=out, workspace=ws)
+        else:
+            call = lambda: binding.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale,
+                                               out=out, workspace=ws)
+    else:
+        mi = workloads.topk_mask().to(dev)
+        shape = binding.topk_mask_shape(mi.batch, mi.max_q_len, mi.max_key_len, True)
+        mbuf = torch.zeros(shape, dtype=torch.int32, device=dev)
+        build = lambda: binding.build_topk_mask(mi.topk, mi.cu_q_lens, mi.max_q_len, mi.max_key_len, mi.key_starts,
+                                                out=mbuf)
+        call = build
+        if args.profile == "mask_consumer":
+            build()
+            g = torch.Generator().manual_seed(1005)
+            qm = torch.randn(mi.batch, mi.max_q_len, 8, 64, generator=g).to(torch.bfloat16).to(dev)
+            kvm = torch.randn(mi.batch, mi.max_key_len, 64, generator=g).to(torch.bfloat16).to(dev)
+            sinkm = torch.randn(8, generator=g).to(dev)
+            om = torch.empty_like(qm)
+            call = lambda: binding.masked_dense_attn(qm, kvm, sinkm, mbuf, 0.125, out=om)
+    for _ in range(args.steps):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    err = binding.sa_device_error(True)
+    print(json.dumps({"profile": args.profile, "calls": args.steps, "device_error": err}))
+    return 0 if err == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -537,11 +581,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the hot-L2 graph and the other configurations")
+    ap.add_argument("--profile", choices=["decode", "decode_fp8", "mask", "mask_consumer"], default=None,
+                    help="no timing: run STEPS calls of one workload, each after an L2 flush, for a profiler")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     return run_gpu(args)
 
 
