@@ -131,7 +131,8 @@ struct Cfg {
     static constexpr int STG_ROW = 336;
     static constexpr int STG_SCALE = 320;
     static constexpr int STG_BYTES = kBN * STG_ROW;
-    static_assert(STG_SCALE + 16 <= STG_ROW && STG_ROW % 16 == 0, "staging row: 320 data bytes, one 16-byte scale window");
+    static_assert(STG_SCALE + 16 <= STG_ROW && STG_ROW % 16 == 0,
+                  "staging row: 320 data bytes, one 16-byte scale window");
     static constexpr int THREADS = (kFirstGatherWarp + kGatherWarps) * 32;
     static_assert(THREADS == 512, "four warpgroups");
     static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
@@ -676,208 +677,211 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // MMA and gather warpgroups: a small register budget
         ptx::setmaxnreg_dec<kOtherRegs>();
         if (warp >= kFirstGatherWarp) {
-          if constexpr (kFp8) {
-            // ------------------------------------------------- gather, FP8 rows
-            // This CTA needs bytes [0, 256) of a row (half 0: codes of dims
-            // 0..255) or [256, 576) (half 1: codes of dims 256..447, then the
-            // 64 RoPE dims in bf16), plus the scale bytes [576, 584).  A row
-            // starts 8 bytes past a 16-byte boundary when its index is odd, so
-            // the copies are the 16-byte-aligned windows covering those bytes
-            // (16-byte cp.async, L2 only): an odd row's first window starts 8
-            // bytes early, inside the previous row, and for half 1 its last
-            // window holds the scale bytes; otherwise one more window brings
-            // them.  In a staging row the wanted bytes then start at `shift`
-            // (0 for an even row, 8 for an odd one) and the scale bytes sit at
-            // STG_SCALE + shift.
-            //
-            // Copy warps: a tile is W copy items a row (windows, then the scale
-            // copy; W = 18 for half 0, 21 for half 1), 32 consecutive items per
-            // instruction, instructions dealt round-robin to the copy warps;
-            // every lane's copies arrive on stg_full when they land, so the
-            // copy warps run NF tiles ahead.  Widen warps: lane l turns 8 dims
-            // (8l.. of this half; lanes 24-31 of half 1 pass the RoPE dims
-            // through) of rows w, w + 3, ... into bf16 in the 128B-swizzled kv
-            // stage the MMA reads, then free the staging buffer.
-            const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
-            const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
-            const int nwin = crank == 0 ? 16 : 20;            // windows of an even row
-            if (warp < kFirstGatherWarp + kF8CopyWarps) {
-                const int cw = warp - kFirstGatherWarp;
-                const int W = crank == 0 ? 18 : 21;           // copy items per row
-                const int n_instr = (kBN * W + 31) / 32;
+            if constexpr (kFp8) {
+                // ------------------------------------------------- gather, FP8 rows
+                // This CTA needs bytes [0, 256) of a row (half 0: codes of dims
+                // 0..255) or [256, 576) (half 1: codes of dims 256..447, then the
+                // 64 RoPE dims in bf16), plus the scale bytes [576, 584).  A row
+                // starts 8 bytes past a 16-byte boundary when its index is odd, so
+                // the copies are the 16-byte-aligned windows covering those bytes
+                // (16-byte cp.async, L2 only): an odd row's first window starts 8
+                // bytes early, inside the previous row, and for half 1 its last
+                // window holds the scale bytes; otherwise one more window brings
+                // them.  In a staging row the wanted bytes then start at `shift`
+                // (0 for an even row, 8 for an odd one) and the scale bytes sit at
+                // STG_SCALE + shift.
+                //
+                // Copy warps: a tile is W copy items a row (windows, then the scale
+                // copy; W = 18 for half 0, 21 for half 1), 32 consecutive items per
+                // instruction, instructions dealt round-robin to the copy warps;
+                // every lane's copies arrive on stg_full when they land, so the
+                // copy warps run NF tiles ahead.  Widen warps: lane l turns 8 dims
+                // (8l.. of this half; lanes 24-31 of half 1 pass the RoPE dims
+                // through) of rows w, w + 3, ... into bf16 in the 128B-swizzled kv
+                // stage the MMA reads, then free the staging buffer.
+                const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
+                const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
+                const int nwin = crank == 0 ? 16 : 20;            // windows of an even row
+                if (warp < kFirstGatherWarp + kF8CopyWarps) {
+                    const int cw = warp - kFirstGatherWarp;
+                    const int W = crank == 0 ? 18 : 21;           // copy items per row
+                    const int n_instr = (kBN * W + 31) / 32;
+                    bool ok = true;
+                    for (int a = 0; a < n_act && ok; ++a) {
+                        const int f = a % C::NF;
+                        if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (cw == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
+                        const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
+                        const int32_t *rc = rowc + act[a] * kBN;
+                        for (int j = cw; j < n_instr; j += kF8CopyWarps) {
+                            const int it = j * 32 + lane;
+                            const int r = it / W, w = it - r * W;
+                            if (r >= kBN) continue;
+                            const int32_t row = rc[r];
+                            const int64_t rr = row >= 0 ? int64_t(row) : 0;
+                            const uint32_t n = row >= 0 ? 16u : 0u;
+                            const int shift = int(rr & 1) * 8;
+                            const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
+                            const int nw = nwin + (shift >> 3);
+                            // one 16-byte copy per item, the same instruction for
+                            // every lane: a window, or the scale window (an even
+                            // row's [576, 592) reads only its 8 scale bytes, the
+                            // rest is zero-filled; half 0 of an odd row takes
+                            // [568, 584); half 1 of an odd row has it as its last
+                            // window), or nothing
+                            const bool win = w < nw;
+                            const bool scl = w == nw && (!shift || crank == 0);
+                            const uint8_t *src =
+                                kv8 + rr * kF8Row + (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
+                            const uint32_t dst = d + (win ? 16u * uint32_t(w) : uint32_t(C::STG_SCALE));
+                            if (win || scl) ptx::cp_async_16(dst, src, win || shift ? n : (n >> 1));
+                        }
+                        ptx::cp_async_arrive_noinc(stg_full(f));
+                    }
+                } else {
+                    // widen warps: half-warp h of warp ww takes rows 2 (ww + W i) + h;
+                    // lane u of the half-warp owns 16 dims (16u.. of this half): 16
+                    // codes, or for u >= 12 of half 1 the RoPE dims 448 + 16 (u - 12)
+                    // as bf16, and stores them as two 16-byte chunks, odd chunk
+                    // first in every other 64-dim block so each 8-lane store phase
+                    // covers eight distinct bank groups
+                    const int ww = warp - kFirstGatherWarp - kF8CopyWarps;
+                    const int h = lane >> 4, u = lane & 15;
+                    constexpr int IT = kBN / (2 * kF8WidenWarps) + (kBN % (2 * kF8WidenWarps) ? 1 : 0);
+                    constexpr int CB = 4;                                            // row pairs per load batch
+                    const bool rope = crank == 1 && u >= 12;
+                    const int sc_idx = crank == 0 ? (u >> 2) : 4 + (u >> 2);         // scale byte of the lane's tile
+                    const int off = rope ? 192 + 32 * (u - 12) : 16 * u;             // lane's bytes in a staging row
+                    const uint32_t blk = uint32_t(u >> 2);                           // 64-dim block of the stage
+                    const uint32_t c_first = 2u * uint32_t(u & 3) + (blk & 1u);      // chunk stored first
+                    for (int a = 0; a < n_act; ++a) {
+                        const int s = a % C::NS, fs = a / C::NS, f = a % C::NF;
+                        if (!wait_all(stg_full(f), (a / C::NF) & 1)) break;
+                        if (fs >= 1 && !wait_all(kv_empty(s), (fs - 1) & 1)) break;
+                        // the last two stages hold Q_c until the softmax warps copied it
+                        if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
+                        if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
+                        const uint8_t *stg = smem + C::OFF_STG + f * C::STG_BYTES;
+                        uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
+                        const int32_t *rc = rowc + act[a] * kBN;
+#pragma unroll
+                        for (int i0 = 0; i0 < IT; i0 += CB) {
+                            // every load of the batch before the first conversion
+                            uint2 v[CB][2], w[CB][2];
+                            uint32_t sb[CB];
+#pragma unroll
+                            for (int k = 0; k < CB; ++k) {
+                                const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
+                                if (i0 + k >= IT || r >= kBN) break;
+                                const int32_t row = rc[r];
+                                // as copied (an invalid row came as row 0)
+                                const int shift = row > 0 ? (row & 1) * 8 : 0;
+                                const uint8_t *srow = stg + r * C::STG_ROW;
+                                const uint8_t *src = srow + shift + off;
+                                v[k][0] = *reinterpret_cast<const uint2 *>(src);
+                                v[k][1] = *reinterpret_cast<const uint2 *>(src + 8);
+                                if (rope) {
+                                    w[k][0] = *reinterpret_cast<const uint2 *>(src + 16);
+                                    w[k][1] = *reinterpret_cast<const uint2 *>(src + 24);
+                                }
+                                sb[k] = srow[C::STG_SCALE + shift + sc_idx];
+                            }
+#pragma unroll
+                            for (int k = 0; k < CB; ++k) {
+                                const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
+                                if (i0 + k >= IT || r >= kBN) break;
+                                uint4 o0, o1;   // dims 0-7 and 8-15 of the lane's 16
+                                if (rope) {
+                                    o0 = make_uint4(v[k][0].x, v[k][0].y, v[k][1].x, v[k][1].y);
+                                    o1 = make_uint4(w[k][0].x, w[k][0].y, w[k][1].x, w[k][1].y);
+                                } else {
+                                    const uint32_t nan = e4m3x4_has_nan(v[k][0].x) | e4m3x4_has_nan(v[k][0].y) |
+                                                         e4m3x4_has_nan(v[k][1].x) | e4m3x4_has_nan(v[k][1].y);
+                                    if (sb[k] <= 134u && !nan) {
+                                        // 2^(sb - 7) as bf16, in both halves
+                                        const uint32_t s2 = ((sb[k] + 120u) << 7) * 0x00010001u;
+                                        e4m3x4_to_bf16x4(v[k][0].x, s2, o0.x, o0.y);
+                                        e4m3x4_to_bf16x4(v[k][0].y, s2, o0.z, o0.w);
+                                        e4m3x4_to_bf16x4(v[k][1].x, s2, o1.x, o1.y);
+                                        e4m3x4_to_bf16x4(v[k][1].y, s2, o1.z, o1.w);
+                                    } else {   // NaN codes or a scale above 2^7: exact conversions
+                                        const float sc = e8m0_scale(sb[k]);
+                                        o0.x = e4m3x2_scaled_bf16x2(v[k][0].x & 0xffffu, sc);
+                                        o0.y = e4m3x2_scaled_bf16x2(v[k][0].x >> 16, sc);
+                                        o0.z = e4m3x2_scaled_bf16x2(v[k][0].y & 0xffffu, sc);
+                                        o0.w = e4m3x2_scaled_bf16x2(v[k][0].y >> 16, sc);
+                                        o1.x = e4m3x2_scaled_bf16x2(v[k][1].x & 0xffffu, sc);
+                                        o1.y = e4m3x2_scaled_bf16x2(v[k][1].x >> 16, sc);
+                                        o1.z = e4m3x2_scaled_bf16x2(v[k][1].y & 0xffffu, sc);
+                                        o1.w = e4m3x2_scaled_bf16x2(v[k][1].y >> 16, sc);
+                                    }
+                                }
+                                uint8_t *line = stage + blk * (kBN * 128) + uint32_t(r) * 128u;
+                                const uint32_t c0 = c_first, c1 = c_first ^ 1u;   // chunk of dims 0-7 is 2(u&3)
+                                const uint4 first = (c0 & 1u) ? o1 : o0, second = (c0 & 1u) ? o0 : o1;
+                                *reinterpret_cast<uint4 *>(line + ((c0 ^ uint32_t(r & 7)) << 4)) = first;
+                                *reinterpret_cast<uint4 *>(line + ((c1 ^ uint32_t(r & 7)) << 4)) = second;
+                            }
+                        }
+                        ptx::fence_proxy_async_smem();   // generic-proxy stores -> MMA reads
+                        ptx::mbar_arrive(kv_full(s));
+                        __syncwarp();                    // every lane done with the staging rows ...
+                        if (lane == 0) ptx::mbar_arrive(stg_empty(f));   // ... before they are refilled
+                        if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
+                    }
+                }
+                ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
+            } else {
+                // ------------------------------------------------------------ gather
+                // every gather warp copies its share of the rows of every tile; each
+                // lane's copies arrive on the stage's mbarrier when they land, so a
+                // warp runs ahead into every free stage (up to NS tiles in flight)
+                constexpr int CPR = DC / 8;     // 16-byte chunks per row slice
+                constexpr int RPI = 32 / CPR;   // rows per warp instruction
+                constexpr int STEP = RPI * kGatherWarps;
+                constexpr int ITERS = (kBN + STEP - 1) / STEP;
+                const int g = warp - kFirstGatherWarp;
+                const int sub = lane / CPR, ch = lane % CPR;
+                const uint32_t dst_col = uint32_t(ch >> 3) * (kBN * 128);
+                const char *kvb = reinterpret_cast<const char *>(p.kv) + (int64_t(crank) * DC + ch * 8) * 2;
                 bool ok = true;
-                for (int a = 0; a < n_act && ok; ++a) {
-                    const int f = a % C::NF;
-                    if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) {
+                int a = 0;
+                for (; a < n_act; ++a) {
+                    const int s = a % C::NS, f = a / C::NS;
+                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
+                    if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    if (cw == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
-                    const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
-                    const int32_t *rc = rowc + act[a] * kBN;
-                    for (int j = cw; j < n_instr; j += kF8CopyWarps) {
-                        const int it = j * 32 + lane;
-                        const int r = it / W, w = it - r * W;
-                        if (r >= kBN) continue;
-                        const int32_t row = rc[r];
-                        const int64_t rr = row >= 0 ? int64_t(row) : 0;
-                        const uint32_t n = row >= 0 ? 16u : 0u;
-                        const int shift = int(rr & 1) * 8;
-                        const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
-                        const int nw = nwin + (shift >> 3);
-                        // one 16-byte copy per item, the same instruction for
-                        // every lane: a window, or the scale window (an even
-                        // row's [576, 592) reads only its 8 scale bytes, the
-                        // rest is zero-filled; half 0 of an odd row takes
-                        // [568, 584); half 1 of an odd row has it as its last
-                        // window), or nothing
-                        const bool win = w < nw;
-                        const bool scl = w == nw && (!shift || crank == 0);
-                        const uint8_t *src = kv8 + rr * kF8Row + (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
-                        const uint32_t dst = d + (win ? 16u * uint32_t(w) : uint32_t(C::STG_SCALE));
-                        if (win || scl) ptx::cp_async_16(dst, src, win || shift ? n : (n >> 1));
-                    }
-                    ptx::cp_async_arrive_noinc(stg_full(f));
-                }
-            } else {
-                // widen warps: half-warp h of warp ww takes rows 2 (ww + W i) + h;
-                // lane u of the half-warp owns 16 dims (16u.. of this half): 16
-                // codes, or for u >= 12 of half 1 the RoPE dims 448 + 16 (u - 12)
-                // as bf16, and stores them as two 16-byte chunks, odd chunk
-                // first in every other 64-dim block so each 8-lane store phase
-                // covers eight distinct bank groups
-                const int ww = warp - kFirstGatherWarp - kF8CopyWarps;
-                const int h = lane >> 4, u = lane & 15;
-                constexpr int IT = kBN / (2 * kF8WidenWarps) + (kBN % (2 * kF8WidenWarps) ? 1 : 0);
-                constexpr int CB = 4;                                            // row pairs per load batch
-                const bool rope = crank == 1 && u >= 12;
-                const int sc_idx = crank == 0 ? (u >> 2) : 4 + (u >> 2);         // scale byte of the lane's tile
-                const int off = rope ? 192 + 32 * (u - 12) : 16 * u;             // lane's bytes in a staging row
-                const uint32_t blk = uint32_t(u >> 2);                           // 64-dim block of the stage
-                const uint32_t c_first = 2u * uint32_t(u & 3) + (blk & 1u);      // chunk stored first
-                for (int a = 0; a < n_act; ++a) {
-                    const int s = a % C::NS, fs = a / C::NS, f = a % C::NF;
-                    if (!wait_all(stg_full(f), (a / C::NF) & 1)) break;
-                    if (fs >= 1 && !wait_all(kv_empty(s), (fs - 1) & 1)) break;
                     // the last two stages hold Q_c until the softmax warps copied it
-                    if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
-                    if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
-                    const uint8_t *stg = smem + C::OFF_STG + f * C::STG_BYTES;
-                    uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
-                    const int32_t *rc = rowc + act[a] * kBN;
-#pragma unroll
-                    for (int i0 = 0; i0 < IT; i0 += CB) {
-                        // every load of the batch before the first conversion
-                        uint2 v[CB][2], w[CB][2];
-                        uint32_t sb[CB];
-#pragma unroll
-                        for (int k = 0; k < CB; ++k) {
-                            const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
-                            if (i0 + k >= IT || r >= kBN) break;
-                            const int32_t row = rc[r];
-                            const int shift = row > 0 ? (row & 1) * 8 : 0;   // as copied (an invalid row came as row 0)
-                            const uint8_t *srow = stg + r * C::STG_ROW;
-                            const uint8_t *src = srow + shift + off;
-                            v[k][0] = *reinterpret_cast<const uint2 *>(src);
-                            v[k][1] = *reinterpret_cast<const uint2 *>(src + 8);
-                            if (rope) {
-                                w[k][0] = *reinterpret_cast<const uint2 *>(src + 16);
-                                w[k][1] = *reinterpret_cast<const uint2 *>(src + 24);
-                            }
-                            sb[k] = srow[C::STG_SCALE + shift + sc_idx];
-                        }
-#pragma unroll
-                        for (int k = 0; k < CB; ++k) {
-                            const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
-                            if (i0 + k >= IT || r >= kBN) break;
-                            uint4 o0, o1;   // dims 0-7 and 8-15 of the lane's 16
-                            if (rope) {
-                                o0 = make_uint4(v[k][0].x, v[k][0].y, v[k][1].x, v[k][1].y);
-                                o1 = make_uint4(w[k][0].x, w[k][0].y, w[k][1].x, w[k][1].y);
-                            } else {
-                                const uint32_t nan = e4m3x4_has_nan(v[k][0].x) | e4m3x4_has_nan(v[k][0].y) |
-                                                     e4m3x4_has_nan(v[k][1].x) | e4m3x4_has_nan(v[k][1].y);
-                                if (sb[k] <= 134u && !nan) {
-                                    const uint32_t s2 = ((sb[k] + 120u) << 7) * 0x00010001u;   // 2^(sb - 7), bf16 x2
-                                    e4m3x4_to_bf16x4(v[k][0].x, s2, o0.x, o0.y);
-                                    e4m3x4_to_bf16x4(v[k][0].y, s2, o0.z, o0.w);
-                                    e4m3x4_to_bf16x4(v[k][1].x, s2, o1.x, o1.y);
-                                    e4m3x4_to_bf16x4(v[k][1].y, s2, o1.z, o1.w);
-                                } else {   // NaN codes or a scale above 2^7: exact conversions
-                                    const float sc = e8m0_scale(sb[k]);
-                                    o0.x = e4m3x2_scaled_bf16x2(v[k][0].x & 0xffffu, sc);
-                                    o0.y = e4m3x2_scaled_bf16x2(v[k][0].x >> 16, sc);
-                                    o0.z = e4m3x2_scaled_bf16x2(v[k][0].y & 0xffffu, sc);
-                                    o0.w = e4m3x2_scaled_bf16x2(v[k][0].y >> 16, sc);
-                                    o1.x = e4m3x2_scaled_bf16x2(v[k][1].x & 0xffffu, sc);
-                                    o1.y = e4m3x2_scaled_bf16x2(v[k][1].x >> 16, sc);
-                                    o1.z = e4m3x2_scaled_bf16x2(v[k][1].y & 0xffffu, sc);
-                                    o1.w = e4m3x2_scaled_bf16x2(v[k][1].y >> 16, sc);
-                                }
-                            }
-                            uint8_t *line = stage + blk * (kBN * 128) + uint32_t(r) * 128u;
-                            const uint32_t c0 = c_first, c1 = c_first ^ 1u;   // chunk of dims 0-7 is 2(u&3)
-                            const uint4 first = (c0 & 1u) ? o1 : o0, second = (c0 & 1u) ? o0 : o1;
-                            *reinterpret_cast<uint4 *>(line + ((c0 ^ uint32_t(r & 7)) << 4)) = first;
-                            *reinterpret_cast<uint4 *>(line + ((c1 ^ uint32_t(r & 7)) << 4)) = second;
-                        }
+                    if (a == C::NS - 2 && !wait_all(q_free, 0)) {
+                        ok = false;
+                        break;
                     }
-                    ptx::fence_proxy_async_smem();   // generic-proxy stores -> MMA reads
-                    ptx::mbar_arrive(kv_full(s));
-                    __syncwarp();                    // every lane done with the staging rows ...
-                    if (lane == 0) ptx::mbar_arrive(stg_empty(f));   // ... before they are refilled
-                    if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
-                }
-            }
-            ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
-          } else {
-            // ------------------------------------------------------------ gather
-            // every gather warp copies its share of the rows of every tile; each
-            // lane's copies arrive on the stage's mbarrier when they land, so a
-            // warp runs ahead into every free stage (up to NS tiles in flight)
-            constexpr int CPR = DC / 8;     // 16-byte chunks per row slice
-            constexpr int RPI = 32 / CPR;   // rows per warp instruction
-            constexpr int STEP = RPI * kGatherWarps;
-            constexpr int ITERS = (kBN + STEP - 1) / STEP;
-            const int g = warp - kFirstGatherWarp;
-            const int sub = lane / CPR, ch = lane % CPR;
-            const uint32_t dst_col = uint32_t(ch >> 3) * (kBN * 128);
-            const char *kvb = reinterpret_cast<const char *>(p.kv) + (int64_t(crank) * DC + ch * 8) * 2;
-            bool ok = true;
-            int a = 0;
-            for (; a < n_act; ++a) {
-                const int s = a % C::NS, f = a / C::NS;
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
-                if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                // the last two stages hold Q_c until the softmax warps copied it
-                if (a == C::NS - 2 && !wait_all(q_free, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
-                const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
-                const int32_t *rc = rowc + act[a] * kBN;
-                    // unrolled by 2 only: the first tile runs this code cold (the
-                // instruction cache misses of a fully unrolled body cost more
-                // than the loop)
+                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
+                    const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
+                    const int32_t *rc = rowc + act[a] * kBN;
+                        // unrolled by 2 only: the first tile runs this code cold (the
+                    // instruction cache misses of a fully unrolled body cost more
+                    // than the loop)
 #pragma unroll 2
-                for (int i = 0; i < ITERS; ++i) {
-                    const int r = i * STEP + g * RPI + sub;   // warp g: row groups g, g + G, ...
-                    if (STEP * ITERS > kBN && r >= kBN) break;
-                    const int32_t row = rc[r];
-                    const char *src = kvb + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
-                    const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
-                    ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
+                    for (int i = 0; i < ITERS; ++i) {
+                        const int r = i * STEP + g * RPI + sub;   // warp g: row groups g, g + G, ...
+                        if (STEP * ITERS > kBN && r >= kBN) break;
+                        const int32_t row = rc[r];
+                        const char *src = kvb + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
+                        const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
+                        ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
+                    }
+                    ptx::cp_async_arrive_noinc(kv_full(s));
+                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
                 }
-                ptx::cp_async_arrive_noinc(kv_full(s));
-                if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
+                ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
+                (void)ok;
             }
-            ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
-            (void)ok;
-          }
         } else {
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
