@@ -256,12 +256,20 @@ int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D
     return sa_sparse_attn_launch_count(B, S, H, D, T, num_splits);
 }
 
-sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const float *attn_sink,
-                                          const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
-                                          int key_start_word, const int32_t *key_ends, float softmax_scale, void *o,
-                                          int64_t B, int64_t S_total, int64_t q0, int64_t S, int64_t H, int64_t D,
-                                          int64_t T, int num_splits, void *workspace, size_t workspace_bytes,
-                                          sa_stream_t stream) {
+namespace {
+
+sa_status mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B, int64_t q0,
+                      int64_t q_rows, int64_t max_key_len, int64_t K, const int32_t *key_starts,
+                      const int32_t *key_ends, uint32_t *mask, const int64_t mask_shape[3], sa_stream_t stream,
+                      bool dry_run);
+
+// The consumer over a window: every check of sa_masked_dense_attn_fwd_window,
+// then (unless dry_run) the launch.
+sa_status masked_window(const void *q, const void *kv, const float *attn_sink, const uint32_t *mask,
+                        int64_t mask_rows, int64_t mask_words, int key_start_word, const int32_t *key_ends,
+                        float softmax_scale, void *o, int64_t B, int64_t S_total, int64_t q0, int64_t S, int64_t H,
+                        int64_t D, int64_t T, int num_splits, void *workspace, size_t workspace_bytes,
+                        sa_stream_t stream, bool dry_run) {
     if (B < 0 || S < 0 || S_total < 0 || q0 < 0 || H < 0 || D < 0 || T < 0 || mask_rows < 0 || mask_words < 0)
         return SA_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
@@ -284,6 +292,7 @@ sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const f
     const size_t need = workspace_bytes_for(B, S, H, D, splits);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
+    if (dry_run) return SA_OK;
 
     sa::AttnArgs a{};
     a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = nullptr; a.topk_len = nullptr;
@@ -302,6 +311,18 @@ sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const f
     if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
+}
+
+}  // namespace
+
+sa_status sa_masked_dense_attn_fwd_window(const void *q, const void *kv, const float *attn_sink,
+                                          const uint32_t *mask, int64_t mask_rows, int64_t mask_words,
+                                          int key_start_word, const int32_t *key_ends, float softmax_scale, void *o,
+                                          int64_t B, int64_t S_total, int64_t q0, int64_t S, int64_t H, int64_t D,
+                                          int64_t T, int num_splits, void *workspace, size_t workspace_bytes,
+                                          sa_stream_t stream) {
+    return masked_window(q, kv, attn_sink, mask, mask_rows, mask_words, key_start_word, key_ends, softmax_scale, o, B,
+                         S_total, q0, S, H, D, T, num_splits, workspace, workspace_bytes, stream, false);
 }
 
 sa_status sa_masked_dense_attn_fwd(const void *q, const void *kv, const float *attn_sink,
@@ -347,17 +368,32 @@ sa_status sa_topk_masked_attn_fwd(const void *q, const void *kv, const float *at
     sa_topk_mask_shape(B, qc, max_key_len, key_starts != nullptr, shp);
     if (mask_buf == nullptr || mask_buf_bytes < size_t(shp[0] * shp[1] * shp[2] * 4)) return SA_ERR_WORKSPACE;
     const int key_start_word = key_starts != nullptr ? 1 : 0;
-    for (int64_t q0 = 0; q0 < max_q_len; q0 += qc) {
-        const int64_t rows = max_q_len - q0 < qc ? max_q_len - q0 : qc;
-        int64_t ws[3];
-        sa_topk_mask_shape(B, rows, max_key_len, key_starts != nullptr, ws);
-        sa_status st = sa_build_topk_mask_window(topk, topk_rows, cu_q_lens, B, q0, rows, max_key_len, K, key_starts,
-                                                 key_ends, mask_buf, ws, stream);
-        if (st != SA_OK) return st;
-        st = sa_masked_dense_attn_fwd_window(q, kv, attn_sink, mask_buf, ws[1], ws[2], key_start_word, key_ends,
-                                             softmax_scale, o, B, max_q_len, q0, rows, H, D, T, 0, workspace,
-                                             workspace_bytes, stream);
-        if (st != SA_OK) return st;
+    // every window is checked before the first launch (windows differ only
+    // in their row count: a full one and the last one)
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool dry = pass == 0;
+        for (int64_t q0 = 0; q0 < max_q_len; q0 += qc) {
+            const int64_t rows = max_q_len - q0 < qc ? max_q_len - q0 : qc;
+            if (dry && q0 > 0 && q0 + qc < max_q_len) continue;   // same shape as the first window
+            int64_t ws[3];
+            sa_topk_mask_shape(B, rows, max_key_len, key_starts != nullptr, ws);
+            auto build = [&] {
+                return mask_window(topk, topk_rows, cu_q_lens, B, q0, rows, max_key_len, K, key_starts, key_ends,
+                                   mask_buf, ws, stream, dry);
+            };
+            auto consume = [&] {
+                return masked_window(q, kv, attn_sink, mask_buf, ws[1], ws[2], key_start_word, key_ends,
+                                     softmax_scale, o, B, max_q_len, q0, rows, H, D, T, 0, workspace,
+                                     workspace_bytes, stream, dry);
+            };
+            // (the checks: the consumer's first, so that its argument errors
+            // are reported before the device is queried; the launches: build
+            // then consume)
+            sa_status st = dry ? consume() : build();
+            if (st != SA_OK) return st;
+            st = dry ? build() : consume();
+            if (st != SA_OK) return st;
+        }
     }
     return SA_OK;
 }
@@ -384,10 +420,13 @@ sa_status sa_topk_mask_shape(int64_t batch, int64_t max_query_len, int64_t max_k
     return SA_OK;
 }
 
-sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B,
-                                    int64_t q0, int64_t q_rows, int64_t max_key_len, int64_t K,
-                                    const int32_t *key_starts, const int32_t *key_ends, uint32_t *mask,
-                                    const int64_t mask_shape[3], sa_stream_t stream) {
+namespace {
+
+// Every check of sa_build_topk_mask_window, then (unless dry_run) the launch.
+sa_status mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B, int64_t q0,
+                      int64_t q_rows, int64_t max_key_len, int64_t K, const int32_t *key_starts,
+                      const int32_t *key_ends, uint32_t *mask, const int64_t mask_shape[3], sa_stream_t stream,
+                      bool dry_run) {
     if (mask_shape == nullptr || B < 0 || q0 < 0 || q_rows < 0 || max_key_len < 0 || K < 0 || topk_rows < 0)
         return SA_ERR_INVALID_ARG;
     if (max_key_len > INT32_MAX || q0 > INT32_MAX - q_rows) return SA_ERR_SHAPE;
@@ -408,6 +447,7 @@ sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, cons
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != SA_OK) return st;
+    if (dry_run) return SA_OK;
     sa::MaskArgs a{};
     a.topk = topk; a.topk_rows = topk_rows; a.cu_q_lens = cu_q_lens;
     a.B = B; a.max_q_len = q_rows; a.max_key_len = max_key_len; a.K = K;
@@ -417,6 +457,16 @@ sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, cons
     if (sa::launch_build_topk_mask(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
+}
+
+}  // namespace
+
+sa_status sa_build_topk_mask_window(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens, int64_t B,
+                                    int64_t q0, int64_t q_rows, int64_t max_key_len, int64_t K,
+                                    const int32_t *key_starts, const int32_t *key_ends, uint32_t *mask,
+                                    const int64_t mask_shape[3], sa_stream_t stream) {
+    return mask_window(topk, topk_rows, cu_q_lens, B, q0, q_rows, max_key_len, K, key_starts, key_ends, mask,
+                       mask_shape, stream, false);
 }
 
 sa_status sa_build_topk_mask(const int32_t *topk, int64_t topk_rows, const int32_t *cu_q_lens,

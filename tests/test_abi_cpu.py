@@ -199,3 +199,16 @@ def test_window_entries_validate_before_any_device_work():
     assert g(16, 4, 16, 2, -1, 16, 100, 8, None, None, 16, shape, None) == 1
     assert g(16, 4, 16, 2, 0, 16, 100, 8, None, None, 16, (2, 128, 8), None) == 2   # wrong shape
     assert g(16, 4, 16, 2, 0, 16, 100, 8, None, 6, 16, shape, None) == 3             # key_ends misaligned
+
+
+def test_windowed_call_checks_every_window_before_launching():
+    f = binding.sa_topk_masked_attn_fwd
+    base = dict(q=16, kv=16, attn_sink=16, topk=16, topk_rows=300, cu_q_lens=16, key_starts=None, key_ends=None,
+                softmax_scale=0.1, o=32, B=2, max_q_len=300, H=8, D=64, T=700, max_key_len=700, K=50, cap_bytes=30000,
+                mask_buf=256, mask_buf_bytes=1 << 20, workspace=None, workspace_bytes=0, stream=None)
+    assert f(**dict(base, T=0)) == 2                    # the consumer's shape error, nothing launched
+    assert f(**dict(base, D=96)) == 2
+    assert f(**dict(base, q=8)) == 3                    # q misaligned
+    assert f(**dict(base, cap_bytes=1000)) == 2         # no window fits the cap
+    assert f(**dict(base, mask_buf_bytes=100)) == 4     # mask buffer smaller than one window
+    assert f(**dict(base, B=0)) == 0
