@@ -502,7 +502,7 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": inp.name, "tokens_per_rank": tokens, "valid_slots": valid, "num_splits": ns,
                    "l2": "flushed between steps (256 MB write outside the timed events)",
-                   "inputs": "seeded N(0,1) bf16 q/kv, fp32 sink, ragged top-k indices (see DESIGN.md)"},
+                   "inputs": "seeded N(0,1) bf16 q/kv, fp32 sink, ragged top-k indices: window rows then random distinct compressed rows, -1 tails"},
         "tflops": tflops, "gathered_kv_gbs": achieved_gbs,
         "roofline": {"bound": bound, "achieved": achieved_gbs if bound == "hbm" else tflops,
                      "peak": hbm if bound == "hbm" else tf_burst, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
