@@ -269,3 +269,14 @@ def test_topk_length_of_the_valid_prefix_matches_minus_one_padding_exactly():
     a = run_gpu(inp)
     b = run_gpu_len(inp, lens)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("H,D,K,T,ns", [
+    (128, 512, 2049, 4000, 0),     # one slot more than a work unit holds: at least 2 splits
+    (128, 512, 5000, 8000, 1),     # an explicit single split is raised to the 3 the slots need
+    (64, 64, 8192, 9000, 0),       # 4 units' worth of slots, separate or in-cluster combine
+    (128, 256, 4100, 5000, 9),     # more splits than a cluster holds
+])
+def test_long_slot_lists_force_splits(H, D, K, T, ns):
+    inp = workloads.random_attn(1, 2, H, D, T, K, p_invalid=0.1, seed=K + ns)
+    assert_close(run_gpu(inp, num_splits=ns), run_oracle(inp), f"H={H} D={D} K={K} splits={ns}")
