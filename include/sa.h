@@ -1,7 +1,7 @@
 /*
  * sa.h -- C ABI of the GB300 (sm_103a) top-k sparse attention library.
  *
- * Two operations, both from the DeepSeek V4 sparse-attention path:
+ * Operations of the DeepSeek V4 sparse-attention path:
  *
  *  1. o = sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale)
  *     "DeepSeek V4 源码剖析, 第5章 sparse_attn 与 FlashMLA": §5.1 (argument
@@ -19,11 +19,20 @@
  *     prefill: `dense_mask_mod` reads bit kv&31 of word kv>>5, LSB first;
  *     `offset_dense_mask_mod` reads key_start from the last word of row 0).
  *
+ *  3. The mask's consumer -- attention over the keys a mask row admits
+ *     (the same PR 48770 page) -- and its chunked form: windows of query
+ *     rows under the 64 MiB global-mask cap of that page, each row built
+ *     only up to its live key end (vLLM PR 56628 page).
+ *
+ *  4. sparse_attn over an FP8 kv cache in the V4 row format (the same
+ *     chapter, §5.3 and §5.6).
+ *
  * Conventions for every entry point:
  *   - Tensors are dense, row-major (C order), in DEVICE memory of the current
  *     CUDA device unless stated otherwise.  The caller owns every buffer,
  *     workspace included; the library allocates no device memory and keeps no
- *     per-call state.
+ *     per-call state (the one exception, sa_sparse_attn_fwd_static_ws, uses
+ *     a workspace array compiled into the library).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  A call returns once its kernels are enqueued.
  *   - Arguments are validated on the host before anything is launched; on any
