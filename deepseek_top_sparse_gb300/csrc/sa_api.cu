@@ -38,7 +38,7 @@ sa_status current_device(DeviceInfo *out) {
     });
     if (!g_dev[dev].ok) return SA_ERR_CUDA;
     *out = g_dev[dev];
-    // The kernels are built for sm_103a only (tcgen05, TMA gather4).
+    // The kernels are built for sm_103a only (tcgen05, TMA).
     if (!(out->major == 10 && out->minor == 3)) return SA_ERR_UNSUPPORTED_DEVICE;
     return SA_OK;
 }
@@ -84,12 +84,24 @@ int plan_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t K, int num_s
     return clamp_splits(K, int(ns));
 }
 
+// Split workspace layout: fp32 partial rows [units, splits, rows, D], padded
+// to 256 bytes, then fp32 log-sum-exp [units, splits, rows].
+size_t partials_bytes(int64_t units, int64_t rows, int64_t D, int splits) {
+    const size_t o_bytes = size_t(units) * size_t(splits) * size_t(rows) * size_t(D) * sizeof(float);
+    return (o_bytes + 255) / 256 * 256;
+}
+
 size_t workspace_bytes_for(int64_t B, int64_t S, int64_t H, int64_t D, int splits) {
     if (splits <= 1) return 0;
-    const size_t tok = size_t(B) * size_t(S);
-    size_t o_bytes = tok * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
-    o_bytes = (o_bytes + 255) / 256 * 256;
-    return o_bytes + tok * size_t(splits) * size_t(H) * sizeof(float);
+    const int64_t units = B * S;
+    return partials_bytes(units, H, D, splits) + size_t(units) * size_t(splits) * size_t(H) * sizeof(float);
+}
+
+// Points the launch arguments at the two parts of a split workspace.
+void carve_workspace(sa::AttnArgs &a, void *workspace, int64_t units, int64_t rows, int64_t D, int splits) {
+    if (splits <= 1) return;
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + partials_bytes(units, rows, D, splits));
 }
 
 }  // namespace
@@ -166,12 +178,7 @@ sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const fl
     a.scale = softmax_scale; a.o = o;
     a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
     a.num_splits = splits;
-    if (splits > 1) {
-        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
-        o_bytes = (o_bytes + 255) / 256 * 256;
-        a.ws_o = static_cast<float *>(workspace);
-        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
-    }
+    carve_workspace(a, workspace, B * S, H, D, splits);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the main kernel, then (for splits too many for one cluster) the combine
     if (sa::launch_sparse_attn(a, dev.sms, s) != cudaSuccess) return SA_ERR_CUDA;
@@ -218,12 +225,7 @@ sa_status sa_sparse_attn_fwd_fp8(const void *q, const uint8_t *kv_fp8, const flo
     a.scale = softmax_scale; a.o = o;
     a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
     a.num_splits = splits;
-    if (splits > 1) {
-        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
-        o_bytes = (o_bytes + 255) / 256 * 256;
-        a.ws_o = static_cast<float *>(workspace);
-        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
-    }
+    carve_workspace(a, workspace, B * S, H, D, splits);
     if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
@@ -302,12 +304,7 @@ sa_status masked_window(const void *q, const void *kv, const float *attn_sink, c
     a.num_splits = splits;
     a.mask = mask; a.mask_rows = mask_rows; a.mask_words = mask_words; a.key_start_word = key_start_word;
     a.key_ends = key_ends;
-    if (splits > 1) {
-        size_t o_bytes = size_t(B) * size_t(S) * size_t(splits) * size_t(H) * size_t(D) * sizeof(float);
-        o_bytes = (o_bytes + 255) / 256 * 256;
-        a.ws_o = static_cast<float *>(workspace);
-        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
-    }
+    carve_workspace(a, workspace, B * S, H, D, splits);
     if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return SA_OK;
