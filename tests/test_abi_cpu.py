@@ -212,3 +212,14 @@ def test_windowed_call_checks_every_window_before_launching():
     assert f(**dict(base, cap_bytes=1000)) == 2         # no window fits the cap
     assert f(**dict(base, mask_buf_bytes=100)) == 4     # mask buffer smaller than one window
     assert f(**dict(base, B=0)) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    # no fallback: with the CUDA library absent the binding raises instead of
+    # computing anything some other way
+    from deepseek_top_sparse_gb300 import build as sa_build
+
+    monkeypatch.setattr(sa_build, "LIB", str(tmp_path / "libsa.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.load(build_if_missing=False)
