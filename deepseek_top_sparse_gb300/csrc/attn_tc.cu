@@ -1403,8 +1403,8 @@ constexpr int kMaxDev = 64;
 
 constexpr int kMaxFusedCluster = 8;   // portable cluster size
 
-// The driver's tensor-map encoder, looked up once through the runtime (no
-// link against the driver library).
+// The CUDA driver API's tensor-map encoder, looked up once through the
+// runtime (no link against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
