@@ -39,6 +39,12 @@
  *   R14 live mask words [0, ceil(max_key_len/32)) are cleared then OR-ed;
  *   R15 padding words and rows q >= q_len are never written;
  *   R16 the reserved word of row 0 holds the raw bits of key_starts[b].
+ *   R19 a per-token topk_length keeps only the slots j < clamp(len, 0, K).
+ *   R21 the mask consumer admits key t iff bit t (+ key_start) of the row is
+ *       set, within the row's 32 * W positions.
+ *   R22 FP8 row byte order: 448 E4M3 codes, 64 bf16 RoPE dims, 8 E8M0 scales.
+ *   R24 a mask window holds query rows q0.. of each request; a live key end
+ *       bounds both the words written and the keys the consumer admits.
  *
  * Inputs are bf16 bit patterns (uint16) as stored on the device; each value
  * is widened exactly to double before any arithmetic.

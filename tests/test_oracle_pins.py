@@ -525,3 +525,19 @@ def test_masked_dense_live_end_drops_the_keys_past_it():
     idx[0][idx[0] >= 41] = -1
     want = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, idx, inp.softmax_scale)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_masked_dense_key_offset_and_live_end_together():
+    # kv[b] is the chunk of mask positions start .. start + T - 1; the live end
+    # is in mask positions, so a chunk key t counts iff t + start < end
+    inp = workloads.random_attn(1, 3, 2, 8, 60, 15, p_invalid=0.0, seed=65)
+    start, end = 11, 40
+    topk = inp.topk_idxs.reshape(3, -1).numpy()
+    m = oracle.build_topk_mask(topk, np.array([0, 3], np.int32), 1, 3, 60)
+    chunk = inp.kv[:, start:].contiguous()
+    got = oracle.masked_dense_attn(inp.q, chunk, inp.attn_sink, m, inp.softmax_scale, key_offset=[start],
+                                   key_ends=[end])
+    keep = (inp.topk_idxs >= start) & (inp.topk_idxs < end)
+    shifted = torch.where(keep, inp.topk_idxs - start, torch.full_like(inp.topk_idxs, -1))
+    want = oracle.sparse_attn(inp.q, chunk, inp.attn_sink, shifted, inp.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
