@@ -101,8 +101,8 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def _np(x, dtype):
-    if isinstance(x, np.ndarray):
-        return np.ascontiguousarray(x, dtype=dtype)
+    if not hasattr(x, "detach"):          # numpy arrays, lists, tuples
+        return np.ascontiguousarray(np.asarray(x), dtype=dtype)
     return np.ascontiguousarray(x.detach().cpu().numpy(), dtype=dtype)
 
 
