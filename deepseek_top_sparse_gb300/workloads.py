@@ -96,6 +96,66 @@ def random_attn(B, S, H, D, T, K, *, p_invalid=0.1, seed=0, distinct=True, scale
                       name=f"random B={B} S={S} H={H} D={D} T={T} K={K}")
 
 
+def wide_range_attn(pattern: str, B=2, S=2, H=128, D=512, T=2048, K=1152, *, p_invalid=0.05,
+                    seed=0) -> AttnInputs:
+    """Inputs whose partial logits span a wide range (stress cases for any
+    lossy step between the two head-dim halves of a row).  Every token takes
+    one or two "special" rows in each block of 32 slots, ordinary rows in the
+    other slots; the picks of a token are distinct.
+
+    pattern "dominant": q drawn x30; the special rows (the first T/8 of kv)
+      are drawn x8, every other row x0.01, so one or two keys of each block
+      carry huge positive or negative logits next to near-zero ones.
+    pattern "outlier": every head's q is u + N(0, 0.25) for one shared
+      direction u ~ N(0,1)^D; the special rows (the first T/16) are -c.u with
+      c uniform in [100, 300] (huge negative logits, weight ~0), the others
+      N(0,1): the keys that carry the weight sit next to an outlier.
+    pattern "cancel": q as for "outlier"; the special rows are
+      c.[u_0, -u_1] + N(0,1), u_0 / u_1 the two halves of u: the partial
+      logit over each half of the head dim is huge and the two nearly cancel,
+      so the sum is ordinary and those keys carry weight.
+    """
+    g = _gen(seed)
+    n_special = T // 8 if pattern == "dominant" else T // 16
+    if pattern == "dominant":
+        q = (torch.randn((B, S, H, D), generator=g) * 30).to(torch.bfloat16)
+        base = torch.randn((B, T, D), generator=g)
+        mult = torch.full((T, 1), 0.01)
+        mult[:n_special] = 8.0
+        kv = (base * mult).to(torch.bfloat16)
+    elif pattern in ("outlier", "cancel"):
+        u = torch.randn((D,), generator=g)
+        q = (u + 0.5 * torch.randn((B, S, H, D), generator=g)).to(torch.bfloat16)
+        kv32 = torch.randn((B, T, D), generator=g)
+        c = 100 + 200 * torch.rand((B, n_special, 1), generator=g)
+        if pattern == "outlier":
+            kv32[:, :n_special] = -c * u
+        else:
+            signed = torch.cat([u[: D // 2], -u[D // 2:]])
+            kv32[:, :n_special] = c * signed + kv32[:, :n_special]
+        kv = kv32.to(torch.bfloat16)
+    else:
+        raise ValueError(pattern)
+    sink = torch.randn((H,), generator=g, dtype=torch.float32)
+    idx = torch.empty((B, S, K), dtype=torch.int32)
+    j = torch.arange(K)
+    special = j % 32 == 3
+    if pattern == "dominant":
+        special |= j % 32 == 20
+    n_sp = int(special.sum())
+    assert n_sp <= n_special and K - n_sp <= T - n_special, "not enough distinct rows"
+    for b in range(B):
+        for s in range(S):
+            row = torch.empty((K,), dtype=torch.int32)
+            row[special] = _distinct(n_special, n_sp, g)
+            row[~special] = n_special + _distinct(T - n_special, K - n_sp, g)
+            idx[b, s] = row
+    if p_invalid > 0:
+        idx[torch.rand((B, S, K), generator=g) < p_invalid] = -1
+    return AttnInputs(q, kv, sink, idx, D ** -0.5,
+                      name=f"wide-range ({pattern}) B={B} S={S} H={H} D={D} T={T} K={K}")
+
+
 FP8_ROW_BYTES = 584      # one row of the FP8 kv cache: 448 codes + 64 bf16 + 8 scale bytes
 
 
