@@ -13,30 +13,38 @@
 // gathered kv row and of o.  Tiles of 64 slots whose slots are all invalid
 // are skipped, so the cost follows the live slots.  Per CTA:
 //
-//   warps 5.. (gather)  one warp per shared-memory stage; each warp copies the
-//                       DC-column slice of its tile's 64 indexed kv rows with
-//                       16-byte cp.async (one 512-byte row slice per warp
-//                       instruction, invalid slots zero-filled), writing the
-//                       128B-swizzled K-major layout the MMAs read;
-//   warp 4 (MMA)        S = Q_c K_c^T with Q_c resident in TMEM (A operand
-//                       from tensor memory), two S buffers in TMEM; O_c += P V_c
-//                       with P and V_c (= the same stage, read MN-major) in
-//                       shared memory, O_c resident in TMEM for the whole unit.
-//                       Issue is event driven: S of a tile may run up to two
-//                       tiles ahead of the P.V that trails it;
-//   warps 0..3          one thread per head row (= TMEM lane): the partial
-//                       logits of tile a+1 go to the partner CTA (distributed
-//                       shared memory) before tile a is finished, so the swap
-//                       overlaps the softmax; both CTAs add S_0 + S_1 (fp32
-//                       addition commutes: identical logits on both), mask
-//                       invalid slots, run the online softmax in base 2 with a
-//                       lazily rescaled running max and store P (bf16).
+//   warps 9..15 (gather) copy the DC-column slice of each tile's 64 indexed
+//                        kv rows with 16-byte cp.async (invalid slots
+//                        zero-filled) into the 128B-swizzled K-major stage the
+//                        MMAs read;
+//   warp 8 (MMA)         S = Q_c K_c^T with Q_c resident in TMEM, into one of
+//                        two S buffers; O_c += P V_c with P (bf16) in the same
+//                        TMEM buffer its S came from and V_c the same stage
+//                        read MN-major; O_c resident in TMEM for the unit;
+//   warps 0..7 (softmax) warp w reads the 16 TMEM lanes [16*(w/4), +16) of
+//                        lane quarter w%4 (16x256b: a thread holds two head
+//                        rows x 16 of the tile's 64 columns, four threads per
+//                        row pair, so row maxima are quad shuffles).
+//
+// With two CTAs a head row's logit is the sum of two partial dot products,
+// one per CTA.  Rows are owned by one CTA each: CTA c owns lanes
+// [16c, 16c+16) of every quarter.  The "sender" warps of a CTA (the lanes it
+// does not own) copy their fp32 partial logits to the owner, exactly; the
+// "owner" warps add the partner's partials to their own, run the online
+// softmax, write P for their rows into their own TMEM and send it (bf16,
+// with each row's rescale factor) to the partner, whose sender warps store
+// it into the partner's TMEM and apply the factor to the partner's half of
+// O.  So each CTA runs the softmax of half the rows, and every logit is the
+// plain fp32 sum of the two MMA partials.
 //
 // TMEM columns (D = 512, DC = 256): O_c [0,256) fp32, S [256,384) two 64-col
-// buffers, Q_c [384,512) bf16 pairs.  Every buffer hand-off is an mbarrier
-// phase that is never more than one phase away from its waiter, and every
-// wait is bounded by the global timer: a wait that runs out records an error
-// code and the kernel drains and returns instead of hanging.
+// buffers (P of a tile overwrites the first 32 columns of its own S buffer),
+// Q_c [384,512) bf16 pairs.  Every buffer hand-off is an mbarrier phase that
+// is never more than one phase away from its waiter; every mbarrier wait is
+// bounded by clock64 and gives up early once any wait of any kernel has
+// recorded an error, so a failing launch drains in about one wait bound.
+// The cluster barriers of the prologue and teardown are hardware barriers
+// that every CTA of the cluster reaches on every path.
 #include <cuda_bf16.h>
 
 #include <cudaTypedefs.h>
@@ -50,37 +58,6 @@ namespace sa {
 
 static __device__ int g_device_error = 0;
 
-// Timeline hooks for performance work: with SA_TRACE defined, CTA 0 records
-// clock64() at fixed points of each role into g_sa_trace[role][tile][event];
-// otherwise they compile to nothing.
-#ifdef SA_TRACE
-__device__ long long g_sa_trace[4][64][16];
-// per CTA: globaltimer (ns) at start, prologue end, epilogue start, end;
-// combine kernel: earliest start and latest end
-__device__ unsigned long long g_sa_cta[4096][4];
-__device__ unsigned long long g_sa_comb[2];
-__device__ __forceinline__ unsigned long long sa_gtime() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-#define SA_CTA_POINT(ev)                                                     \
-    do {                                                                     \
-        if (threadIdx.x == 0 && blockIdx.x < 4096) g_sa_cta[blockIdx.x][ev] = sa_gtime(); \
-    } while (0)
-#define SA_TRACE_POINT(role, tile, ev)                                                              \
-    do {                                                                                            \
-        if (blockIdx.x == 0 && (tile) >= 0 && (tile) < 64) g_sa_trace[role][tile][ev] = clock64(); \
-    } while (0)
-#else
-#define SA_TRACE_POINT(role, tile, ev) \
-    do {                               \
-    } while (0)
-#define SA_CTA_POINT(ev) \
-    do {                 \
-    } while (0)
-#endif
-
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -88,11 +65,12 @@ constexpr int kBN = 64;                 // kv rows per tile (MMA N of S, K of P.
 constexpr int kM = 128;                 // head rows per MMA (TMEM lanes)
 constexpr int kMaxUnitSlots = 2048;     // slots per work unit (host enforces)
 constexpr int kMaxUnitTiles = kMaxUnitSlots / kBN;
-// Bound on any single wait, in SM clock cycles (~2 s at 2 GHz): far beyond
-// any legitimate wait.  clock64 is read only after 1024 unsuccessful polls.
-constexpr long long kWaitCycles = 4000000000ll;
+// Bound on any single wait, in SM clock cycles (~0.1 s at 2 GHz): far beyond
+// any legitimate wait.  clock64 and the device error word are read only after
+// 1024 unsuccessful polls.
+constexpr long long kWaitCycles = 200000000ll;
 constexpr float kRescaleThreshold = 8.f;     // log2 units: P <= 256 before normalising
-constexpr int kSoftmaxWarps = 8;              // two per TMEM lane quarter, 32 columns each
+constexpr int kSoftmaxWarps = 8;              // two per TMEM lane quarter, 16 lanes each
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps;
 constexpr int kFirstGatherWarp = kMmaWarp + 1;
@@ -101,8 +79,7 @@ constexpr int kFirstGatherWarp = kMmaWarp + 1;
 constexpr int kGatherWarps = 7;               // all fill every tile, rows interleaved
 // 16 warps = 4 warpgroups launched at 128 registers a thread; after the
 // prologue the two softmax warpgroups grow to 160 and the MMA + gather
-// warpgroups shrink to 96: 256 * 160 + 256 * 96 = 512 * 128 (the smallest
-// split with no spills on either side).
+// warpgroups shrink to 96: 256 * 160 + 256 * 96 = 512 * 128.
 constexpr int kLaunchRegs = 128;
 constexpr int kSoftmaxRegs = 160;
 constexpr int kOtherRegs = 96;
@@ -137,26 +114,32 @@ struct Cfg {
     static_assert(THREADS == 512, "four warpgroups");
     static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
                   "register split equals the launch allocation");
-    // partner's partial logits of one tile as block floating point: 16-bit
-    // codes [8 chunks][128 rows][16 B] then one fp32 step per (row, half)
-    static constexpr int XQ_BYTES = kM * kBN * 2;         // 16 KB
-    static constexpr int X_BYTES = XQ_BYTES + 2 * kM * 4; // + 1 KB of steps
-    static_assert(X_BYTES % 1024 == 0, "receive buffers keep 1 KB alignment");
+    // Partner messages (CL == 2), one buffer per (S buffer b, lane quarter q):
+    //   X: the partner's fp32 partial logits of this CTA's 16 rows of the
+    //      quarter, [8 chunks][32 lanes][16 B] (chunk k = the four values of
+    //      16x256b repetition k);
+    //   PM: the partner's P of its 16 rows, [4 chunks][32 lanes][16 B] (the
+    //      16 words of a 16x128b.x8 store), then one fp32 rescale factor per
+    //      row (16 x 4 B).
+    static constexpr int XQ = 8 * 32 * 16;
+    static constexpr int PM_P = 4 * 32 * 16;
+    static constexpr int PMQ = PM_P + 16 * 4;
     static constexpr int OFF_KV = 0;
     static constexpr int OFF_STG = OFF_KV + NS * STAGE_BYTES;
     static constexpr int OFF_X = OFF_STG + NF * STG_BYTES;
-    static_assert(OFF_X % 1024 == 0, "receive buffers keep 1 KB alignment");
-    static constexpr int OFF_IDX = OFF_X + (CL == 2 ? 2 * X_BYTES : 0);
+    static constexpr int OFF_PM = OFF_X + (CL == 2 ? 2 * 4 * XQ : 0);
+    static constexpr int OFF_IDX = OFF_PM + (CL == 2 ? 2 * 4 * PMQ : 0);
     static constexpr int OFF_VALID = OFF_IDX + kMaxUnitSlots * 4;
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
-    static constexpr int OFF_RED = OFF_LIST + kMaxUnitTiles * 4 + 16;   // float [3][2][128]
-    static constexpr int OFF_LSE = OFF_RED + 3 * 2 * kM * 4;             // float [8 splits][128]
-    static constexpr int OFF_SINK = OFF_LSE + 8 * kM * 4;                // float [128]
+    static constexpr int OFF_STAT = OFF_LIST + kMaxUnitTiles * 4 + 16;  // float2 [128]: (m, l) per row
+    static constexpr int OFF_LSE = OFF_STAT + kM * 8;                   // float [8 splits][128]
+    static constexpr int OFF_SINK = OFF_LSE + 8 * kM * 4;               // float [128]
     static constexpr int OFF_BAR = OFF_SINK + kM * 4;
-    // kv_full[NS] kv_empty[NS] s_full s_empty p_full[2] p_empty[2]
-    // x_full[2] x_empty[2] o_done q_ready mma_done red_bar l_bar (spare) q_smem q_free
-    // FP8: + stg_full[NF] stg_empty[NF]
-    static constexpr int NUM_BARS = 2 * NS + 18 + 2 * NF;
+    // kv_full[NS] kv_empty[NS] s_full[2] p_full[2] o_done q_ready mma_done
+    // stat_bar q_smem q_free (2 spare) x_full[8] x_empty[8] pm_full[8]
+    // pm_empty[8] ([buffer][quarter]); FP8: + stg_full[NF] stg_empty[NF]
+    static constexpr int BAR_X = 2 * NS + 12;
+    static constexpr int NUM_BARS = BAR_X + 32 + 2 * NF;
     // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
     // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
     static constexpr int OFF_QS = OFF_KV + (NS - 2) * STAGE_BYTES;
@@ -164,19 +147,19 @@ struct Cfg {
     static_assert(Q_BYTES == 2 * STAGE_BYTES, "Q_c fills two kv stages");
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_TSLOT + 16 + 1024;    // + slack to align the base to 1 KB
-    // TMEM columns: O_c fp32, S fp32 (one tile), P bf16 pairs (two tiles), Q_c bf16 pairs
+    // TMEM columns: O_c fp32, two S buffers of one tile (fp32; P of the tile
+    // as bf16 pairs over its first half), Q_c bf16 pairs
     static constexpr int O_COL = 0;
     static constexpr int S_COL = DC;
-    static constexpr int P_COL = DC + kBN;
     static constexpr int Q_COL = DC + 2 * kBN;
     static constexpr int TMEM_USED = Q_COL + DC / 2;
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // output staging (epilogue): kM rows of up to DC fp32, padded by 16 bytes,
-    // over the kv ring, receive buffers and index lists (all dead by then)
+    // over the kv ring, partner buffers and index lists (all dead by then)
     static constexpr int STAGE_ROW = DC * 4 + 16;
-    static_assert(kM * STAGE_ROW <= OFF_RED - OFF_KV, "output staging fits below the reduction scratch");
+    static_assert(kM * STAGE_ROW <= OFF_STAT - OFF_KV, "output staging stays below the row statistics");
 };
 
 struct TcParams {
@@ -209,6 +192,10 @@ struct TcParams {
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
+// Bounded mbarrier wait.  Gives up (and returns false) when the wait has run
+// past max_cycles, recording kErrWaitTimeout, or as soon as some wait has
+// already recorded an error: once one wait has failed, every later wait of
+// every CTA returns within about 1024 polls, so a failing launch drains fast.
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long max_cycles = kWaitCycles) {
     auto poll = [&] { return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity); };
@@ -216,9 +203,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long lon
     const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (poll()) return true;
-        if ((n & 1023u) == 0 && clock64() - t0 > max_cycles) {
-            record_error(kErrWaitTimeout);
-            return false;
+        if ((n & 1023u) == 0) {
+            if (*reinterpret_cast<volatile int *>(&g_device_error) != 0) return false;
+            if (clock64() - t0 > max_cycles) {
+                record_error(kErrWaitTimeout);
+                return false;
+            }
         }
     }
 }
@@ -227,28 +217,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long lon
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, wait_bar<kCluster>(bar, parity));
-}
-
-// Block floating point for the partner exchange: 32 partial logits become
-// 16-bit codes sharing one power-of-two step 2^(e-14), where max|x| < 2^e,
-// so |x| / step < 2^14 and the absolute error is at most half a step
-// (<= max|x| * 2^-15).  Encoding adds kBfpMagic = 1.5*2^23 + 2^15 to x/step:
-// the float's low 16 bits are then (round(x/step) + 2^15), with no integer
-// conversion.  Decoding ORs a code into 2^23 and removes 2^23 + 2^15.  A
-// non-finite block gets a NaN step, so NaN still propagates.
-constexpr float kBfpMagic = 12615680.0f;      // 1.5 * 2^23 + 2^15
-constexpr float kBfpDecodeBias = 8421376.0f;  // 2^23 + 2^15
-
-struct BfpStep {
-    float step, inv;
-};
-
-__device__ __forceinline__ BfpStep bfp_step(float amax) {
-    const uint32_t bexp = (__float_as_uint(amax) >> 23) & 0xFFu;   // biased exponent of max|x|
-    if (bexp == 0xFFu || amax != amax) return {__uint_as_float(0x7FC00000u), 0.f};  // inf / NaN
-    if (bexp < 20u) return {__uint_as_float(6u << 23), __uint_as_float(248u << 23)};  // ~0: 2^-121
-    // max|x| < 2^(bexp-126); step = 2^(bexp-126-14): biased exponent bexp-13
-    return {__uint_as_float((bexp - 13u) << 23), __uint_as_float((267u - bexp) << 23)};
 }
 
 constexpr int ptx_log2(int x) { return x <= 1 ? 0 : 1 + ptx_log2(x >> 1); }
@@ -354,7 +322,6 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
             if (rt + u * RP < cr1) pre[u] = __ldcg(src + u * pass_f4);
     }
     const float sink_r = tid < nrows ? reinterpret_cast<const float *>(smem + C::OFF_SINK)[cr0 + tid] : 0.f;
-    if (tid == 0) SA_TRACE_POINT(1, 60, 0);
     // (pre holds passes 0..kB-1 of the first other split)
     if (tid < nrows) {
         const int r = cr0 + tid;
@@ -378,7 +345,6 @@ __device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, i
             tab[i * kM + r] = (zero || li == -INFINITY) ? 0.f * fn : exp2f(li - M) * fn;
         }
     }
-    if (tid == 0) SA_TRACE_POINT(1, 60, 1);
     __syncthreads();
     const uint8_t *own = smem + C::OFF_KV + rt * C::STAGE_ROW + c * 16;
     float4 acc[kB];
@@ -503,31 +469,29 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     int32_t *rowc = reinterpret_cast<int32_t *>(smem + C::OFF_IDX);
     uint64_t *vmask = reinterpret_cast<uint64_t *>(smem + C::OFF_VALID);
     int32_t *act = reinterpret_cast<int32_t *>(smem + C::OFF_LIST);  // act[0..n) tiles, act[kMaxUnitTiles] = n
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);      // [3][2][128]
+    float2 *stat = reinterpret_cast<float2 *>(smem + C::OFF_STAT);  // (m, l) per head row, after the tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
     auto kv_full = [&](int s) { return bar(s); };
     auto kv_empty = [&](int s) { return bar(C::NS + s); };
-    const uint32_t s_full = bar(2 * C::NS);
-    const uint32_t s_empty = bar(2 * C::NS + 1);
-    auto p_full = [&](int i) { return bar(2 * C::NS + 2 + i); };
-    auto p_empty = [&](int i) { return bar(2 * C::NS + 4 + i); };
-    auto x_full = [&](int i) { return bar(2 * C::NS + 6 + i); };
-    auto x_empty = [&](int i) { return bar(2 * C::NS + 8 + i); };
-    const uint32_t o_done = bar(2 * C::NS + 10);
-    const uint32_t q_ready = bar(2 * C::NS + 11);
-    const uint32_t mma_done = bar(2 * C::NS + 12);
-    const uint32_t red_bar = bar(2 * C::NS + 13);
-    const uint32_t l_bar = bar(2 * C::NS + 14);
-    const uint32_t q_smem = bar(2 * C::NS + 16);   // Q_c landed in shared memory
-    const uint32_t q_free = bar(2 * C::NS + 17);   // Q_c copied to TMEM: its stages are free
-    auto stg_full = [&](int f) { return bar(2 * C::NS + 18 + f); };           // FP8: staging f landed
-    auto stg_empty = [&](int f) { return bar(2 * C::NS + 18 + C::NF + f); };  // FP8: staging f widened
+    auto s_full = [&](int i) { return bar(2 * C::NS + i); };        // S buffer i written by QK^T
+    auto p_full = [&](int i) { return bar(2 * C::NS + 2 + i); };    // P of buffer i stored, O rows rescaled
+    const uint32_t o_done = bar(2 * C::NS + 4);    // a P.V completed
+    const uint32_t q_ready = bar(2 * C::NS + 5);   // Q_c in TMEM
+    const uint32_t mma_done = bar(2 * C::NS + 6);  // every MMA of the unit completed
+    const uint32_t stat_bar = bar(2 * C::NS + 7);  // row statistics of every row in place
+    const uint32_t q_smem = bar(2 * C::NS + 8);    // Q_c landed in shared memory
+    const uint32_t q_free = bar(2 * C::NS + 9);    // Q_c copied to TMEM: its stages are free
+    // partner messages, per (S buffer b, lane quarter q)
+    auto x_full = [&](int b2, int q) { return bar(C::BAR_X + b2 * 4 + q); };        // partner's partials landed
+    auto x_empty = [&](int b2, int q) { return bar(C::BAR_X + 8 + b2 * 4 + q); };   // partner read our partials
+    auto pm_full = [&](int b2, int q) { return bar(C::BAR_X + 16 + b2 * 4 + q); };  // partner's P rows landed
+    auto pm_empty = [&](int b2, int q) { return bar(C::BAR_X + 24 + b2 * 4 + q); }; // partner read our P rows
+    auto stg_full = [&](int f) { return bar(C::BAR_X + 32 + f); };            // FP8: staging f landed
+    auto stg_empty = [&](int f) { return bar(C::BAR_X + 32 + C::NF + f); };   // FP8: staging f widened
 
     // ---------------------------------------------------------------- prologue
-    if (tid == 0) SA_TRACE_POINT(3, 0, 0);
-    SA_CTA_POINT(0);
     // The index list heads the longest dependency chain (index -> kv row ->
     // QK^T), so its loads go out first; every load of a thread is issued
     // before the first is used.
@@ -574,19 +538,21 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             ptx::mbar_init(kv_full(s), kFp8 ? 32 * kF8WidenWarps : 32 * kGatherWarps);
             ptx::mbar_init(kv_empty(s), 1);
         }
-        ptx::mbar_init(s_full, 1);
-        ptx::mbar_init(s_empty, kSoftmaxThreads);
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(p_full(i), kSoftmaxThreads);
-            ptx::mbar_init(p_empty(i), 1);
-            ptx::mbar_init(x_full(i), 1);   // + X_BYTES of st.async complete_tx per phase
-            ptx::mbar_init(x_empty(i), 1);  // one credit per phase from the partner
+            ptx::mbar_init(s_full(i), 1);
+            ptx::mbar_init(p_full(i), kSoftmaxWarps);   // one elected lane per softmax warp
+            for (int q = 0; q < 4; ++q) {
+                ptx::mbar_init(x_full(i, q), 1);    // the owner's expect_tx + XQ bytes from the partner
+                ptx::mbar_init(x_empty(i, q), 1);   // one credit from the partner's owner warp
+                ptx::mbar_init(pm_full(i, q), 1);   // the sender's expect_tx + PMQ bytes from the partner
+                ptx::mbar_init(pm_empty(i, q), 1);  // one credit from the partner's sender warp
+            }
         }
         ptx::mbar_init(o_done, 1);
         ptx::mbar_init(q_ready, kSoftmaxThreads);
         ptx::mbar_init(mma_done, 1);
-        ptx::mbar_init(red_bar, kSoftmaxThreads);
-        ptx::mbar_init(l_bar, kSoftmaxThreads);
+        // owner warps (8, or 4 plus one expect_tx for the partner's 512 bytes)
+        ptx::mbar_init(stat_bar, CL == 2 ? 5 : kSoftmaxWarps);
         ptx::mbar_init(q_smem, 1);
         ptx::mbar_init(q_free, kSoftmaxThreads);
         for (int f = 0; f < C::NF; ++f) {
@@ -600,7 +566,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         for (int c = 0; c < DC / 64; ++c)
             ptx::tma_load_2d(ptx::smem_u32(smem + C::OFF_QS + c * (kM * 128)), &qmap, int32_t(crank) * DC + c * 64,
                              int32_t(iotok * p.H), q_smem);
-        SA_TRACE_POINT(3, 0, 10);
     }
     // slot indices -> kv row numbers (-1 = invalid) and a 64-bit validity
     // mask per tile, 32 slots per warp step
@@ -621,7 +586,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // leading slots (a stream compaction over the 32-key chunks); only the
         // last tile can be partial
         static_assert(kSteps * kWarpsAll == kMaxUnitSlots / 32 && kMaxUnitSlots / 32 == 64, "one count per lane pair");
-        int *cnt = reinterpret_cast<int *>(red);   // [64] admitted keys per chunk (scratch until the softmax)
+        int *cnt = reinterpret_cast<int *>(stat);  // [64] admitted keys per chunk (scratch until the softmax)
         uint32_t mb[kSteps];
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
@@ -647,9 +612,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         }
     }
     if (tid < kM) sink_tab[tid] = sink_t;
-    if (tid == 0) SA_TRACE_POINT(3, 0, 11);
     __syncthreads();
-    if (tid == 0) SA_TRACE_POINT(3, 0, 12);
     if (warp == 0) {
         // list of tiles with a valid slot, in order (ntiles <= 32: one warp)
         static_assert(kMaxUnitTiles <= 32, "one lane per tile");
@@ -657,7 +620,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         const uint32_t bal = __ballot_sync(0xffffffffu, live);
         if (live) act[__popc(bal & ((1u << lane) - 1u))] = lane;
         if (lane == 0) act[kMaxUnitTiles] = __popc(bal);
-        if (lane == 0) SA_TRACE_POINT(3, 0, 13);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -668,11 +630,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     const bool clustered = CL == 2 || p.fused;
     if (clustered) ptx::cluster_arrive_relaxed();
     ptx::tc_fence_after();
-    if (tid == 0) SA_TRACE_POINT(3, 0, 14);
     const uint32_t tbase = *tslot;
     const int n_act = act[kMaxUnitTiles];
-    if (tid == 0) SA_TRACE_POINT(3, 0, 1);
-    SA_CTA_POINT(1);
     if (warp >= kSoftmaxWarps) {
         // MMA and gather warpgroups: a small register budget
         ptx::setmaxnreg_dec<kOtherRegs>();
@@ -713,7 +672,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                             ok = false;
                             break;
                         }
-                        if (cw == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
                         const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
                         const int32_t *rc = rowc + act[a] * kBN;
                         for (int j = cw; j < n_instr; j += kF8CopyWarps) {
@@ -763,7 +721,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         if (fs >= 1 && !wait_all(kv_empty(s), (fs - 1) & 1)) break;
                         // the last two stages hold Q_c until the softmax warps copied it
                         if (a == C::NS - 2 && !wait_all(q_free, 0)) break;
-                        if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
                         const uint8_t *stg = smem + C::OFF_STG + f * C::STG_BYTES;
                         uint8_t *stage = smem + C::OFF_KV + s * C::STAGE_BYTES;
                         const int32_t *rc = rowc + act[a] * kBN;
@@ -830,7 +787,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         ptx::mbar_arrive(kv_full(s));
                         __syncwarp();                    // every lane done with the staging rows ...
                         if (lane == 0) ptx::mbar_arrive(stg_empty(f));   // ... before they are refilled
-                        if (ww == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
                     }
                 }
                 ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
@@ -851,7 +807,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 int a = 0;
                 for (; a < n_act; ++a) {
                     const int s = a % C::NS, f = a / C::NS;
-                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 0);
                     if (f >= 1 && !wait_all(kv_empty(s), (f - 1) & 1)) {
                         ok = false;
                         break;
@@ -861,7 +816,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         ok = false;
                         break;
                     }
-                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 1);
                     const uint32_t stage = ptx::smem_u32(smem + C::OFF_KV + s * C::STAGE_BYTES);
                     const int32_t *rc = rowc + act[a] * kBN;
                         // unrolled by 2 only: the first tile runs this code cold (the
@@ -877,7 +831,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
                     }
                     ptx::cp_async_arrive_noinc(kv_full(s));
-                    if (g == 0 && lane == 0) SA_TRACE_POINT(0, a, 2);
                 }
                 ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
                 (void)ok;
@@ -894,34 +847,34 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 long long t0 = 0;
                 while (ok && pn < n_act) {
                     bool prog = false;
-                    // S(q) overwrites the single S buffer once S(q-1) has been read
-                    if (qn < n_act && qn <= pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1) &&
-                        (qn == 0 || ptx::mbar_test_wait(s_empty, (qn - 1) & 1))) {
+                    // S(q) goes to buffer q & 1, whose previous tile q-2 holds
+                    // P there until its P.V has read it: QK^T(q) is issued
+                    // only after P.V(q-2) (the MMAs of a CTA run in issue
+                    // order), so at most two tiles of S are ahead of P.V
+                    if (qn < n_act && qn < pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1)) {
                         ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> MMA reads
                         ptx::tc_fence_after();
                         const uint32_t ka = ptx::smem_u32(smem + C::OFF_KV + (qn % C::NS) * C::STAGE_BYTES);
+                        const uint32_t sa = tbase + C::S_COL + (qn & 1) * kBN;
     #pragma unroll
                         for (int k = 0; k < DC / 16; ++k) {
                             const uint64_t bd = ptx::sdesc_sw128(ka + (k / 4) * (kBN * 128) + (k % 4) * 32, 16, 1024);
-                            ptx::mma_ts(tbase + C::S_COL, tbase + C::Q_COL + k * 8, bd, idesc_qk, k > 0 ? 1u : 0u);
+                            ptx::mma_ts(sa, tbase + C::Q_COL + k * 8, bd, idesc_qk, k > 0 ? 1u : 0u);
                         }
-                        ptx::mma_commit(s_full);
-                        SA_TRACE_POINT(1, qn, 0);
+                        ptx::mma_commit(s_full(qn & 1));
                         ++qn;
                         prog = true;
                     } else if (pn < qn && ptx::mbar_test_wait(p_full(pn & 1), (pn >> 1) & 1)) {
                         ptx::tc_fence_after();
                         const uint32_t va = ptx::smem_u32(smem + C::OFF_KV + (pn % C::NS) * C::STAGE_BYTES);
-                        const uint32_t pa = tbase + C::P_COL + (pn & 1) * (kBN / 2);
+                        const uint32_t pa = tbase + C::S_COL + (pn & 1) * kBN;   // P: bf16 pairs, 32 columns
     #pragma unroll
                         for (int t = 0; t < kBN / 16; ++t) {
                             const uint64_t bd = ptx::sdesc_sw128(va + t * 2048, kBN * 128, 1024);
                             ptx::mma_ts(tbase + C::O_COL, pa + t * 8, bd, idesc_pv, (pn > 0 || t > 0) ? 1u : 0u);
                         }
                         ptx::mma_commit(kv_empty(pn % C::NS));
-                        ptx::mma_commit(p_empty(pn & 1));
                         ptx::mma_commit(o_done);
-                        SA_TRACE_POINT(1, pn, 1);
                         ++pn;
                         prog = true;
                     }
@@ -929,9 +882,13 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         idle = 0;
                     } else if (++idle == 1) {
                         t0 = clock64();
-                    } else if ((idle & 1023u) == 0 && clock64() - t0 > kWaitCycles) {
-                        record_error(kErrWaitTimeout);
-                        ok = false;
+                    } else if ((idle & 1023u) == 0) {
+                        if (*reinterpret_cast<volatile int *>(&g_device_error) != 0) {
+                            ok = false;
+                        } else if (clock64() - t0 > kWaitCycles) {
+                            record_error(kErrWaitTimeout);
+                            ok = false;
+                        }
                     }
                 }
                 ptx::mma_commit(mma_done);
@@ -943,8 +900,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     } else {
         ptx::setmaxnreg_inc<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax / epilogue
-        // thread = (head row h, column half): columns [32*half, 32*half+32) of
-        // every tile and [half*DC/2, (half+1)*DC/2) of q and o
+        // Q copy and epilogue: thread = (head row h, column half), columns
+        // [half*DC/2, (half+1)*DC/2) of q and o; the softmax maps threads
+        // to TMEM lanes differently (below)
         const int quarter = warp & 3;            // TMEM lanes this warp may access
         const int half = warp >> 2;
         const int h = quarter * 32 + lane;       // head row == TMEM lane
@@ -992,226 +950,287 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(q_ready);
-            if (tid == 0) SA_TRACE_POINT(2, 0, 11);
         }
 
-        uint32_t xrow_rem = 0, xfull_rem0 = 0, xfull_rem1 = 0, xempty_rem0 = 0, xempty_rem1 = 0;
-        if constexpr (CL == 2) {
-            xrow_rem = ptx::map_to_rank(ptx::smem_u32(smem + C::OFF_X + h * 16), rank ^ 1u);
-            xfull_rem0 = ptx::map_to_rank(x_full(0), rank ^ 1u);
-            xfull_rem1 = ptx::map_to_rank(x_full(1), rank ^ 1u);
-            xempty_rem0 = ptx::map_to_rank(x_empty(0), rank ^ 1u);
-            xempty_rem1 = ptx::map_to_rank(x_empty(1), rank ^ 1u);
-        }
-        const uint32_t s_addr = lane_addr + C::S_COL + 32 * half;
-        // read this thread's 32 partial logits of tile j (frees the S buffer)
-        // and, with a partner, send them to its receive buffer j & 1 as
-        // asynchronous stores that complete_tx on the partner's x_full
-        auto take = [&](int j, uint32_t (&r)[32]) -> bool {
-            if (tid == 0) SA_TRACE_POINT(2, j, 0);
-            if (!wait_all(s_full, j & 1)) return false;
-            if (tid == 0) SA_TRACE_POINT(2, j, 1);
-            ptx::tc_fence_after();
-            ptx::tmem_ld32(s_addr, r);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(s_empty);
-            if constexpr (CL == 2) {
-                // Both CTAs use the block-floating-point value of BOTH partials,
-                // so the two sums (and everything after them) are bit-identical.
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(r[i])));
-                const BfpStep st = bfp_step(amax);
-                const float step = st.step;
-                const float nbias = -kBfpMagic * step;
-                uint32_t m[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float y0 = fmaf(__uint_as_float(r[2 * i]), st.inv, kBfpMagic);
-                    const float y1 = fmaf(__uint_as_float(r[2 * i + 1]), st.inv, kBfpMagic);
-                    m[i] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
-                    r[2 * i] = __float_as_uint(fmaf(y0, step, nbias));   // own partial, same rounding
-                    r[2 * i + 1] = __float_as_uint(fmaf(y1, step, nbias));
-                }
-                if (j >= 2 && !wait_all(x_empty(j & 1), ((j >> 1) - 1) & 1)) return false;
-                if (tid == 0) SA_TRACE_POINT(2, j, 2);
-                // chunk-major codes [8 chunks][128 rows][16 B] (each warp
-                // instruction writes 512 contiguous bytes), then the steps
-                const uint32_t buf = xrow_rem + uint32_t(j & 1) * C::X_BYTES;
-                const uint32_t xb = (j & 1) ? xfull_rem1 : xfull_rem0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    ptx::st_async_v4(buf + uint32_t(4 * half + c) * (kM * 16u), m[4 * c], m[4 * c + 1], m[4 * c + 2],
-                                     m[4 * c + 3], xb);
-                ptx::st_async_b32(buf - uint32_t(h) * 16u + C::XQ_BYTES + uint32_t(half * kM + h) * 4u,
-                                  __float_as_uint(step), xb);
-                if (tid == 0) SA_TRACE_POINT(2, j, 3);
-            }
-            return true;
-        };
+        // ---------------------------------------------------------- softmax
+        // Warp w reads TMEM lanes [16*half, 16*half + 16) of quarter w % 4
+        // with the 16x256b shape: for 8-column step k of a tile a thread holds
+        // rows rA = g8 and rB = g8 + 8 of those lanes at columns 8k + 2qu and
+        // 8k + 2qu + 1 (registers 4k .. 4k+3: rA, rA, rB, rB).  P of the same
+        // two columns is one bf16 pair, which the 16x128b shape stores at
+        // TMEM column 4k + qu of the same rows: the K-pair index of those
+        // columns, as the P.V MMA reads its A operand.
+        const int qu = lane & 3, g8 = lane >> 2;
+        const uint32_t half_addr = tbase + (uint32_t(quarter * 32 + half * 16) << 16);
+        const bool owner = CL == 1 || half == int(crank);
+        const float sl2 = p.scale_log2;
         bool ok = true;
-        constexpr bool pos_scale = kPosScale;
-        float m_run = -INFINITY, l_run = 0.f;
-        uint32_t cur[32], nxt[32];
-        if (clustered) ptx::cluster_wait();   // before the first remote access
-        if (n_act > 0) ok = take(0, cur);
-        int a = 0;
-        for (; ok && a < n_act; ++a) {
-            const uint32_t vm = uint32_t(vmask[act[a]] >> (32 * half));
-            if (a + 1 < n_act && !take(a + 1, nxt)) {
-                ok = false;
-                break;
+        // O rows of this warp's lanes times alA (row rA) and alB (row rB)
+        auto rescale_rows = [&](float alA, float alB) {
+#pragma unroll 1
+            for (int c = 0; c < DC; c += 64) {
+                uint32_t r[32];
+                ptx::tmem_ld_16x256b_x8(half_addr + C::O_COL + c, r);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    r[4 * k] = __float_as_uint(__uint_as_float(r[4 * k]) * alA);
+                    r[4 * k + 1] = __float_as_uint(__uint_as_float(r[4 * k + 1]) * alA);
+                    r[4 * k + 2] = __float_as_uint(__uint_as_float(r[4 * k + 2]) * alB);
+                    r[4 * k + 3] = __float_as_uint(__uint_as_float(r[4 * k + 3]) * alB);
+                }
+                ptx::tmem_st_16x256b_x8(half_addr + C::O_COL + c, r);
             }
-            float s[32];
-            if constexpr (CL == 2) {
-                if (tid == 0) ptx::mbar_arrive_expect_tx(x_full(a & 1), C::X_BYTES);
-                if (tid == 0) SA_TRACE_POINT(2, a, 4);
-                if (!wait_all<true>(x_full(a & 1), (a >> 1) & 1)) {
+            ptx::tmem_wait_st();
+        };
+        // partner addresses (the same offsets in the other CTA of the pair)
+        auto remote = [&](uint32_t local) { return ptx::map_to_rank(local, rank ^ 1u); };
+        auto x_buf = [&](int b2) { return ptx::smem_u32(smem + C::OFF_X + (b2 * 4 + quarter) * C::XQ); };
+        auto pm_buf = [&](int b2) { return ptx::smem_u32(smem + C::OFF_PM + (b2 * 4 + quarter) * C::PMQ); };
+        if (clustered) ptx::cluster_wait();   // before the first remote access
+        if (owner) {
+            // ------------------------------------------------ owner rows
+            float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+            for (int a = 0; a < n_act; ++a) {
+                const int sb = a & 1;
+                const uint32_t ph = uint32_t(a >> 1) & 1u;
+                if constexpr (CL == 2) {
+                    if (lane == 0) ptx::mbar_arrive_expect_tx(x_full(sb, quarter), C::XQ);
+                }
+                if (!wait_all(s_full(sb), ph)) {
                     ok = false;
                     break;
                 }
-                if (tid == 0) SA_TRACE_POINT(2, a, 5);
-                const uint8_t *xbuf = smem + C::OFF_X + (a & 1) * C::X_BYTES;
-                const float step = *reinterpret_cast<const float *>(xbuf + C::XQ_BYTES + (half * kM + h) * 4);
-                const float dbias = -kBfpDecodeBias * step;
+                ptx::tc_fence_after();
+                float s[32];
+                {
+                    uint32_t r[32];
+                    ptx::tmem_ld_16x256b_x8(half_addr + C::S_COL + sb * kBN, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; ++i2) s[i2] = __uint_as_float(r[i2]);
+                }
+                if constexpr (CL == 2) {
+                    // + the partner's partial logits of the same rows and columns
+                    if (!wait_all<true>(x_full(sb, quarter), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *xb = smem + C::OFF_X + (sb * 4 + quarter) * C::XQ + lane * 16;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 v = *reinterpret_cast<const float4 *>(xb + k * 512);
+                        s[4 * k] += v.x;
+                        s[4 * k + 1] += v.y;
+                        s[4 * k + 2] += v.z;
+                        s[4 * k + 3] += v.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_remote_relaxed(remote(x_empty(sb, quarter)));
+                }
+                // Row maxima of scale * s over the valid columns.  With a
+                // positive scale (the usual case) invalid slots become -inf,
+                // the scale is applied once to the maximum, and 2^(scale *
+                // -inf - m) gives P = 0 below.  A zero or negative scale would
+                // turn -inf into NaN or +inf, so it takes a path that leaves
+                // invalid slots out of the maximum and selects P = 0 for them.
+                const uint64_t vm = vmask[act[a]];
+                const bool full = vm == ~0ull;
+                const uint64_t vq = vm >> (2 * qu);   // bit 8k + e: column 8k + 2qu + e
+                float mxA = -INFINITY, mxB = -INFINITY;
+                if constexpr (kPosScale) {
+                    if (!full) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                if (!((vq >> (8 * k + e)) & 1ull)) s[4 * k + e] = s[4 * k + 2 + e] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        mxA = fmaxf(mxA, fmaxf(s[4 * k], s[4 * k + 1]));
+                        mxB = fmaxf(mxB, fmaxf(s[4 * k + 2], s[4 * k + 3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if ((vq >> (8 * k + e)) & 1ull) {
+                                mxA = fmaxf(mxA, s[4 * k + e] * sl2);
+                                mxB = fmaxf(mxB, s[4 * k + 2 + e] * sl2);
+                            }
+                }
+                mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+                mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+                mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+                mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+                if constexpr (kPosScale) {
+                    mxA *= sl2;
+                    mxB *= sl2;
+                }
+                // lazy rescale: the running maximum moves only when a row's
+                // maximum grows by more than the threshold; the factor goes to
+                // the partner, which scales its half of the row's O
+                float alA = 1.f, alB = 1.f;
+                if (a == 0) {
+                    mA = mxA;
+                    mB = mxB;
+                } else {
+                    const bool needA = mxA > mA + kRescaleThreshold;
+                    const bool needB = mxB > mB + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, needA || needB)) {
+                        if (needA) {
+                            alA = exp2f(mA - mxA);
+                            lA *= alA;
+                            mA = mxA;
+                        }
+                        if (needB) {
+                            alB = exp2f(mB - mxB);
+                            lB *= alB;
+                            mB = mxB;
+                        }
+                        if (!wait_all(o_done, uint32_t(a - 1) & 1u)) {   // P.V(a-1) done
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        rescale_rows(alA, alB);
+                    }
+                }
+                // P = 2^(scale*s - m) as bf16 pairs (invalid slots give exactly
+                // 0); l sums the rounded values the MMA accumulates
+                uint32_t pw[16];
+                float sumA = 0.f, sumB = 0.f;
+                const float nA = -mA, nB = -mB;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float p0 = ex2_approx(fmaf(s[4 * k], sl2, nA));
+                    float p1 = ex2_approx(fmaf(s[4 * k + 1], sl2, nA));
+                    float p2 = ex2_approx(fmaf(s[4 * k + 2], sl2, nB));
+                    float p3 = ex2_approx(fmaf(s[4 * k + 3], sl2, nB));
+                    if constexpr (!kPosScale) {
+                        if (!full) {
+                            const bool v0 = (vq >> (8 * k)) & 1ull, v1 = (vq >> (8 * k + 1)) & 1ull;
+                            p0 = v0 ? p0 : 0.f;
+                            p2 = v0 ? p2 : 0.f;
+                            p1 = v1 ? p1 : 0.f;
+                            p3 = v1 ? p3 : 0.f;
+                        }
+                    }
+                    pw[2 * k] = pack_bf16(p0, p1, sumA);
+                    pw[2 * k + 1] = pack_bf16(p2, p3, sumB);
+                }
+                lA += sumA;
+                lB += sumB;
+                if constexpr (CL == 2) {
+                    // P of these rows and their rescale factors to the partner
+                    if (a >= 2 && !wait_all(pm_empty(sb, quarter), uint32_t((a >> 1) - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = remote(pm_buf(sb)), fbar = remote(pm_full(sb, quarter));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        ptx::st_async_v4(dst + uint32_t(c * 512 + lane * 16), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
+                                         pw[4 * c + 3], fbar);
+                    if (qu < 2)
+                        ptx::st_async_b32(dst + uint32_t(C::PM_P + (qu * 8 + g8) * 4),
+                                          __float_as_uint(qu == 0 ? alA : alB), fbar);
+                }
+                ptx::tmem_st_16x128b_x8(half_addr + C::S_COL + sb * kBN, pw);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(p_full(sb));
+            }
+            // row statistics (m, l) of these rows, here and at the partner
+            lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+            lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+            lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+            lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+            if (qu == 0) {
+                const int rA = quarter * 32 + half * 16 + g8;
+                stat[rA] = make_float2(mA, lA);
+                stat[rA + 8] = make_float2(mB, lB);
+                if constexpr (CL == 2) {
+                    const uint32_t dst = remote(ptx::smem_u32(&stat[rA])), sbar = remote(stat_bar);
+                    ptx::st_async_v2(dst, __float_as_uint(mA), __float_as_uint(lA), sbar);
+                    ptx::st_async_v2(dst + 64, __float_as_uint(mB), __float_as_uint(lB), sbar);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(stat_bar);
+        } else if constexpr (CL == 2) {
+            // ------------------------------------------------ partner rows
+            // S of tile j (partner rows) to the partner, one tile ahead
+            auto send_s = [&](int j2) -> bool {
+                const int jb = j2 & 1;
+                if (!wait_all(s_full(jb), uint32_t(j2 >> 1) & 1u)) return false;
+                ptx::tc_fence_after();
+                uint32_t r[32];
+                ptx::tmem_ld_16x256b_x8(half_addr + C::S_COL + jb * kBN, r);
+                ptx::tmem_wait_ld();
+                if (j2 >= 2 && !wait_all(x_empty(jb, quarter), uint32_t((j2 >> 1) - 1) & 1u)) return false;
+                const uint32_t dst = remote(x_buf(jb)) + uint32_t(lane * 16), fbar = remote(x_full(jb, quarter));
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    ptx::st_async_v4(dst + uint32_t(k * 512), r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3], fbar);
+                return true;
+            };
+            if (quarter == 0 && lane == 0) ptx::mbar_arrive_expect_tx(stat_bar, 64 * 8);
+            if (n_act > 0) ok = send_s(0);
+            for (int a = 0; ok && a < n_act; ++a) {
+                if (a + 1 < n_act && !send_s(a + 1)) {
+                    ok = false;
+                    break;
+                }
+                const int sb = a & 1;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(pm_full(sb, quarter), C::PMQ);
+                if (!wait_all<true>(pm_full(sb, quarter), uint32_t(a >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *pm = smem + C::OFF_PM + (sb * 4 + quarter) * C::PMQ;
+                uint32_t pw[16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xbuf + (4 * half + c) * (kM * 16) + h * 16);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 8 * c + 2 * e;
-                        const float lo = fmaf(__uint_as_float((w[e] & 0xFFFFu) | 0x4B000000u), step, dbias);
-                        const float hi = fmaf(__uint_as_float((w[e] >> 16) | 0x4B000000u), step, dbias);
-                        s[i] = __uint_as_float(cur[i]) + lo;
-                        s[i + 1] = __uint_as_float(cur[i + 1]) + hi;
-                    }
+                    const uint4 v = *reinterpret_cast<const uint4 *>(pm + c * 512 + lane * 16);
+                    pw[4 * c] = v.x;
+                    pw[4 * c + 1] = v.y;
+                    pw[4 * c + 2] = v.z;
+                    pw[4 * c + 3] = v.w;
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(cur[j]);
-            }
-            // masked, scaled row max of this half (the scale is applied once,
-            // to the max, when it is positive; invalid slots become -inf)
-            // Row max of scale * s over the valid slots.  With a positive scale
-            // (the usual case) invalid slots become -inf, the scale is applied
-            // once to the max, and 2^(scale * -inf - m) gives P = 0 below.  A
-            // zero or negative scale would turn -inf into NaN or +inf, so it
-            // takes a path that leaves invalid slots out of the max and
-            // selects P = 0 for them.
-            const bool full = vm == 0xFFFFFFFFu;
-            float mloc = -INFINITY;
-            if constexpr (pos_scale) {
-                if (!full) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[j] = ((vm >> j) & 1u) ? s[j] : -INFINITY;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) mloc = fmaxf(mloc, s[j]);
-                mloc *= p.scale_log2;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((vm >> j) & 1u) mloc = fmaxf(mloc, s[j] * p.scale_log2);
-            }
-            // row max over both column halves
-            if (tid == 0) SA_TRACE_POINT(2, a, 6);
-            red[(a & 1) * 256 + half * 128 + h] = mloc;
-            ptx::mbar_arrive(red_bar);
-            if (!wait_all(red_bar, a & 1)) {
-                ok = false;
-                break;
-            }
-            if constexpr (CL == 2) {
-                // every softmax thread has read receive buffer a & 1: return the credit
-                if (tid == 0) ptx::mbar_arrive_remote_relaxed((a & 1) ? xempty_rem1 : xempty_rem0);
-            }
-            if (tid == 0) SA_TRACE_POINT(2, a, 7);
-            const float mx = fmaxf(mloc, red[(a & 1) * 256 + (half ^ 1) * 128 + h]);
-            // P buffer a & 1 is free once the P.V of tile a-2 has completed
-            if (a >= 2 && !wait_all(p_empty(a & 1), ((a >> 1) - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            if (tid == 0) SA_TRACE_POINT(2, a, 8);
-            if (a == 0) {
-                m_run = mx;
-            } else {
-                // lazy rescale: only when the running max grows by more than
-                // the threshold; warp-uniform because TMEM access is
-                const bool need = mx > m_run + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? exp2f(m_run - mx) : 1.f;
-                    if (need) {
-                        l_run *= alpha;
-                        m_run = mx;
-                    }
-                    if (!wait_all(o_done, (a - 1) & 1)) {  // previous P.V done
+                const float alA = reinterpret_cast<const float *>(pm + C::PM_P)[g8];
+                const float alB = reinterpret_cast<const float *>(pm + C::PM_P)[8 + g8];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_remote_relaxed(remote(pm_empty(sb, quarter)));
+                if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
+                    if (!wait_all(o_done, uint32_t(a - 1) & 1u)) {   // P.V(a-1) done
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-#pragma unroll 1
-                    for (int ch = 0; ch < DC / 64; ++ch) {
-                        uint32_t r[32];
-                        const uint32_t oc = lane_addr + C::O_COL + half * (DC / 2) + ch * 32;
-                        ptx::tmem_ld32(oc, r);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        ptx::tmem_st32(oc, r);
-                    }
+                    rescale_rows(alA, alB);
                 }
+                ptx::tmem_st_16x128b_x8(half_addr + C::S_COL + sb * kBN, pw);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(p_full(sb));
             }
-            // P = 2^(scale*s - m) as bf16 pairs into TMEM (A operand of P.V);
-            // invalid slots give exactly 0
-            uint32_t pw[16];
-            float lsum = 0.f;
-            const float nm = -m_run;
-            // two copies of the loop keep the usual path free of selects
-            auto p_tile = [&](auto masked) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, nm));
-                    float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, nm));
-                    if constexpr (decltype(masked)::value) {
-                        p0 = ((vm >> (2 * c)) & 1u) ? p0 : 0.f;
-                        p1 = ((vm >> (2 * c + 1)) & 1u) ? p1 : 0.f;
-                    }
-                    lsum += p0 + p1;
-                    const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-                    pw[c] = *reinterpret_cast<const uint32_t *>(&v);
-                }
-            };
-            if (pos_scale || full) {
-                p_tile(std::false_type{});
-            } else if constexpr (!pos_scale) {
-                p_tile(std::true_type{});
-            }
-            ptx::tmem_st16(lane_addr + C::P_COL + (a & 1) * (kBN / 2) + half * 16, pw);
-            ptx::tmem_wait_st();
-            if (tid == 0) SA_TRACE_POINT(2, a, 9);
-            l_run += lsum;
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(p_full(a & 1));
-            if (tid == 0) SA_TRACE_POINT(2, a, 10);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
         }
         // ------------------------------------------------------------ epilogue
-        if (tid == 0) SA_TRACE_POINT(3, 0, 2);
-        SA_CTA_POINT(2);
+        // thread = (head row h, column half) again: columns [half*DC/2,
+        // (half+1)*DC/2) of row h of O, with the row's (m, l) from the table
         if (ok) ok = wait_all(mma_done, 0);
-        if (tid == 0) SA_TRACE_POINT(3, 0, 4);
-        float l_tot = l_run;
+        if (ok) ok = wait_all<CL == 2>(stat_bar, 0);
+        float m_run = -INFINITY, l_tot = 0.f;
         if (ok) {
-            red[2 * 256 + half * 128 + h] = l_run;
-            ptx::mbar_arrive(l_bar);
-            ok = wait_all(l_bar, 0);
-            if (ok) l_tot = l_run + red[2 * 256 + (half ^ 1) * 128 + h];
+            const float2 st = stat[h];
+            m_run = st.x;
+            l_tot = st.y;
         }
-        if (tid == 0) SA_TRACE_POINT(3, 0, 5);
         ptx::tc_fence_after();
         if (ok) {
             // Output rows are staged in shared memory (the kv ring, receive
@@ -1286,16 +1305,13 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                     p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
                 }
             }
-            if (tid == 0) SA_TRACE_POINT(3, 0, 6);
         }
         ptx::setmaxnreg_dec<kLaunchRegs>();
     }
 
     // ---------------------------------------------------------------- teardown
-    if (tid == 0) SA_TRACE_POINT(3, 0, 3);
     ptx::tc_fence_before();
     __syncthreads();
-    if (tid == 0) SA_TRACE_POINT(3, 0, 8);
     if (warp == kMmaWarp) {
         if (lane == 0) wait_bar(mma_done, 0);  // no MMA in flight before TMEM is released
         __syncwarp();
@@ -1304,7 +1320,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     }
     // the staged rows leave (all warps); a fused split keeps its own combine rows
     copy_out_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
-    if (tid == 0) SA_TRACE_POINT(3, 0, 7);
     if (p.fused) {
         // Every split of this token has published its partial rows and
         // log-sum-exp (release/acquire at cluster scope); all partner
@@ -1312,13 +1327,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // of this CTA's DC columns: its own partial from shared memory, the
         // others' from L2, in the log-sum-exp form with the sink added once.
         ptx::cluster_sync();
-        if (tid == 0) SA_TRACE_POINT(3, 0, 15);
         combine_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
     } else if constexpr (CL == 2) {
         ptx::cluster_sync();  // no remote access outlives the partner
     }
-    if (tid == 0) SA_TRACE_POINT(3, 0, 9);
-    SA_CTA_POINT(3);
 }
 
 // Split-KV combine (§5.5, log-sum-exp form with the sink added exactly once):
@@ -1336,9 +1348,6 @@ attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws
     constexpr int G = E / V;               // vectors per lane
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);  // tok * H + h
-#ifdef SA_TRACE
-    if (threadIdx.x == 0) atomicMin(&g_sa_comb[0], sa_gtime());
-#endif
     if (row >= rows) return;
     const int64_t tok = row / H, h = row % H;
     const float *lse = ws_lse + tok * ns * H + h;
@@ -1392,9 +1401,6 @@ attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws
             *reinterpret_cast<__nv_bfloat162 *>(dst + g * 64) = lo;
         }
     }
-#ifdef SA_TRACE
-    if (lane == 0) atomicMax(&g_sa_comb[1], sa_gtime());
-#endif
 }
 
 // ---------------------------------------------------------------- host side
@@ -1617,23 +1623,6 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-#ifdef SA_TRACE
-}  // namespace sa
-extern "C" int sa_trace_read(long long *out) { return (int)cudaMemcpyFromSymbol(out, sa::g_sa_trace, sizeof(sa::g_sa_trace)); }
-extern "C" int sa_trace_clear() {
-    static long long z[4 * 64 * 16] = {0};
-    static unsigned long long zc[4096 * 4] = {0};
-    unsigned long long comb[2] = {~0ull, 0ull};
-    cudaMemcpyToSymbol(sa::g_sa_cta, zc, sizeof(zc));
-    cudaMemcpyToSymbol(sa::g_sa_comb, comb, sizeof(comb));
-    return (int)cudaMemcpyToSymbol(sa::g_sa_trace, z, sizeof(z));
-}
-extern "C" int sa_trace_read_cta(unsigned long long *cta, unsigned long long *comb) {
-    cudaMemcpyFromSymbol(comb, sa::g_sa_comb, sizeof(sa::g_sa_comb));
-    return (int)cudaMemcpyFromSymbol(cta, sa::g_sa_cta, sizeof(sa::g_sa_cta));
-}
-namespace sa {
-#endif
 
 // Self-test of the bounded wait: one warp waits, with the kernel's own wait
 // routine and a short cycle limit, on an mbarrier phase that nothing ever
