@@ -18,9 +18,10 @@
 //                        zero-filled) into the 128B-swizzled K-major stage the
 //                        MMAs read;
 //   warp 8 (MMA)         S = Q_c K_c^T with Q_c resident in TMEM, into one of
-//                        two S buffers; O_c += P V_c with P (bf16) in the same
-//                        TMEM buffer its S came from and V_c the same stage
-//                        read MN-major; O_c resident in TMEM for the unit;
+//                        two S buffers (QK^T runs up to two tiles ahead of
+//                        the softmax); O_c += P V_c with P (bf16) in one of two
+//                        shared-memory buffers and V_c the same stage read
+//                        MN-major; O_c resident in TMEM for the unit;
 //   warps 0..7 (softmax) warp w reads the 16 TMEM lanes [16*(w/4), +16) of
 //                        lane quarter w%4 (16x256b: a thread holds two head
 //                        rows x 16 of the tile's 64 columns, four threads per
@@ -31,15 +32,14 @@
 // [16c, 16c+16) of every quarter.  The "sender" warps of a CTA (the lanes it
 // does not own) copy their fp32 partial logits to the owner, exactly; the
 // "owner" warps add the partner's partials to their own, run the online
-// softmax, write P for their rows into their own TMEM and send it (bf16,
-// with each row's rescale factor) to the partner, whose sender warps store
-// it into the partner's TMEM and apply the factor to the partner's half of
-// O.  So each CTA runs the softmax of half the rows, and every logit is the
-// plain fp32 sum of the two MMA partials.
+// softmax and write P for their rows into the P buffer; one bulk copy per
+// warp puts the same rows into the partner's P buffer, and each row's
+// rescale factor goes with them to the partner's sender warps, which apply
+// it to the partner's half of O.  So each CTA runs the softmax of half the
+// rows, and every logit is the plain fp32 sum of the two MMA partials.
 //
 // TMEM columns (D = 512, DC = 256): O_c [0,256) fp32, S [256,384) two 64-col
-// buffers (P of a tile overwrites the first 32 columns of its own S buffer),
-// Q_c [384,512) bf16 pairs.  Every buffer hand-off is an mbarrier phase that
+// buffers, Q_c [384,512) bf16 pairs.  Every buffer hand-off is an mbarrier phase that
 // is never more than one phase away from its waiter; every mbarrier wait is
 // bounded by clock64 and gives up early once any wait of any kernel has
 // recorded an error, so a failing launch drains in about one wait bound.
@@ -99,12 +99,12 @@ struct Cfg {
     static_assert(DC == 64 || DC == 128 || DC == 256, "per-CTA head-dim slice");
     static_assert(!F8 || (DC == 256 && CL == 2), "FP8 rows only at D = 512 (two 256-column halves)");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
-    static constexpr int NS = F8 ? 3 : (CL == 2 ? 5 : 4);  // kv ring depth (bf16 stages the MMA reads)
+    static constexpr int NS = F8 ? 3 : 4;   // kv ring depth (bf16 stages the MMA reads)
     // FP8: the raw bytes of a tile land in one of NF staging buffers (one
     // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
     // values at [0, 320), its scale bytes at 320) and are widened to bf16
     // into a kv stage by the gather warps
-    static constexpr int NF = F8 ? 3 : 0;
+    static constexpr int NF = F8 ? 2 : 0;
     static constexpr int STG_ROW = 336;
     static constexpr int STG_SCALE = 320;
     static constexpr int STG_BYTES = kBN * STG_ROW;
@@ -114,32 +114,37 @@ struct Cfg {
     static_assert(THREADS == 512, "four warpgroups");
     static_assert(kSoftmaxThreads * kSoftmaxRegs + (THREADS - kSoftmaxThreads) * kOtherRegs == THREADS * kLaunchRegs,
                   "register split equals the launch allocation");
-    // Partner messages (CL == 2), one buffer per (S buffer b, lane quarter q):
+    // P of a tile (bf16, the A operand of P.V): [128 rows][64] in the
+    // 128B-swizzled K-major layout (8-row atoms of 1 KB), two buffers.
+    static constexpr int P_BYTES = kM * kBN * 2;
+    // Partner messages (CL == 2), one buffer per (tile parity b, lane quarter q):
     //   X: the partner's fp32 partial logits of this CTA's 16 rows of the
     //      quarter, [8 chunks][32 lanes][16 B] (chunk k = the four values of
     //      16x256b repetition k);
-    //   PM: the partner's P of its 16 rows, [4 chunks][32 lanes][16 B] (the
-    //      16 words of a 16x128b.x8 store), then one fp32 rescale factor per
-    //      row (16 x 4 B).
+    //   F: one fp32 rescale factor for each of the partner's 16 rows of the
+    //      quarter (its P rows arrive directly in the P buffer).
     static constexpr int XQ = 8 * 32 * 16;
-    static constexpr int PM_P = 4 * 32 * 16;
-    static constexpr int PMQ = PM_P + 16 * 4;
+    static constexpr int FQ = 16 * 4;
     static constexpr int OFF_KV = 0;
     static constexpr int OFF_STG = OFF_KV + NS * STAGE_BYTES;
-    static constexpr int OFF_X = OFF_STG + NF * STG_BYTES;
-    static constexpr int OFF_PM = OFF_X + (CL == 2 ? 2 * 4 * XQ : 0);
-    static constexpr int OFF_IDX = OFF_PM + (CL == 2 ? 2 * 4 * PMQ : 0);
+    static constexpr int OFF_P = OFF_STG + NF * STG_BYTES;
+    static_assert(OFF_P % 1024 == 0, "P buffers keep the 1 KB swizzle alignment");
+    static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_F = OFF_X + (CL == 2 ? 2 * 4 * XQ : 0);
+    static constexpr int OFF_IDX = OFF_F + (CL == 2 ? 2 * 4 * FQ : 0);
     static constexpr int OFF_VALID = OFF_IDX + kMaxUnitSlots * 4;
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
     static constexpr int OFF_STAT = OFF_LIST + kMaxUnitTiles * 4 + 16;  // float2 [128]: (m, l) per row
     static constexpr int OFF_LSE = OFF_STAT + kM * 8;                   // float [8 splits][128]
     static constexpr int OFF_SINK = OFF_LSE + 8 * kM * 4;               // float [128]
     static constexpr int OFF_BAR = OFF_SINK + kM * 4;
-    // kv_full[NS] kv_empty[NS] s_full[2] p_full[2] o_done q_ready mma_done
-    // stat_bar q_smem q_free (2 spare) x_full[8] x_empty[8] pm_full[8]
-    // pm_empty[8] ([buffer][quarter]); FP8: + stg_full[NF] stg_empty[NF]
-    static constexpr int BAR_X = 2 * NS + 12;
-    static constexpr int NUM_BARS = BAR_X + 32 + 2 * NF;
+    // kv_full[NS] kv_empty[NS] s_full[2] s_empty[2] p_full[2] p_empty[2]
+    // o_done[2] q_ready mma_done stat_bar q_smem q_free, then x_full[8]
+    // x_empty[8] pm_full[8] ([parity][quarter]); FP8: + stg_full[NF]
+    // stg_empty[NF].  The layout is the same in every CTA (p_empty receives
+    // multicast arrivals at its offset).
+    static constexpr int BAR_X = 2 * NS + 15;
+    static constexpr int NUM_BARS = BAR_X + 24 + 2 * NF;
     // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
     // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
     static constexpr int OFF_QS = OFF_KV + (NS - 2) * STAGE_BYTES;
@@ -147,8 +152,7 @@ struct Cfg {
     static_assert(Q_BYTES == 2 * STAGE_BYTES, "Q_c fills two kv stages");
     static constexpr int OFF_TSLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_TSLOT + 16 + 1024;    // + slack to align the base to 1 KB
-    // TMEM columns: O_c fp32, two S buffers of one tile (fp32; P of the tile
-    // as bf16 pairs over its first half), Q_c bf16 pairs
+    // TMEM columns: O_c fp32, two S buffers of one tile (fp32), Q_c bf16 pairs
     static constexpr int O_COL = 0;
     static constexpr int S_COL = DC;
     static constexpr int Q_COL = DC + 2 * kBN;
@@ -157,7 +161,7 @@ struct Cfg {
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // output staging (epilogue): kM rows of up to DC fp32, padded by 16 bytes,
-    // over the kv ring, partner buffers and index lists (all dead by then)
+    // over the kv ring, P and partner buffers and index lists (all dead by then)
     static constexpr int STAGE_ROW = DC * 4 + 16;
     static_assert(kM * STAGE_ROW <= OFF_STAT - OFF_KV, "output staging stays below the row statistics");
 };
@@ -476,20 +480,21 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     auto kv_full = [&](int s) { return bar(s); };
     auto kv_empty = [&](int s) { return bar(C::NS + s); };
     auto s_full = [&](int i) { return bar(2 * C::NS + i); };        // S buffer i written by QK^T
-    auto p_full = [&](int i) { return bar(2 * C::NS + 2 + i); };    // P of buffer i stored, O rows rescaled
-    const uint32_t o_done = bar(2 * C::NS + 4);    // a P.V completed
-    const uint32_t q_ready = bar(2 * C::NS + 5);   // Q_c in TMEM
-    const uint32_t mma_done = bar(2 * C::NS + 6);  // every MMA of the unit completed
-    const uint32_t stat_bar = bar(2 * C::NS + 7);  // row statistics of every row in place
-    const uint32_t q_smem = bar(2 * C::NS + 8);    // Q_c landed in shared memory
-    const uint32_t q_free = bar(2 * C::NS + 9);    // Q_c copied to TMEM: its stages are free
-    // partner messages, per (S buffer b, lane quarter q)
+    auto s_empty = [&](int i) { return bar(2 * C::NS + 2 + i); };   // S buffer i read by every softmax warp
+    auto p_full = [&](int i) { return bar(2 * C::NS + 4 + i); };    // P buffer i complete, O rows rescaled
+    auto p_empty = [&](int i) { return bar(2 * C::NS + 6 + i); };   // P.V of buffer i done (both CTAs of a pair)
+    auto o_done = [&](int i) { return bar(2 * C::NS + 8 + i); };    // the P.V of a tile of parity i completed
+    const uint32_t q_ready = bar(2 * C::NS + 10);  // Q_c in TMEM
+    const uint32_t mma_done = bar(2 * C::NS + 11); // every MMA of the unit completed
+    const uint32_t stat_bar = bar(2 * C::NS + 12); // row statistics of every row in place
+    const uint32_t q_smem = bar(2 * C::NS + 13);   // Q_c landed in shared memory
+    const uint32_t q_free = bar(2 * C::NS + 14);   // Q_c copied to TMEM: its stages are free
+    // partner messages, per (tile parity b, lane quarter q)
     auto x_full = [&](int b2, int q) { return bar(C::BAR_X + b2 * 4 + q); };        // partner's partials landed
     auto x_empty = [&](int b2, int q) { return bar(C::BAR_X + 8 + b2 * 4 + q); };   // partner read our partials
-    auto pm_full = [&](int b2, int q) { return bar(C::BAR_X + 16 + b2 * 4 + q); };  // partner's P rows landed
-    auto pm_empty = [&](int b2, int q) { return bar(C::BAR_X + 24 + b2 * 4 + q); }; // partner read our P rows
-    auto stg_full = [&](int f) { return bar(C::BAR_X + 32 + f); };            // FP8: staging f landed
-    auto stg_empty = [&](int f) { return bar(C::BAR_X + 32 + C::NF + f); };   // FP8: staging f widened
+    auto pm_full = [&](int b2, int q) { return bar(C::BAR_X + 16 + b2 * 4 + q); };  // partner's P rows + factors landed
+    auto stg_full = [&](int f) { return bar(C::BAR_X + 24 + f); };            // FP8: staging f landed
+    auto stg_empty = [&](int f) { return bar(C::BAR_X + 24 + C::NF + f); };   // FP8: staging f widened
 
     // ---------------------------------------------------------------- prologue
     // The index list heads the longest dependency chain (index -> kv row ->
@@ -540,15 +545,17 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(s_full(i), 1);
-            ptx::mbar_init(p_full(i), kSoftmaxWarps);   // one elected lane per softmax warp
+            ptx::mbar_init(s_empty(i), kSoftmaxWarps);  // one elected lane per softmax warp
+            ptx::mbar_init(p_full(i), kSoftmaxWarps);
+            ptx::mbar_init(p_empty(i), CL);             // the P.V commit of each CTA of the pair
             for (int q = 0; q < 4; ++q) {
                 ptx::mbar_init(x_full(i, q), 1);    // the owner's expect_tx + XQ bytes from the partner
                 ptx::mbar_init(x_empty(i, q), 1);   // one credit from the partner's owner warp
-                ptx::mbar_init(pm_full(i, q), 1);   // the sender's expect_tx + PMQ bytes from the partner
-                ptx::mbar_init(pm_empty(i, q), 1);  // one credit from the partner's sender warp
+                ptx::mbar_init(pm_full(i, q), 1);   // the sender's expect_tx + P rows and factors
             }
         }
-        ptx::mbar_init(o_done, 1);
+        ptx::mbar_init(o_done(0), 1);
+        ptx::mbar_init(o_done(1), 1);
         ptx::mbar_init(q_ready, kSoftmaxThreads);
         ptx::mbar_init(mma_done, 1);
         // owner warps (8, or 4 plus one expect_tx for the partner's 512 bytes)
@@ -847,11 +854,14 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 long long t0 = 0;
                 while (ok && pn < n_act) {
                     bool prog = false;
-                    // S(q) goes to buffer q & 1, whose previous tile q-2 holds
-                    // P there until its P.V has read it: QK^T(q) is issued
-                    // only after P.V(q-2) (the MMAs of a CTA run in issue
-                    // order), so at most two tiles of S are ahead of P.V
-                    if (qn < n_act && qn < pn + 2 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1)) {
+                    // S(q) goes to buffer q & 1 once every softmax warp has
+                    // read S(q-2) from it, and only after P.V(q-3) was issued:
+                    // whoever has seen S(q) then knows that P.V(q-3) is
+                    // complete (the MMAs of a CTA run in issue order), which
+                    // keeps every o_done / p_empty waiter within one phase of
+                    // the phase it waits for.  P.V(p) reads P buffer p & 1.
+                    if (qn < n_act && qn < pn + 3 && ptx::mbar_test_wait(kv_full(qn % C::NS), (qn / C::NS) & 1) &&
+                        (qn < 2 || ptx::mbar_test_wait(s_empty(qn & 1), ((qn >> 1) - 1) & 1))) {
                         ptx::fence_proxy_async_smem();  // gathered rows (generic-proxy writes) -> MMA reads
                         ptx::tc_fence_after();
                         const uint32_t ka = ptx::smem_u32(smem + C::OFF_KV + (qn % C::NS) * C::STAGE_BYTES);
@@ -865,16 +875,23 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                         ++qn;
                         prog = true;
                     } else if (pn < qn && ptx::mbar_test_wait(p_full(pn & 1), (pn >> 1) & 1)) {
+                        ptx::fence_proxy_async_smem();  // P (generic-proxy writes) -> MMA reads
                         ptx::tc_fence_after();
                         const uint32_t va = ptx::smem_u32(smem + C::OFF_KV + (pn % C::NS) * C::STAGE_BYTES);
-                        const uint32_t pa = tbase + C::S_COL + (pn & 1) * kBN;   // P: bf16 pairs, 32 columns
+                        const uint32_t pa = ptx::smem_u32(smem + C::OFF_P + (pn & 1) * C::P_BYTES);
     #pragma unroll
                         for (int t = 0; t < kBN / 16; ++t) {
+                            const uint64_t ad = ptx::sdesc_sw128(pa + t * 32, 16, 1024);
                             const uint64_t bd = ptx::sdesc_sw128(va + t * 2048, kBN * 128, 1024);
-                            ptx::mma_ts(tbase + C::O_COL, pa + t * 8, bd, idesc_pv, (pn > 0 || t > 0) ? 1u : 0u);
+                            ptx::mma_ss(tbase + C::O_COL, ad, bd, idesc_pv, (pn > 0 || t > 0) ? 1u : 0u);
                         }
                         ptx::mma_commit(kv_empty(pn % C::NS));
-                        ptx::mma_commit(o_done);
+                        ptx::mma_commit(o_done(pn & 1));
+                        // P buffer pn & 1 is free here and (with a partner) there
+                        if constexpr (CL == 2)
+                            ptx::mma_commit_multicast(p_empty(pn & 1), uint16_t((1u << rank) | (1u << (rank ^ 1u))));
+                        else
+                            ptx::mma_commit(p_empty(pn & 1));
                         ++pn;
                         prog = true;
                     }
@@ -957,9 +974,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         // with the 16x256b shape: for 8-column step k of a tile a thread holds
         // rows rA = g8 and rB = g8 + 8 of those lanes at columns 8k + 2qu and
         // 8k + 2qu + 1 (registers 4k .. 4k+3: rA, rA, rB, rB).  P of the same
-        // two columns is one bf16 pair, which the 16x128b shape stores at
-        // TMEM column 4k + qu of the same rows: the K-pair index of those
-        // columns, as the P.V MMA reads its A operand.
+        // two columns is one bf16 pair: one 4-byte word of the row in the P
+        // buffer (16-byte chunk k, bytes 4qu..4qu+3), which the P.V MMA reads
+        // from shared memory as its A operand.
         const int qu = lane & 3, g8 = lane >> 2;
         const uint32_t half_addr = tbase + (uint32_t(quarter * 32 + half * 16) << 16);
         const bool owner = CL == 1 || half == int(crank);
@@ -983,10 +1000,20 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             }
             ptx::tmem_wait_st();
         };
+        // Wait until P.V(j) has completed.  Whoever calls this has seen S of
+        // tile j + 1, and QK^T(j+1) is issued after P.V(j-2), so P.V(j-2) is
+        // complete: o_done(j & 1) is at the phase of P.V(j) or past it, and a
+        // parity wait cannot mistake an older phase for it.
+        auto pv_done = [&](int j) -> bool { return wait_all(o_done(j & 1), uint32_t(j >> 1) & 1u); };
         // partner addresses (the same offsets in the other CTA of the pair)
         auto remote = [&](uint32_t local) { return ptx::map_to_rank(local, rank ^ 1u); };
         auto x_buf = [&](int b2) { return ptx::smem_u32(smem + C::OFF_X + (b2 * 4 + quarter) * C::XQ); };
-        auto pm_buf = [&](int b2) { return ptx::smem_u32(smem + C::OFF_PM + (b2 * 4 + quarter) * C::PMQ); };
+        auto f_buf = [&](int b2) { return ptx::smem_u32(smem + C::OFF_F + (b2 * 4 + quarter) * C::FQ); };
+        // this warp's 16 rows of P buffer b2: two 1 KB atoms, rows rA and rA + 8
+        // at row g8 of each (row r of an atom at r * 128, its 16-byte chunk c
+        // at (c ^ r) * 16)
+        const int rowblk = quarter * 32 + half * 16;
+        auto p_rows = [&](int b2) { return smem + C::OFF_P + b2 * C::P_BYTES + (rowblk >> 3) * 1024; };
         if (clustered) ptx::cluster_wait();   // before the first remote access
         if (owner) {
             // ------------------------------------------------ owner rows
@@ -1010,6 +1037,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
 #pragma unroll
                     for (int i2 = 0; i2 < 32; ++i2) s[i2] = __uint_as_float(r[i2]);
                 }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(s_empty(sb));
                 if constexpr (CL == 2) {
                     // + the partner's partial logits of the same rows and columns
                     if (!wait_all<true>(x_full(sb, quarter), ph)) {
@@ -1090,7 +1120,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                             lB *= alB;
                             mB = mxB;
                         }
-                        if (!wait_all(o_done, uint32_t(a - 1) & 1u)) {   // P.V(a-1) done
+                        if (!pv_done(a - 1)) {
                             ok = false;
                             break;
                         }
@@ -1123,26 +1153,37 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 }
                 lA += sumA;
                 lB += sumB;
-                if constexpr (CL == 2) {
-                    // P of these rows and their rescale factors to the partner
-                    if (a >= 2 && !wait_all(pm_empty(sb, quarter), uint32_t((a >> 1) - 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dst = remote(pm_buf(sb)), fbar = remote(pm_full(sb, quarter));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        ptx::st_async_v4(dst + uint32_t(c * 512 + lane * 16), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
-                                         pw[4 * c + 3], fbar);
-                    if (qu < 2)
-                        ptx::st_async_b32(dst + uint32_t(C::PM_P + (qu * 8 + g8) * 4),
-                                          __float_as_uint(qu == 0 ? alA : alB), fbar);
+                // P of these rows into P buffer sb (free once the P.V of tile
+                // a-2 is done in both CTAs of the pair), and with a partner
+                // the same rows into its buffer sb, with their rescale factors
+                if (a >= 2 && !wait_all(p_empty(sb), uint32_t((a >> 1) - 1) & 1u)) {
+                    ok = false;
+                    break;
                 }
-                ptx::tmem_st_16x128b_x8(half_addr + C::S_COL + sb * kBN, pw);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
+                {
+                    uint8_t *ra = p_rows(sb) + g8 * 128 + qu * 4;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int c = (k ^ g8) * 16;
+                        *reinterpret_cast<uint32_t *>(ra + c) = pw[2 * k];
+                        *reinterpret_cast<uint32_t *>(ra + 1024 + c) = pw[2 * k + 1];
+                    }
+                }
+                if constexpr (CL == 2) {
+                    if (qu < 2)
+                        ptx::st_async_b32(remote(f_buf(sb)) + uint32_t((qu * 8 + g8) * 4),
+                                          __float_as_uint(qu == 0 ? alA : alB), remote(pm_full(sb, quarter)));
+                }
+                ptx::fence_proxy_async_smem();   // P stores -> MMA and bulk-copy reads
+                ptx::tc_fence_before();          // (rescaled O rows -> the next P.V)
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(p_full(sb));
+                if (lane == 0) {
+                    if constexpr (CL == 2) {
+                        const uint32_t src = ptx::smem_u32(p_rows(sb));
+                        ptx::bulk_copy_to_cluster(remote(src), src, 2048, remote(pm_full(sb, quarter)));
+                    }
+                    ptx::mbar_arrive(p_full(sb));
+                }
             }
             // row statistics (m, l) of these rows, here and at the partner
             lA += __shfl_xor_sync(0xffffffffu, lA, 1);
@@ -1171,6 +1212,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                 uint32_t r[32];
                 ptx::tmem_ld_16x256b_x8(half_addr + C::S_COL + jb * kBN, r);
                 ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(s_empty(jb));
                 if (j2 >= 2 && !wait_all(x_empty(jb, quarter), uint32_t((j2 >> 1) - 1) & 1u)) return false;
                 const uint32_t dst = remote(x_buf(jb)) + uint32_t(lane * 16), fbar = remote(x_full(jb, quarter));
 #pragma unroll
@@ -1185,37 +1229,25 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
                     ok = false;
                     break;
                 }
+                // the partner's P rows of tile a (into P buffer a & 1) and
+                // their rescale factors, applied to this CTA's half of O
                 const int sb = a & 1;
-                if (lane == 0) ptx::mbar_arrive_expect_tx(pm_full(sb, quarter), C::PMQ);
+                if (lane == 0) ptx::mbar_arrive_expect_tx(pm_full(sb, quarter), 2048 + C::FQ);
                 if (!wait_all<true>(pm_full(sb, quarter), uint32_t(a >> 1) & 1u)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *pm = smem + C::OFF_PM + (sb * 4 + quarter) * C::PMQ;
-                uint32_t pw[16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(pm + c * 512 + lane * 16);
-                    pw[4 * c] = v.x;
-                    pw[4 * c + 1] = v.y;
-                    pw[4 * c + 2] = v.z;
-                    pw[4 * c + 3] = v.w;
-                }
-                const float alA = reinterpret_cast<const float *>(pm + C::PM_P)[g8];
-                const float alB = reinterpret_cast<const float *>(pm + C::PM_P)[8 + g8];
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_remote_relaxed(remote(pm_empty(sb, quarter)));
+                const float *fa = reinterpret_cast<const float *>(smem + C::OFF_F + (sb * 4 + quarter) * C::FQ);
+                const float alA = fa[g8], alB = fa[8 + g8];
                 if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
-                    if (!wait_all(o_done, uint32_t(a - 1) & 1u)) {   // P.V(a-1) done
+                    if (!pv_done(a - 1)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     rescale_rows(alA, alB);
+                    ptx::tc_fence_before();
                 }
-                ptx::tmem_st_16x128b_x8(half_addr + C::S_COL + sb * kBN, pw);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(p_full(sb));
             }

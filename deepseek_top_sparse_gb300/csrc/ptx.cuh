@@ -154,6 +154,18 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's (dst from mapa); on arrival it
+// performs complete_tx(bytes) on `remote_bar` (an mbarrier in the
+// destination CTA).  The source must not be rewritten until the copy has
+// landed.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+
 // ------------------------------------------------------------- cp.async (LSU)
 
 // 16-byte global -> shared copy; src_bytes = 0 zero-fills the destination
@@ -269,6 +281,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// As mma_commit, but the arrival goes to the mbarrier at the same shared
+// memory offset in every CTA of the cluster whose bit is set in cta_mask.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(cta_mask)
                  : "memory");
 }
 
