@@ -144,7 +144,7 @@ struct Cfg {
     // stg_empty[NF].  The layout is the same in every CTA (p_empty receives
     // multicast arrivals at its offset).
     static constexpr int BAR_X = 2 * NS + 15;
-    static constexpr int NUM_BARS = BAR_X + 24 + 2 * NF;
+    static constexpr int NUM_BARS = BAR_X + 24 + 2 * NF + 1;   // + rcv_bar
     // Q_c arrives by TMA in the last two kv stages (128 rows x DC bf16 =
     // 2 stages), as DC / 64 boxes of [128 rows][128 B], 128B-swizzled
     static constexpr int OFF_QS = OFF_KV + (NS - 2) * STAGE_BYTES;
@@ -160,10 +160,6 @@ struct Cfg {
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    // output staging (epilogue): kM rows of up to DC fp32, padded by 16 bytes,
-    // over the kv ring, P and partner buffers and index lists (all dead by then)
-    static constexpr int STAGE_ROW = DC * 4 + 16;
-    static_assert(kM * STAGE_ROW <= OFF_STAT - OFF_KV, "output staging stays below the row statistics");
 };
 
 struct TcParams {
@@ -245,155 +241,6 @@ __device__ __forceinline__ void combine_range(const TcParams &p, int split, int 
     cr1 = cr0 + rp < p.H ? cr0 + rp : int(p.H);
 }
 
-// Staged output rows to global memory, by all C::THREADS threads: thread t
-// copies 16-byte chunk t % CHK of rows t / CHK, t / CHK + THREADS / CHK, ...
-// (each warp instruction covers 512 contiguous bytes), 8 shared-memory loads
-// in flight before their stores.  Non-split: bf16 rows of o.  Split: fp32
-// partial rows of the workspace, except (fused) the rows this split combines
-// itself.  (One TMA bulk store per row measured slower: ~60 cycles per bulk
-// operation.)
-template <int DC, typename C>
-__device__ __forceinline__ void copy_out_rows(const TcParams &p, const uint8_t *smem, int64_t tok, int64_t iotok,
-                                              int split, uint32_t crank, int tid) {
-    const bool split_out = p.num_splits > 1;
-    int cr0 = 0, cr1 = 0;
-    if (p.fused) combine_range(p, split, cr0, cr1);
-    const int chk = split_out ? DC * 4 / 16 : DC * 2 / 16;         // 16-byte chunks per row
-    const int rows_per_pass = C::THREADS / chk;
-    const int c = tid % chk;
-    const int r0 = tid / chk;
-    const int64_t row_bytes = split_out ? p.D * 4 : p.D * 2;
-    char *dst = split_out
-        ? reinterpret_cast<char *>(p.ws_o + ((tok * p.num_splits + split) * p.H) * p.D + int64_t(crank) * DC)
-        : reinterpret_cast<char *>(p.o + (iotok * p.H) * p.D + int64_t(crank) * DC);
-    dst += c * 16;
-    const uint8_t *src = smem + C::OFF_KV + c * 16;
-    constexpr int kBatch = 8;
-    for (int rb = r0; rb < kM; rb += kBatch * rows_per_pass) {
-        uint4 v[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int r = rb + u * rows_per_pass;
-            if (r < p.H && (r < cr0 || r >= cr1)) v[u] = *reinterpret_cast<const uint4 *>(src + r * C::STAGE_ROW);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int r = rb + u * rows_per_pass;
-            if (r < p.H && (r < cr0 || r >= cr1)) *reinterpret_cast<uint4 *>(dst + r * row_bytes) = v[u];
-        }
-    }
-}
-
-// In-cluster split combine for one CTA (see the kernel's teardown), run by
-// all C::THREADS threads, over rows [cr0, cr1) of this CTA's DC columns.
-// Thread t owns float4 column chunk t % CH of rows cr0 + t / CH + k * RP
-// (RP = THREADS / CH rows per pass), so one base pointer per split serves
-// all its loads.
-//   1. each thread loads its partial chunks from the first other split and,
-//      for the weights, its row's sink (the lse table was filled through
-//      distributed shared memory before the cluster barrier);
-//   2. per row the final weights w_i / den (the combine kernel's formula);
-//   3. weighted sums: the first other split's chunks (loaded in step 1) and
-//      this split's own partial from shared memory first, then any further
-//      splits from L2.  A split combines at most 64 rows (two or more
-//      splits), which is at most kB passes, so one batch covers them.
-template <int DC, typename C>
-__device__ __forceinline__ void combine_rows(const TcParams &p, uint8_t *smem, int64_t tok, int64_t iotok,
-                                             int split,
-                                             uint32_t crank, int tid) {
-    const int ns = p.num_splits;
-    int cr0, cr1;
-    combine_range(p, split, cr0, cr1);
-    const int nrows = cr1 > cr0 ? cr1 - cr0 : 0;
-    float *tab = reinterpret_cast<float *>(smem + C::OFF_LSE);   // [split][row]
-    constexpr int CH = DC / 4;                 // float4 chunks per row
-    constexpr int RP = C::THREADS / CH;        // rows per pass
-    constexpr int kB = 8;                      // passes: covers 64 rows for every DC
-    static_assert(kB * RP >= kM / 2, "one batch covers a split's rows");
-    static_assert(C::THREADS % CH == 0 && kM <= C::THREADS, "thread -> (row, chunk) map");
-    const int c = tid % CH;
-    const int rt = cr0 + tid / CH;             // this thread's first row
-    const int first_other = split == 0 ? 1 : 0;
-    auto part = [&](int i) {                   // split i's chunk c of row rt
-        return reinterpret_cast<const float4 *>(p.ws_o + ((tok * ns + i) * p.H + rt) * p.D + int64_t(crank) * DC) + c;
-    };
-    const int64_t pass_f4 = int64_t(RP) * p.D / 4;   // float4 stride between passes
-    float4 pre[kB];
-    {
-        const float4 *src = part(first_other);
-#pragma unroll
-        for (int u = 0; u < kB; ++u)
-            if (rt + u * RP < cr1) pre[u] = __ldcg(src + u * pass_f4);
-    }
-    const float sink_r = tid < nrows ? reinterpret_cast<const float *>(smem + C::OFF_SINK)[cr0 + tid] : 0.f;
-    // (pre holds passes 0..kB-1 of the first other split)
-    if (tid < nrows) {
-        const int r = cr0 + tid;
-        float mx = -INFINITY;
-        for (int i = 0; i < ns; ++i) mx = fmaxf(mx, tab[i * kM + r]);
-        const float s2 = sink_r * kLog2e;
-        const float M = fmaxf(mx, s2);
-        const bool zero = (s2 == INFINITY) || (M == -INFINITY);
-        float den = 0.f;
-        if (!zero) {
-            for (int i = 0; i < ns; ++i) {
-                const float li = tab[i * kM + r];
-                if (li != -INFINITY) den += exp2f(li - M);
-            }
-            den += exp2f(s2 - M);
-        }
-        const float f = zero ? 0.f : 1.f / den;
-        const float fn = isnan(s2) ? NAN : f;
-        for (int i = 0; i < ns; ++i) {
-            const float li = tab[i * kM + r];
-            tab[i * kM + r] = (zero || li == -INFINITY) ? 0.f * fn : exp2f(li - M) * fn;
-        }
-    }
-    __syncthreads();
-    const uint8_t *own = smem + C::OFF_KV + rt * C::STAGE_ROW + c * 16;
-    float4 acc[kB];
-#pragma unroll
-    for (int u = 0; u < kB; ++u) {
-        const int r = rt + u * RP;
-        if (r < cr1) {
-            const float wo = tab[first_other * kM + r], ws = tab[split * kM + r];
-            const float4 o4 = *reinterpret_cast<const float4 *>(own + u * RP * C::STAGE_ROW);
-            acc[u] = make_float4(fmaf(wo, pre[u].x, ws * o4.x), fmaf(wo, pre[u].y, ws * o4.y),
-                                 fmaf(wo, pre[u].z, ws * o4.z), fmaf(wo, pre[u].w, ws * o4.w));
-        }
-    }
-    for (int i = 0; i < ns; ++i) {
-        if (i == split || i == first_other) continue;
-        const float4 *src = part(i);
-        float4 v[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u)
-            if (rt + u * RP < cr1) v[u] = __ldcg(src + u * pass_f4);
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int r = rt + u * RP;
-            if (r < cr1) {
-                const float w = tab[i * kM + r];
-                acc[u].x = fmaf(w, v[u].x, acc[u].x);
-                acc[u].y = fmaf(w, v[u].y, acc[u].y);
-                acc[u].z = fmaf(w, v[u].z, acc[u].z);
-                acc[u].w = fmaf(w, v[u].w, acc[u].w);
-            }
-        }
-    }
-    uint2 *dst = reinterpret_cast<uint2 *>(p.o + (iotok * p.H + rt) * p.D + int64_t(crank) * DC) + c;
-    const int64_t pass_u2 = int64_t(RP) * p.D / 4;
-#pragma unroll
-    for (int u = 0; u < kB; ++u) {
-        if (rt + u * RP < cr1) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-            dst[u * pass_u2] =
-                make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
-        }
-    }
-}
-
 // E8M0 scale byte -> 2^(byte - 127) as a float (255 -> NaN; 0 -> 2^-127, a
 // subnormal float).
 __device__ __forceinline__ float e8m0_scale(uint32_t b) {
@@ -449,7 +296,8 @@ __device__ __forceinline__ uint32_t e4m3x4_has_nan(uint32_t c) {
 // explicitly, so the usual one carries no code for it.
 template <int DC, int CL, bool kPosScale, bool kFp8>
 __global__ void __launch_bounds__(Cfg<DC, CL, kFp8>::THREADS, 1)
-attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
+attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+               const __grid_constant__ CUtensorMap wmap) {
     using C = Cfg<DC, CL, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -495,6 +343,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
     auto pm_full = [&](int b2, int q) { return bar(C::BAR_X + 16 + b2 * 4 + q); };  // partner's P rows + factors landed
     auto stg_full = [&](int f) { return bar(C::BAR_X + 24 + f); };            // FP8: staging f landed
     auto stg_empty = [&](int f) { return bar(C::BAR_X + 24 + C::NF + f); };   // FP8: staging f widened
+    const uint32_t rcv_bar = bar(C::BAR_X + 24 + 2 * C::NF);   // in-cluster combine: partials landed
 
     // ---------------------------------------------------------------- prologue
     // The index list heads the longest dependency chain (index -> kv row ->
@@ -566,6 +415,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             ptx::mbar_init(stg_full(f), 32 * kF8CopyWarps);
             ptx::mbar_init(stg_empty(f), kF8WidenWarps);
         }
+        ptx::mbar_init(rcv_bar, 1);   // thread 0's expect_tx + the bytes of every box
         ptx::fence_mbar_init();
         // Q_c of this unit: DC / 64 boxes of 128 head rows x 64 columns
         ptx::mbar_arrive_expect_tx(q_smem, C::Q_BYTES);
@@ -1253,95 +1103,251 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
             }
         }
         // ------------------------------------------------------------ epilogue
-        // thread = (head row h, column half) again: columns [half*DC/2,
-        // (half+1)*DC/2) of row h of O, with the row's (m, l) from the table
+        // every row's (m, l) is in the table once all MMAs have completed;
+        // with splits, thread (row h, half 0) publishes the row's
+        // log-sum-exp m + log2(l) (base 2; -inf for an empty split): to every
+        // split CTA of the token with the same head-dim half (fused), or to
+        // the workspace for the combine kernel
         if (ok) ok = wait_all(mma_done, 0);
         if (ok) ok = wait_all<CL == 2>(stat_bar, 0);
-        float m_run = -INFINITY, l_tot = 0.f;
-        if (ok) {
+        if (ok && p.num_splits > 1 && hv && half == 0) {
             const float2 st = stat[h];
-            m_run = st.x;
-            l_tot = st.y;
-        }
-        ptx::tc_fence_after();
-        if (ok) {
-            // Output rows are staged in shared memory (the kv ring, receive
-            // buffers and index lists are dead once every MMA has completed)
-            // and then written out row by row.  Staged rows are linear with a
-            // 16-byte pad (stride STAGE_ROW), so the 16-byte writes of 32
-            // consecutive rows spread over all banks.
-            const bool split_out = p.num_splits > 1;
-            float f = 0.f, lse = -INFINITY;
-            if (!split_out) {
-                const float s2 = hv ? sink_tab[h] * kLog2e : 0.f;
-                if (n_act > 0 && s2 != INFINITY) {
-                    const float M = fmaxf(m_run, s2);
-                    const float e = exp2f(m_run - M);
-                    f = e / (l_tot * e + exp2f(s2 - M));
-                }
-                if (isnan(s2)) f = NAN;
-            } else if (n_act > 0) {
-                // split partial: O / l (fp32) and lse = m + log2(l) (base 2)
-                f = 1.f / l_tot;
-                lse = m_run + log2f(l_tot);
-            }
-            uint8_t *stage = smem + C::OFF_KV;
-            uint8_t *srow = stage + h * C::STAGE_ROW;
-            auto stage_chunk = [&](const uint32_t (&r)[32], int ch) {
-                if (split_out) {
-                    float4 *d = reinterpret_cast<float4 *>(srow + (half * (DC / 2) + ch * 32) * 4);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        d[v] = make_float4(__uint_as_float(r[4 * v]) * f, __uint_as_float(r[4 * v + 1]) * f,
-                                           __uint_as_float(r[4 * v + 2]) * f, __uint_as_float(r[4 * v + 3]) * f);
-                } else {
-                    uint4 *d = reinterpret_cast<uint4 *>(srow + (half * (DC / 2) + ch * 32) * 2);
-                    float dummy = 0.f;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(r[8 * v + 0]) * f, __uint_as_float(r[8 * v + 1]) * f, dummy);
-                        w.y = pack_bf16(__uint_as_float(r[8 * v + 2]) * f, __uint_as_float(r[8 * v + 3]) * f, dummy);
-                        w.z = pack_bf16(__uint_as_float(r[8 * v + 4]) * f, __uint_as_float(r[8 * v + 5]) * f, dummy);
-                        w.w = pack_bf16(__uint_as_float(r[8 * v + 6]) * f, __uint_as_float(r[8 * v + 7]) * f, dummy);
-                        d[v] = w;
-                    }
-                }
-            };
-            // two 32-column TMEM loads share one wait
-#pragma unroll
-            for (int ch = 0; ch < DC / 64; ch += 2) {
-                constexpr int NCH = DC / 64;
-                uint32_t r0[32], r1[32];
-                if (n_act > 0) {
-                    ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + ch * 32, r0);
-                    if (ch + 1 < NCH) ptx::tmem_ld32(lane_addr + C::O_COL + half * (DC / 2) + (ch + 1) * 32, r1);
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
-                }
-                stage_chunk(r0, ch);
-                if (ch + 1 < NCH) stage_chunk(r1, ch + 1);
-            }
-            if (split_out && hv && half == 0) {
-                if (p.fused) {
-                    // this split's lse of row h into the lse table of every
-                    // split CTA with the same head-dim half (cluster rank
-                    // s * CL + crank); the teardown's cluster barrier orders it
-                    const uint32_t slot =
-                        ptx::smem_u32(smem + C::OFF_LSE + ((split % 8) * kM + h) * 4);
-                    for (int s2 = 0; s2 < p.num_splits; ++s2)
-                        ptx::st_cluster_b32(ptx::map_to_rank(slot, uint32_t(s2 * CL) + crank), __float_as_uint(lse));
-                } else if (crank == 0) {
-                    p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
-                }
+            const float lse = n_act > 0 ? st.x + log2f(st.y) : -INFINITY;
+            if (p.fused) {
+                const uint32_t slot = ptx::smem_u32(smem + C::OFF_LSE + ((split % 8) * kM + h) * 4);
+                for (int s2 = 0; s2 < p.num_splits; ++s2)
+                    ptx::st_cluster_b32(ptx::map_to_rank(slot, uint32_t(s2 * CL) + crank), __float_as_uint(lse));
+            } else if (crank == 0) {
+                p.ws_lse[(tok * p.num_splits + split) * p.H + h] = lse;
             }
         }
+        if (!ok) stat[h] = make_float2(NAN, NAN);   // a failed unit writes NaN, never stale data
         ptx::setmaxnreg_dec<kLaunchRegs>();
     }
 
     // ---------------------------------------------------------------- teardown
+    // Output from TMEM by all 16 warps: warp w reads the rows of lane quarter
+    // w % 4 (thread = row hr) and column slice w / 4 (DC / 4 columns, in
+    // chunks of CC), scales them and writes them into 128B-swizzled staging
+    // boxes in the dead kv ring; TMA then stores whole boxes (the H rows of
+    // the token by 128 bytes of columns).
+    //   one split: o = O * f, f = 2^(m-M) / (l 2^(m-M) + 2^(sink*log2e - M)),
+    //     M = max(m, sink*log2e) (§5.5: the sink joins the denominator once,
+    //     at the end), bf16;
+    //   splits, separate combine: the partial O / l (fp32) to the workspace;
+    //   splits combined in the cluster: once every split's log-sum-exp is in
+    //     the table, split s scales its O by its final weight w_s / l_s (the
+    //     combine kernel's formula), stores the 64-column granules other splits
+    //     finish to the workspace and, after a cluster barrier, finishes its
+    //     own granules: its weighted O plus the other splits' from L2.
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (p.fused) ptx::cluster_sync();   // every split's log-sum-exp is in the table
+    ptx::tc_fence_after();
+    {
+        constexpr int CW = DC / 4;                        // columns of a warp's slice
+        constexpr int CC = CW < 32 ? CW : 32;             // columns per TMEM load
+        constexpr int NG = DC / 64;                       // 64-column granules of this CTA
+        constexpr int BOX = kM * 128;                     // one staging box: 128 rows x 128 B
+        const int q4 = warp & 3, cs = warp >> 2;
+        const int hr = q4 * 32 + lane;                    // this thread's row
+        const bool rv = hr < p.H;
+        const int c_slice = cs * CW;                      // first column of the slice
+        const int gran = c_slice / 64;                    // its granule (warp-uniform)
+        const uint32_t taddr = tbase + (uint32_t(q4 * 32) << 16) + C::O_COL + c_slice;
+        const float2 st = stat[hr];
+        const float sink2 = sink_tab[hr] * kLog2e;
+        const int ns = p.num_splits;
+        const int32_t y_o = int32_t(iotok * p.H);                         // o rows of the token
+        const int32_t y_ws = int32_t((tok * ns + split) * p.H);           // workspace rows of this split
+        // chunk cc of the slice (fp32; 0 when the unit had no live tile); all
+        // 32 lanes load (tcgen05.ld is warp-collective)
+        auto load_chunk = [&](int cc, float (&x)[CC]) {
+            if (n_act > 0) {
+                uint32_t r[CC];
+                if constexpr (CC == 32) ptx::tmem_ld32(taddr + cc * CC, r);
+                else ptx::tmem_ld16(taddr + cc * CC, r);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i2 = 0; i2 < CC; ++i2) x[i2] = __uint_as_float(r[i2]);
+            } else {
+#pragma unroll
+                for (int i2 = 0; i2 < CC; ++i2) x[i2] = 0.f;
+            }
+        };
+        // staging box `box` at `base`: row r's 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4)
+        auto box_addr = [&](int base, int box, int chunk) {
+            return smem + base + box * BOX + hr * 128 + (((chunk ^ hr) & 7) << 4);
+        };
+        // columns [c0, c0 + CC) of row hr as fp32 (box = column / 32) or bf16 (box = column / 64)
+        auto stage_f32 = [&](int base, int c0, const float (&x)[CC], float f) {
+#pragma unroll
+            for (int v2 = 0; v2 < CC / 4; ++v2) {
+                const int c = c0 + 4 * v2;
+                *reinterpret_cast<float4 *>(box_addr(base, c / 32, (c % 32) / 4)) =
+                    make_float4(x[4 * v2] * f, x[4 * v2 + 1] * f, x[4 * v2 + 2] * f, x[4 * v2 + 3] * f);
+            }
+        };
+        auto stage_bf16 = [&](int base, int c0, const float (&x)[CC], float f) {
+            float dummy = 0.f;
+#pragma unroll
+            for (int v2 = 0; v2 < CC / 8; ++v2) {
+                const int c = c0 + 8 * v2;
+                uint4 w;
+                w.x = pack_bf16(x[8 * v2] * f, x[8 * v2 + 1] * f, dummy);
+                w.y = pack_bf16(x[8 * v2 + 2] * f, x[8 * v2 + 3] * f, dummy);
+                w.z = pack_bf16(x[8 * v2 + 4] * f, x[8 * v2 + 5] * f, dummy);
+                w.w = pack_bf16(x[8 * v2 + 6] * f, x[8 * v2 + 7] * f, dummy);
+                *reinterpret_cast<uint4 *>(box_addr(base, c / 64, (c % 64) / 8)) = w;
+            }
+        };
+        auto publish = [&] {   // generic stores -> TMA reads, all staging written
+            ptx::fence_proxy_async_smem();
+            __syncthreads();
+        };
+        const uint32_t sbase = ptx::smem_u32(smem);
+        if (ns == 1) {
+            float f = 0.f;
+            if (n_act > 0 && sink2 != INFINITY) {
+                const float M = fmaxf(st.x, sink2);
+                const float e = exp2f(st.x - M);
+                f = e / (st.y * e + exp2f(sink2 - M));
+            }
+            if (isnan(sink2) || isnan(st.x)) f = NAN;
+#pragma unroll 1
+            for (int cc = 0; cc < CW / CC; ++cc) {
+                float x[CC];
+                load_chunk(cc, x);
+                if (rv) stage_bf16(0, c_slice + cc * CC, x, f);
+            }
+            publish();
+            if (tid == 0) {
+                for (int j = 0; j < NG; ++j) ptx::tma_store_2d(&omap, sbase + j * BOX, int32_t(crank) * DC + 64 * j, y_o);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+        } else if (!p.fused) {
+            const float f = n_act > 0 ? 1.f / st.y : 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < CW / CC; ++cc) {
+                float x[CC];
+                load_chunk(cc, x);
+                if (rv) stage_f32(0, c_slice + cc * CC, x, f);
+            }
+            publish();
+            if (tid == 0) {
+                for (int k = 0; k < 2 * NG; ++k) ptx::tma_store_2d(&wmap, sbase + k * BOX, int32_t(crank) * DC + 32 * k, y_ws);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+        } else {
+            // final weight of every split for row hr (the combine kernel's formula)
+            const float *tab = reinterpret_cast<const float *>(smem + C::OFF_LSE);   // [split][row]
+            float mx = -INFINITY;
+            for (int i2 = 0; i2 < ns; ++i2) mx = fmaxf(mx, tab[i2 * kM + hr]);
+            const float M = fmaxf(mx, sink2);
+            const bool zero = (sink2 == INFINITY) || (M == -INFINITY);
+            float den = 0.f;
+            if (!zero) {
+                for (int i2 = 0; i2 < ns; ++i2) {
+                    const float li = tab[i2 * kM + hr];
+                    if (li != -INFINITY) den += exp2f(li - M);
+                }
+                den += exp2f(sink2 - M);
+            }
+            const float fn = isnan(sink2) ? NAN : 1.f;
+            const float lo = tab[split * kM + hr];
+            // this split's O, weighted: w_s / l_s (0 for an empty split)
+            const float g = (zero || lo == -INFINITY) ? 0.f * fn : exp2f(lo - M) / den / st.y * fn;
+            const int gs0 = split * NG / ns, gs1 = (split + 1) * NG / ns;   // this split's granules
+            const bool mine = gran >= gs0 && gran < gs1;
+            if (!mine) {
+#pragma unroll 1
+                for (int cc = 0; cc < CW / CC; ++cc) {
+                    float x[CC];
+                    load_chunk(cc, x);
+                    if (rv) stage_f32(0, c_slice + cc * CC, x, g);
+                }
+            }
+            publish();
+            if (tid == 0) {
+                for (int k = 0; k < 2 * NG; ++k)
+                    if (k / 2 < gs0 || k / 2 >= gs1)
+                        ptx::tma_store_2d(&wmap, sbase + k * BOX, int32_t(crank) * DC + 32 * k, y_ws);
+                ptx::bulk_commit();
+                ptx::bulk_wait_all();              // written, not just read
+                ptx::fence_proxy_async_global();   // async-proxy writes before the barrier's release
+            }
+            ptx::cluster_sync();   // every split's weighted granules are in the workspace
+            // the other splits' weighted partials of this split's granules, a
+            // round of as many splits as the receive area holds at a time,
+            // added to this split's own
+            const int nsub = 2 * (gs1 - gs0);                                // 32-column boxes per split
+            const int hbase = (C::OFF_STAT - NG * BOX) / 1024 * 1024;          // bf16 staging, above the receive area
+            const int per_round = nsub > 0 ? hbase / (nsub * BOX) : 1;
+            float acc[CW];
+            if (mine) {
+#pragma unroll
+                for (int cc = 0; cc < CW / CC; ++cc) {
+                    float x[CC];
+                    load_chunk(cc, x);
+#pragma unroll
+                    for (int i2 = 0; i2 < CC; ++i2) acc[cc * CC + i2] = x[i2] * g;
+                }
+            }
+            bool rok = true;
+            int done = 0, round = 0;
+            while (nsub > 0 && done < ns - 1) {
+                const int cnt = ns - 1 - done < per_round ? ns - 1 - done : per_round;
+                if (tid == 0) {
+                    ptx::fence_proxy_async_global();   // the barrier's acquire before these async-proxy reads
+                    ptx::mbar_arrive_expect_tx(rcv_bar, uint32_t(cnt * nsub) * uint32_t(p.H) * 128u);
+                    for (int t2 = 0; t2 < cnt; ++t2) {
+                        const int oth = done + t2 < split ? done + t2 : done + t2 + 1;   // t2-th other split
+                        for (int k = 0; k < nsub; ++k)
+                            ptx::tma_load_2d(sbase + (t2 * nsub + k) * BOX, &wmap, int32_t(crank) * DC + 64 * gs0 + 32 * k,
+                                             int32_t((tok * ns + oth) * p.H), rcv_bar);
+                    }
+                }
+                rok = rok && wait_all(rcv_bar, uint32_t(round) & 1u);
+                if (mine && rok) {
+                    for (int t2 = 0; t2 < cnt; ++t2) {
+#pragma unroll
+                        for (int v2 = 0; v2 < CW / 4; ++v2) {
+                            const int c = c_slice + 4 * v2;                     // column of this CTA
+                            const int k = (c - 64 * gs0) / 32;                  // box among this split's
+                            const float4 w4 = *reinterpret_cast<const float4 *>(
+                                smem + (t2 * nsub + k) * BOX + hr * 128 + (((((c % 32) / 4) ^ hr) & 7) << 4));
+                            acc[4 * v2] += w4.x;
+                            acc[4 * v2 + 1] += w4.y;
+                            acc[4 * v2 + 2] += w4.z;
+                            acc[4 * v2 + 3] += w4.w;
+                        }
+                    }
+                }
+                __syncthreads();   // the receive area is read before it is refilled
+                done += cnt;
+                ++round;
+            }
+            // the finished granules as bf16, staged above the receive area
+            if (mine && rv) {
+#pragma unroll
+                for (int cc = 0; cc < CW / CC; ++cc) {
+                    float x[CC];
+#pragma unroll
+                    for (int i2 = 0; i2 < CC; ++i2) x[i2] = rok ? acc[cc * CC + i2] : NAN;
+                    stage_bf16(hbase, c_slice + cc * CC, x, 1.f);
+                }
+            }
+            publish();
+            if (tid == 0) {
+                for (int j = gs0; j < gs1; ++j)
+                    ptx::tma_store_2d(&omap, sbase + hbase + j * BOX, int32_t(crank) * DC + 64 * j, y_o);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -1350,18 +1356,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, C::TMEM_COLS);
     }
-    // the staged rows leave (all warps); a fused split keeps its own combine rows
-    copy_out_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
-    if (p.fused) {
-        // Every split of this token has published its partial rows and
-        // log-sum-exp (release/acquire at cluster scope); all partner
-        // exchanges are over too.  Split s now combines rows [s*rp, s*rp+rp)
-        // of this CTA's DC columns: its own partial from shared memory, the
-        // others' from L2, in the log-sum-exp form with the sink added once.
-        ptx::cluster_sync();
-        combine_rows<DC, C>(p, smem, tok, iotok, split, crank, tid);
-    } else if constexpr (CL == 2) {
-        ptx::cluster_sync();  // no remote access outlives the partner
+    if constexpr (CL == 2) {
+        if (!p.fused) ptx::cluster_sync();  // no remote access outlives the partner
     }
 }
 
@@ -1474,6 +1470,37 @@ cudaError_t encode_q_map(CUtensorMap *m, const AttnArgs &a) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The kernel's output boxes: the H rows of one token by 128 bytes of
+// columns, 128B-swizzled.  o: bf16 [B * io_S * H rows][D] (64 columns a box);
+// the split workspace: fp32 [tokens * splits * H rows][D] (32 columns a box).
+cudaError_t encode_out_maps(CUtensorMap *omap, CUtensorMap *wmap, const AttnArgs &a) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const int64_t io_S = a.io_S > 0 ? a.io_S : a.S;
+    cuuint32_t estr[2] = {1, 1};
+    {
+        cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.B * io_S * a.H)};
+        cuuint64_t strides[1] = {cuuint64_t(a.D) * 2};
+        cuuint32_t box[2] = {64, cuuint32_t(a.H)};
+        const CUresult r = enc(omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.o, dims, strides, box, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    if (a.num_splits > 1) {
+        cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.B * a.S * a.num_splits * a.H)};
+        cuuint64_t strides[1] = {cuuint64_t(a.D) * 4};
+        cuuint32_t box[2] = {32, cuuint32_t(a.H)};
+        const CUresult r = enc(wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.ws_o, dims, strides, box, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    } else {
+        *wmap = CUtensorMap{};   // unused without splits
+    }
+    return cudaSuccess;
+}
+
 // Opt the kernel into its dynamic shared memory once per device.
 template <int DC, int CL, bool F8>
 cudaError_t prepare_kernel(int dev) {
@@ -1582,8 +1609,11 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     CUtensorMap qmap;
     e = encode_q_map(&qmap, a);
     if (e != cudaSuccess) return e;
-    return a.scale > 0.f ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, true, F8>, p, qmap)
-                         : cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, false, F8>, p, qmap);
+    CUtensorMap omap, wmap;
+    e = encode_out_maps(&omap, &wmap, a);
+    if (e != cudaSuccess) return e;
+    return a.scale > 0.f ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, true, F8>, p, qmap, omap, wmap)
+                         : cudaLaunchKernelEx(&cfg, attn_tc_kernel<DC, CL, false, F8>, p, qmap, omap, wmap);
 }
 
 }  // namespace
