@@ -67,6 +67,12 @@ def _load():
                 [p, p, p, p, p, ctypes.c_double] + [i64] * 6 + [p, i64, p, ctypes.c_int])
             lib.oracle_sparse_attn_fp8_tokens.argtypes = (
                 [p, p, p, p, p, ctypes.c_double] + [i64] * 5 + [p, i64, p, ctypes.c_int])
+            lib.oracle_sparse_attn_extra_tokens.argtypes = (
+                [p, p, p, p, p, p, p, p, ctypes.c_double] + [i64] * 8 + [p, i64, p, ctypes.c_int])
+            lib.oracle_sparse_attn_extra_tokens.restype = ctypes.c_int
+            lib.oracle_sparse_attn_fp8_extra_tokens.argtypes = (
+                [p, p, p, p, p, p, p, p, ctypes.c_double] + [i64] * 7 + [p, i64, p, ctypes.c_int])
+            lib.oracle_sparse_attn_fp8_extra_tokens.restype = ctypes.c_int
             lib.oracle_decode_kv_fp8.argtypes = [p, i64, p]
             lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
@@ -107,10 +113,12 @@ def _np(x, dtype):
 
 
 def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0,
-                topk_length=None):
+                topk_length=None, extra_kv=None, extra_idxs=None, extra_length=None):
     """float64 o[B,S,H,D] (or o[len(tokens),H,D] for flat token ids b*S+s).
     topk_length: optional int32 [B,S]; slot j of token (b,s) counts only if
-    j < clamp(topk_length[b,s], 0, K)."""
+    j < clamp(topk_length[b,s], 0, K).  extra_kv [B,T2,D] bf16 with
+    extra_idxs int32 [B,S,K2] (and optional extra_length [B,S]): a second kv
+    source whose slots join each token's softmax after its K main slots."""
     qb, kvb = _bf16_bits(q), _bf16_bits(kv)
     sink = _np(attn_sink, np.float32)
     idx = _np(topk_idxs, np.int32)
@@ -123,9 +131,20 @@ def sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale: float, tokens=None, 
         lens = _np(topk_length, np.int32).reshape(B, S)
     tok = np.arange(B * S, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
     o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
-    rc = _load().oracle_sparse_attn_tokens_len(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), _ptr(lens),
-                                              float(softmax_scale), B, S, H, D, T, K, _ptr(tok), tok.shape[0],
-                                              _ptr(o), int(nthreads))
+    if extra_kv is None:
+        rc = _load().oracle_sparse_attn_tokens_len(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                                  float(softmax_scale), B, S, H, D, T, K, _ptr(tok), tok.shape[0],
+                                                  _ptr(o), int(nthreads))
+    else:
+        kv2 = _bf16_bits(extra_kv)
+        idx2 = _np(extra_idxs, np.int32)
+        T2, K2 = kv2.shape[1], idx2.shape[-1]
+        assert kv2.shape == (B, T2, D) and idx2.shape == (B, S, K2)
+        lens2 = None if extra_length is None else _np(extra_length, np.int32).reshape(B, S)
+        rc = _load().oracle_sparse_attn_extra_tokens(_ptr(qb), _ptr(kvb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                                    _ptr(kv2), _ptr(idx2), _ptr(lens2), float(softmax_scale), B, S,
+                                                    H, D, T, K, T2, K2, _ptr(tok), tok.shape[0], _ptr(o),
+                                                    int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn rejected its arguments (rc={rc})")
     return o.reshape(B, S, H, D) if tokens is None else o
@@ -165,8 +184,10 @@ def decode_kv_fp8(kv8) -> np.ndarray:
 
 
 def sparse_attn_fp8(q, kv8, attn_sink, topk_idxs, softmax_scale: float, tokens=None, nthreads: int = 0,
-                    topk_length=None):
-    """sparse_attn over an FP8 kv cache uint8 [B,T,584]; q bf16 [B,S,H,512]."""
+                    topk_length=None, extra_kv8=None, extra_idxs=None, extra_length=None):
+    """sparse_attn over an FP8 kv cache uint8 [B,T,584]; q bf16 [B,S,H,512];
+    optionally an extra FP8 source extra_kv8 [B,T2,584] with extra_idxs
+    [B,S,K2] (and extra_length [B,S])."""
     qb, kb = _bf16_bits(q), _u8(kv8)
     sink = _np(attn_sink, np.float32)
     idx = _np(topk_idxs, np.int32)
@@ -177,9 +198,20 @@ def sparse_attn_fp8(q, kv8, attn_sink, topk_idxs, softmax_scale: float, tokens=N
     lens = None if topk_length is None else _np(topk_length, np.int32).reshape(B, S)
     tok = np.arange(B * S, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
     o = np.zeros((tok.shape[0], H, D), dtype=np.float64)
-    rc = _load().oracle_sparse_attn_fp8_tokens(_ptr(qb), _ptr(kb), _ptr(sink), _ptr(idx), _ptr(lens),
-                                               float(softmax_scale), B, S, H, T, K, _ptr(tok), tok.shape[0],
-                                               _ptr(o), int(nthreads))
+    if extra_kv8 is None:
+        rc = _load().oracle_sparse_attn_fp8_tokens(_ptr(qb), _ptr(kb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                                   float(softmax_scale), B, S, H, T, K, _ptr(tok), tok.shape[0],
+                                                   _ptr(o), int(nthreads))
+    else:
+        kb2 = _u8(extra_kv8)
+        idx2 = _np(extra_idxs, np.int32)
+        T2, K2 = kb2.shape[1], idx2.shape[-1]
+        assert kb2.shape == (B, T2, FP8_ROW_BYTES) and idx2.shape == (B, S, K2)
+        lens2 = None if extra_length is None else _np(extra_length, np.int32).reshape(B, S)
+        rc = _load().oracle_sparse_attn_fp8_extra_tokens(_ptr(qb), _ptr(kb), _ptr(sink), _ptr(idx), _ptr(lens),
+                                                        _ptr(kb2), _ptr(idx2), _ptr(lens2), float(softmax_scale), B,
+                                                        S, H, T, K, T2, K2, _ptr(tok), tok.shape[0], _ptr(o),
+                                                        int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn_fp8 rejected its arguments (rc={rc})")
     return o.reshape(B, S, H, D) if tokens is None else o

@@ -30,6 +30,10 @@
  *             tiles of 64 dims, 8 scales per token (7 used), V carries the
  *             RoPE dims too; §5.6: the nope part is stored quantised, the RoPE
  *             part stays bf16, and the kernel dequantises what it gathers.
+ *             The same §5.6 lists the SM100 decode kernel's separate tensor
+ *             maps for an extra kv source (extra_kv_nope / extra_kv_rope)
+ *             beside kv_nope / kv_rope, and §5.13 names an extra_topk_length
+ *             beside topk_length among the scheduler metadata's inputs.
  *
  * Readings taken where the pages are silent (each one is tested):
  *   R1 a slot is valid iff 0 <= idx < T (the pages only define -1).
@@ -45,6 +49,10 @@
  *   R22 FP8 row byte order: 448 E4M3 codes, 64 bf16 RoPE dims, 8 E8M0 scales.
  *   R24 a mask window holds query rows q0.. of each request; a live key end
  *       bounds both the words written and the keys the consumer admits.
+ *   R25 a second kv source (extra_kv [B,T2,D], same format) comes with its own
+ *       slot list [B,S,K2] and optional per-token length; a token's softmax
+ *       runs over its K main slots and its K2 extra slots together (main
+ *       first), the sink added once.
  *
  * Inputs are bf16 bit patterns (uint16) as stored on the device; each value
  * is widened exactly to double before any arithmetic.
@@ -127,6 +135,13 @@ typedef struct {
     const float *sink;
     const int32_t *idx;
     const int32_t *topk_len; /* [B*S] valid-prefix length per query token, or NULL */
+    /* the extra source (R25): kv2 / kv8_2 [B,T2,.] in the format of the main
+     * one, idx2 [B,S,K2], topk_len2 [B*S] or NULL; K2 = 0 without it */
+    const uint16_t *kv2;
+    const uint8_t *kv8_2;
+    const int32_t *idx2;
+    const int32_t *topk_len2;
+    int64_t T2, K2;
     double scale;
     double *o;
     int64_t B, S, H, D, T, K;
@@ -136,13 +151,15 @@ typedef struct {
     pthread_mutex_t mu;
 } attn_job;
 
-/* kv row `row` (= b*T + t) as D doubles, from bf16 or from the FP8 layout */
-static void load_kv_row(const attn_job *J, int64_t row, double *out) {
-    if (J->kv8) {
-        fp8_row_decode(J->kv8 + row * FP8_ROW_BYTES, out);
+/* kv row `row` (= b*T + t) of source `src` (0 main, 1 extra) as D doubles,
+ * from bf16 or from the FP8 layout */
+static void load_kv_row(const attn_job *J, int src, int64_t row, double *out) {
+    const uint8_t *k8 = src ? J->kv8_2 : J->kv8;
+    if (k8) {
+        fp8_row_decode(k8 + row * FP8_ROW_BYTES, out);
         return;
     }
-    const uint16_t *kr = J->kv + row * J->D;
+    const uint16_t *kr = (src ? J->kv2 : J->kv) + row * J->D;
     for (int64_t d = 0; d < J->D; ++d) out[d] = bf16_to_double(kr[d]);
 }
 
@@ -154,34 +171,54 @@ static void load_kv_row(const attn_job *J, int64_t row, double *out) {
  *   -inf for invalid ones; the sink logit attn_sink[h] is appended; softmax
  *   over the K+1 values; o = sum_{j<K} w_j * kv[b, idx_j, :] (the sink's
  *   weight is dropped).  [V4-5.2], [V4-5.5] */
+static int64_t clamp_len(const int32_t *lens, int64_t tok, int64_t K) {
+    if (lens == NULL) return K;
+    int64_t len = lens[tok];
+    if (len < 0) len = 0;
+    if (len > K) len = K;
+    return len;
+}
+
+/* One query token (b, s), every head h:
+ *   logits_j = scale * q[b,s,h,:] . kv[b, idx_j, :]   for valid slots j,
+ *   a slot j being valid when 0 <= idx_j < T and, if a per-token topk_length
+ *   is given, j < min(max(topk_length[b,s], 0), K) (the "topk length per
+ *   sequence" variant of the FlashMLA kernels, [V4-5.3]);
+ *   -inf for invalid ones; the sink logit attn_sink[h] is appended; softmax
+ *   over the K+1 values; o = sum_{j<K} w_j * kv[b, idx_j, :] (the sink's
+ *   weight is dropped).  [V4-5.2], [V4-5.5]
+ * With an extra source (R25) the token's slots are its K main slots followed
+ * by its K2 extra slots, slot K + j gathering extra_kv[b, idx2_j, :] under the
+ * same validity rule with T2 and the extra length; one softmax covers all
+ * K + K2 slots and the sink. */
 static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] */) {
     const int64_t b = tok / J->S, s = tok % J->S;
-    const int64_t H = J->H, D = J->D, T = J->T, K = J->K;
+    const int64_t H = J->H, D = J->D, K = J->K, K2 = J->K2, N = J->K + J->K2;
     const int32_t *idx = J->idx + (b * J->S + s) * K;
-    int64_t len = K;
-    if (J->topk_len) {
-        len = J->topk_len[b * J->S + s];
-        if (len < 0) len = 0;
-        if (len > K) len = K;
-    }
-    double *logit = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    const int32_t *idx2 = K2 > 0 ? J->idx2 + (b * J->S + s) * K2 : NULL;
+    const int64_t len = clamp_len(J->topk_len, b * J->S + s, K);
+    const int64_t len2 = clamp_len(J->topk_len2, b * J->S + s, K2);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    char *valid = (char *)malloc((size_t)(N > 0 ? N : 1));
     double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
     /* the gathered rows of the token's valid slots, widened once (shared by
      * every head: kv is one head shared by all query heads) */
-    double *krows = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)D);
-    for (int64_t j = 0; j < K; ++j) {
-        const int64_t t = idx[j];
-        if (j < len && t >= 0 && t < T) load_kv_row(J, b * T + t, krows + j * D);
+    double *krows = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * (size_t)D);
+    for (int64_t j = 0; j < N; ++j) {
+        const int src = j >= K;
+        const int64_t t = src ? idx2[j - K] : idx[j];
+        const int64_t Tsrc = src ? J->T2 : J->T;
+        valid[j] = (src ? (j - K < len2) : (j < len)) && t >= 0 && t < Tsrc; /* R1, R19 */
+        if (valid[j]) load_kv_row(J, src, b * Tsrc + t, krows + j * D);
     }
     for (int64_t h = 0; h < H; ++h) {
         double *orow = out + h * D;
         for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
         const uint16_t *qh = J->q + ((b * J->S + s) * H + h) * D;
         for (int64_t d = 0; d < D; ++d) qrow[d] = bf16_to_double(qh[d]);
-        /* logits of the K slots, -inf where the slot is invalid (R1) */
-        for (int64_t j = 0; j < K; ++j) {
-            int64_t t = idx[j];
-            if (j >= len || t < 0 || t >= T) {
+        /* logits of the slots, -inf where the slot is invalid (R1) */
+        for (int64_t j = 0; j < N; ++j) {
+            if (!valid[j]) {
                 logit[j] = -INFINITY;
                 continue;
             }
@@ -193,7 +230,7 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         const double sink = (double)J->sink[h];
         /* softmax over [logits..., sink] */
         double m = sink;
-        for (int64_t j = 0; j < K; ++j)
+        for (int64_t j = 0; j < N; ++j)
             if (logit[j] > m) m = logit[j];
         if (isnan(sink)) { /* R7: NaN propagates */
             for (int64_t d = 0; d < D; ++d) orow[d] = NAN;
@@ -202,8 +239,8 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         if (m == INFINITY && sink == INFINITY) continue; /* R4: o = 0 */
         if (m == -INFINITY) continue;                    /* R6: o = 0 */
         double denom = exp(sink - m);
-        for (int64_t j = 0; j < K; ++j) denom += exp(logit[j] - m);
-        for (int64_t j = 0; j < K; ++j) {
+        for (int64_t j = 0; j < N; ++j) denom += exp(logit[j] - m);
+        for (int64_t j = 0; j < N; ++j) {
             if (logit[j] == -INFINITY) continue; /* weight exactly 0 */
             const double w = exp(logit[j] - m) / denom;
             const double *krow = krows + j * D;
@@ -211,6 +248,7 @@ static void attn_one_token(const attn_job *J, int64_t tok, double *out /* [H,D] 
         }
     }
     free(logit);
+    free(valid);
     free(qrow);
     free(krows);
 }
@@ -233,15 +271,26 @@ static int resolve_threads(int nthreads) {
     return n > 0 ? (int)n : 1;
 }
 
-static int run_attn_job(const uint16_t *q, const uint16_t *kv, const uint8_t *kv8, const float *attn_sink,
-                        const int32_t *topk_idxs, const int32_t *topk_length, double softmax_scale, int64_t B,
-                        int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, const int64_t *tokens, int64_t ntok,
-                        double *o, int nthreads) {
+typedef struct {
+    const uint16_t *kv2;
+    const uint8_t *kv8_2;
+    const int32_t *idx2, *len2;
+    int64_t T2, K2;
+} extra_src;
+
+static int run_attn_job_x(const uint16_t *q, const uint16_t *kv, const uint8_t *kv8, const float *attn_sink,
+                          const int32_t *topk_idxs, const int32_t *topk_length, const extra_src *X,
+                          double softmax_scale, int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int64_t K,
+                          const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
     if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || K < 0 || ntok < 0) return ORACLE_EINVAL;
+    if (X && (X->K2 < 0 || X->T2 < 0 || (X->K2 > 0 && (X->idx2 == NULL || (X->kv2 == NULL && X->kv8_2 == NULL)))))
+        return ORACLE_EINVAL;
     for (int64_t i = 0; i < ntok; ++i)
         if (tokens[i] < 0 || tokens[i] >= B * S) return ORACLE_EINVAL;
     attn_job J;
     J.q = q; J.kv = kv; J.kv8 = kv8; J.sink = attn_sink; J.idx = topk_idxs; J.topk_len = topk_length;
+    J.kv2 = X ? X->kv2 : NULL; J.kv8_2 = X ? X->kv8_2 : NULL; J.idx2 = X ? X->idx2 : NULL;
+    J.topk_len2 = X ? X->len2 : NULL; J.T2 = X ? X->T2 : 0; J.K2 = X ? X->K2 : 0;
     J.scale = softmax_scale;
     J.o = o; J.B = B; J.S = S; J.H = H; J.D = D; J.T = T; J.K = K;
     J.tokens = tokens; J.ntok = ntok; J.next = 0;
@@ -254,6 +303,14 @@ static int run_attn_job(const uint16_t *q, const uint16_t *kv, const uint8_t *kv
     free(th);
     pthread_mutex_destroy(&J.mu);
     return ORACLE_OK;
+}
+
+static int run_attn_job(const uint16_t *q, const uint16_t *kv, const uint8_t *kv8, const float *attn_sink,
+                        const int32_t *topk_idxs, const int32_t *topk_length, double softmax_scale, int64_t B,
+                        int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, const int64_t *tokens, int64_t ntok,
+                        double *o, int nthreads) {
+    return run_attn_job_x(q, kv, kv8, attn_sink, topk_idxs, topk_length, NULL, softmax_scale, B, S, H, D, T, K,
+                          tokens, ntok, o, nthreads);
 }
 
 /* Evaluates the tokens listed in `tokens` (flat b*S+s ids); o is [ntok,H,D].
@@ -276,6 +333,30 @@ int oracle_sparse_attn_fp8_tokens(const uint16_t *q, const uint8_t *kv8, const f
     if (kv8 == NULL) return ORACLE_EINVAL;
     return run_attn_job(q, NULL, kv8, attn_sink, topk_idxs, topk_length, softmax_scale, B, S, H, FP8_DIM, T, K,
                         tokens, ntok, o, nthreads);
+}
+
+/* With the extra kv source (R25): extra_kv bf16 [B,T2,D] (or, for the FP8
+ * variant, 584-byte rows), extra_idxs [B,S,K2], extra_length [B*S] or NULL. */
+int oracle_sparse_attn_extra_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,
+                                    const int32_t *topk_idxs, const int32_t *topk_length, const uint16_t *extra_kv,
+                                    const int32_t *extra_idxs, const int32_t *extra_length, double softmax_scale,
+                                    int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, int64_t T2,
+                                    int64_t K2, const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
+    const extra_src X = {extra_kv, NULL, extra_idxs, extra_length, T2, K2};
+    return run_attn_job_x(q, kv, NULL, attn_sink, topk_idxs, topk_length, &X, softmax_scale, B, S, H, D, T, K,
+                          tokens, ntok, o, nthreads);
+}
+
+int oracle_sparse_attn_fp8_extra_tokens(const uint16_t *q, const uint8_t *kv8, const float *attn_sink,
+                                        const int32_t *topk_idxs, const int32_t *topk_length,
+                                        const uint8_t *extra_kv8, const int32_t *extra_idxs,
+                                        const int32_t *extra_length, double softmax_scale, int64_t B, int64_t S,
+                                        int64_t H, int64_t T, int64_t K, int64_t T2, int64_t K2,
+                                        const int64_t *tokens, int64_t ntok, double *o, int nthreads) {
+    if (kv8 == NULL) return ORACLE_EINVAL;
+    const extra_src X = {NULL, extra_kv8, extra_idxs, extra_length, T2, K2};
+    return run_attn_job_x(q, NULL, kv8, attn_sink, topk_idxs, topk_length, &X, softmax_scale, B, S, H, FP8_DIM, T,
+                          K, tokens, ntok, o, nthreads);
 }
 
 int oracle_sparse_attn_tokens(const uint16_t *q, const uint16_t *kv, const float *attn_sink,

@@ -541,3 +541,89 @@ def test_masked_dense_key_offset_and_live_end_together():
     shifted = torch.where(keep, inp.topk_idxs - start, torch.full_like(inp.topk_idxs, -1))
     want = oracle.sparse_attn(inp.q, chunk, inp.attn_sink, shifted, inp.softmax_scale)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------- extra kv source (R25)
+
+def _extra_case(seed, B=2, S=3, H=4, D=32, T=40, K=24, T2=30, K2=20, p_invalid=0.15, fp8=False):
+    """A main and an extra source with their own slot lists and lengths."""
+    g = torch.Generator().manual_seed(seed)
+    if fp8:
+        main = workloads.random_attn_fp8(B, S, H, T, K, p_invalid=p_invalid, seed=seed)
+        extra = workloads.random_attn_fp8(B, S, H, T2, K2, p_invalid=p_invalid, seed=seed + 1)
+    else:
+        main = workloads.random_attn(B, S, H, D, T, K, p_invalid=p_invalid, seed=seed)
+        extra = workloads.random_attn(B, S, H, D, T2, K2, p_invalid=p_invalid, seed=seed + 1)
+    len1 = torch.randint(-2, K + 3, (B, S), generator=g, dtype=torch.int32)
+    len2 = torch.randint(-2, K2 + 3, (B, S), generator=g, dtype=torch.int32)
+    return main, extra, len1, len2
+
+
+def _concatenated(main_kv, extra_kv, idx, idx2, len1, len2):
+    """The same problem as one source: kv rows [main | extra] per batch, slots
+    [main | extra] per token with the extra indices shifted past the main rows
+    and every slot at or past its list's length (or out of its source's range)
+    set to -1."""
+    T, T2 = main_kv.shape[1], extra_kv.shape[1]
+    kv = torch.cat([main_kv, extra_kv], dim=1)
+    K, K2 = idx.shape[-1], idx2.shape[-1]
+    a = idx.clone().long()
+    a[(a < 0) | (a >= T) | (torch.arange(K) >= len1.clamp(0, K).long().unsqueeze(-1))] = -1
+    e = idx2.clone().long()
+    bad = (e < 0) | (e >= T2) | (torch.arange(K2) >= len2.clamp(0, K2).long().unsqueeze(-1))
+    e = torch.where(bad, torch.full_like(e, -1), e + T)
+    return kv, torch.cat([a, e], dim=-1).to(torch.int32)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_extra_source_equals_one_concatenated_source(seed):
+    main, extra, len1, len2 = _extra_case(seed)
+    got = oracle.sparse_attn(main.q, main.kv, main.attn_sink, main.topk_idxs, main.softmax_scale, topk_length=len1,
+                             extra_kv=extra.kv, extra_idxs=extra.topk_idxs, extra_length=len2)
+    kv, idx = _concatenated(main.kv, extra.kv, main.topk_idxs, extra.topk_idxs, len1, len2)
+    want = oracle.sparse_attn(main.q, kv, main.attn_sink, idx, main.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_extra_source_matches_library_sdpa_on_the_union():
+    main, extra, len1, len2 = _extra_case(7)
+    kv, idx = _concatenated(main.kv, extra.kv, main.topk_idxs, extra.topk_idxs, len1, len2)
+    union = workloads.AttnInputs(main.q, kv, main.attn_sink, idx, main.softmax_scale)
+    got = oracle.sparse_attn(main.q, main.kv, main.attn_sink, main.topk_idxs, main.softmax_scale, topk_length=len1,
+                             extra_kv=extra.kv, extra_idxs=extra.topk_idxs, extra_length=len2)
+    np.testing.assert_allclose(got, _sdpa_reference(union), rtol=1e-10, atol=1e-12)
+
+
+def test_extra_source_alone_and_swapped_roles():
+    main, extra, len1, len2 = _extra_case(11, p_invalid=0.0)
+    none = torch.full_like(main.topk_idxs, -1)
+    alone = oracle.sparse_attn(main.q, main.kv, main.attn_sink, none, main.softmax_scale,
+                               extra_kv=extra.kv, extra_idxs=extra.topk_idxs)
+    want = oracle.sparse_attn(main.q, extra.kv, main.attn_sink, extra.topk_idxs, main.softmax_scale)
+    np.testing.assert_allclose(alone, want, rtol=1e-12, atol=1e-12)
+    # the two sources are interchangeable: one softmax over both slot lists
+    a = oracle.sparse_attn(main.q, main.kv, main.attn_sink, main.topk_idxs, main.softmax_scale, topk_length=len1,
+                           extra_kv=extra.kv, extra_idxs=extra.topk_idxs, extra_length=len2)
+    b = oracle.sparse_attn(main.q, extra.kv, main.attn_sink, extra.topk_idxs, main.softmax_scale, topk_length=len2,
+                           extra_kv=main.kv, extra_idxs=main.topk_idxs, extra_length=len1)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_extra_source_empty_list_changes_nothing():
+    main, extra, len1, _ = _extra_case(13)
+    zero = torch.zeros_like(len1)
+    got = oracle.sparse_attn(main.q, main.kv, main.attn_sink, main.topk_idxs, main.softmax_scale, topk_length=len1,
+                             extra_kv=extra.kv, extra_idxs=extra.topk_idxs, extra_length=zero)
+    want = oracle.sparse_attn(main.q, main.kv, main.attn_sink, main.topk_idxs, main.softmax_scale, topk_length=len1)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("seed", [21, 22])
+def test_extra_fp8_source_equals_one_concatenated_source(seed):
+    main, extra, len1, len2 = _extra_case(seed, H=4, T=30, K=20, T2=25, K2=18, fp8=True)
+    got = oracle.sparse_attn_fp8(main.q, main.kv8, main.attn_sink, main.topk_idxs, main.softmax_scale,
+                                 topk_length=len1, extra_kv8=extra.kv8, extra_idxs=extra.topk_idxs, extra_length=len2)
+    kv8 = torch.cat([main.kv8, extra.kv8], dim=1)
+    _, idx = _concatenated(main.kv8, extra.kv8, main.topk_idxs, extra.topk_idxs, len1, len2)
+    want = oracle.sparse_attn_fp8(main.q, kv8, main.attn_sink, idx, main.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
