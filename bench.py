@@ -412,36 +412,42 @@ def run_gpu(args):
     # ---- mask build on the mask workload (B=4, Q=2048, 8193 keys, K=2048)
     mask_obj = None
     if rank == 0 and not args.no_mask:
-        mi = workloads.topk_mask().to(dev)
+        # Four input sets of the same workload (268 MB of indices, twice the
+        # L2) are built in turn, back to back: each call reads its indices from
+        # HBM (the three calls in between evict them), and launches queue
+        # behind one another as in a serving loop.
+        sets = [workloads.topk_mask(seed=1004 + i).to(dev) for i in range(4)]
+        mi = sets[0]
         shape = binding.topk_mask_shape(mi.batch, mi.max_q_len, mi.max_key_len, True)
         mbuf = torch.zeros(shape, dtype=torch.int32, device=dev)
 
-        def mstep():
-            binding.build_topk_mask(mi.topk, mi.cu_q_lens, mi.max_q_len, mi.max_key_len, mi.key_starts, out=mbuf)
+        def mstep(i=0):
+            m = sets[i % 4]
+            binding.build_topk_mask(m.topk, m.cu_q_lens, m.max_q_len, m.max_key_len, m.key_starts, out=mbuf)
 
-        for _ in range(max(3, args.warmup)):
-            flush.zero_()
-            mstep()
+        for i in range(max(4, args.warmup)):
+            mstep(i)
         torch.cuda.synchronize()
-        m_ms = []
-        for _ in range(max(args.steps, 10)):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            mstep()
-            b.record(stream)
-            b.synchronize()
-            m_ms.append(a.elapsed_time(b))
-        mms = sum(m_ms) / len(m_ms)
+        n_calls = 4 * max(10, args.steps // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n_calls):
+            mstep(i)
+        b.record(stream)
+        b.synchronize()
+        mms = a.elapsed_time(b) / n_calls
+        assert binding.sa_device_error(True) == 0
         live_words = (mi.max_key_len + 31) // 32
         m_bytes = mi.topk.numel() * 4 + mi.batch * mi.max_q_len * live_words * 4
         hbm, _, _, src = _peaks()
         m_gbs = m_bytes / (mms * 1e-3) / 1e9
         mask_obj = {"workload": mi.name, "us_per_call": mms * 1e3, "gbs": m_gbs,
-                    "algorithmic_bytes": m_bytes,
+                    "algorithmic_bytes": m_bytes, "calls": n_calls,
+                    "timing": "back-to-back calls rotating over 4 input sets (268 MB of indices > L2)",
                     "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": m_gbs / hbm, "peak_source": src,
                                  "traffic": _profile_traffic("mask_build", _source_hash(MASK_SOURCES))}}
+        del sets[1:]
 
         # ---- the mask's consumer: dense attention over the admitted keys of
         # the same 4 x 2048 query rows (8 heads of 64, 8193 keys per request)

@@ -28,11 +28,11 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_SHAPE", 3: "SA_ERR_AL
 EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_workspace_size",
            "sa_sparse_attn_fwd", "sa_sparse_attn_fwd_splits", "sa_topk_mask_shape",
            "sa_build_topk_mask", "sa_device_error", "sa_sparse_attn_fwd_static_ws",
-           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_sparse_attn_fwd_topk_length",
+           "sa_sparse_attn_launch_count", "sa_selftest_wait_timeout", "sa_selftest_wait_drain", "sa_sparse_attn_fwd_topk_length",
            "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count",
            "sa_sparse_attn_fwd_fp8", "sa_sparse_attn_fp8_launch_count", "sa_build_topk_mask_window",
            "sa_masked_dense_attn_fwd_window", "sa_topk_mask_chunk_rows", "sa_topk_masked_attn_fwd",
-           "sa_topk_masked_attn_workspace_size")
+           "sa_topk_masked_attn_workspace_size", "sa_sparse_attn_fwd_extra", "sa_sparse_attn_fwd_fp8_extra")
 
 _lock = threading.Lock()
 _lib = None
@@ -90,6 +90,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_masked_dense_attn_launch_count.restype = i32
         lib.sa_sparse_attn_fwd_fp8.argtypes = [p, p, p, p, p, ctypes.c_float, p] + [i64] * 5 + [i32, p, sz, p]
         lib.sa_sparse_attn_fwd_fp8.restype = i32
+        lib.sa_sparse_attn_fwd_extra.argtypes = [p, p, p, p, p, p, p, p, ctypes.c_float, p] + [i64] * 8 + [i32, p, sz, p]
+        lib.sa_sparse_attn_fwd_extra.restype = i32
+        lib.sa_sparse_attn_fwd_fp8_extra.argtypes = ([p, p, p, p, p, p, p, p, ctypes.c_float, p] + [i64] * 7 +
+                                                     [i32, p, sz, p])
+        lib.sa_sparse_attn_fwd_fp8_extra.restype = i32
         lib.sa_sparse_attn_fp8_launch_count.argtypes = [i64] * 4 + [i32]
         lib.sa_sparse_attn_fp8_launch_count.restype = i32
         lib.sa_build_topk_mask_window.argtypes = [p, i64, p, i64, i64, i64, i64, i64, p, p, p, p, p]
@@ -106,6 +111,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_topk_masked_attn_workspace_size.restype = sz
         lib.sa_selftest_wait_timeout.argtypes = [ctypes.c_longlong]
         lib.sa_selftest_wait_timeout.restype = i32
+        lib.sa_selftest_wait_drain.argtypes = [i32, ctypes.c_longlong, ctypes.POINTER(ctypes.c_float)]
+        lib.sa_selftest_wait_drain.restype = i32
         lib.sa_device_error.argtypes = [i32]
         lib.sa_device_error.restype = i32
         _lib = lib
@@ -235,6 +242,13 @@ def sa_selftest_wait_timeout(max_cycles: int) -> int:
     return int(load().sa_selftest_wait_timeout(int(max_cycles)))
 
 
+def sa_selftest_wait_drain(ctas: int, first_cycles: int) -> tuple[int, float]:
+    """(code, elapsed ms) of the fast-drain self-test (see include/sa.h)."""
+    ms = ctypes.c_float(0.0)
+    code = int(load().sa_selftest_wait_drain(int(ctas), int(first_cycles), ctypes.byref(ms)))
+    return code, float(ms.value)
+
+
 def sa_device_error(clear: bool = True) -> int:
     return int(load().sa_device_error(int(bool(clear))))
 
@@ -299,6 +313,62 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk
                                    _dptr(out), B, S, H, D, T, K, int(num_splits), _dptr(workspace), ws_bytes,
                                    _stream_ptr(stream))
     _check("sa_sparse_attn_fwd_splits", rc)
+    return out
+
+
+def sa_sparse_attn_fwd_extra(q, kv, attn_sink, topk_idxs, topk_length, extra_kv, extra_topk_idxs,
+                             extra_topk_length, softmax_scale, o, B, S, H, D, T, K, T2, K2, num_splits, workspace,
+                             workspace_bytes, stream):
+    return int(load().sa_sparse_attn_fwd_extra(q, kv, attn_sink, topk_idxs, topk_length, extra_kv, extra_topk_idxs,
+                                               extra_topk_length, softmax_scale, o, B, S, H, D, T, K, T2, K2,
+                                               num_splits, workspace, workspace_bytes, stream))
+
+
+def sa_sparse_attn_fwd_fp8_extra(q, kv_fp8, attn_sink, topk_idxs, topk_length, extra_kv_fp8, extra_topk_idxs,
+                                 extra_topk_length, softmax_scale, o, B, S, H, T, K, T2, K2, num_splits, workspace,
+                                 workspace_bytes, stream):
+    return int(load().sa_sparse_attn_fwd_fp8_extra(q, kv_fp8, attn_sink, topk_idxs, topk_length, extra_kv_fp8,
+                                                   extra_topk_idxs, extra_topk_length, softmax_scale, o, B, S, H, T,
+                                                   K, T2, K2, num_splits, workspace, workspace_bytes, stream))
+
+
+def sparse_attn_extra(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk_idxs: torch.Tensor,
+                      extra_kv: torch.Tensor, extra_topk_idxs: torch.Tensor, softmax_scale: float,
+                      topk_length: torch.Tensor | None = None, extra_topk_length: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, num_splits: int = 0,
+                      stream=None) -> torch.Tensor:
+    """sparse_attn over two kv sources: each token's K main slots (kv,
+    topk_idxs) and its K2 extra slots (extra_kv [B,T2,D] or, for FP8 caches,
+    uint8 [B,T2,584] like kv; extra_topk_idxs [B,S,K2]) in one softmax."""
+    fp8 = kv.dtype == torch.uint8
+    B, S, H, D = q.shape
+    T, T2 = kv.shape[1], extra_kv.shape[1]
+    K, K2 = topk_idxs.shape[-1], extra_topk_idxs.shape[-1]
+    for name, t in (("q", q), ("kv", kv), ("attn_sink", attn_sink), ("topk_idxs", topk_idxs),
+                    ("extra_kv", extra_kv), ("extra_topk_idxs", extra_topk_idxs), ("topk_length", topk_length),
+                    ("extra_topk_length", extra_topk_length)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if extra_kv.dtype != kv.dtype or topk_idxs.dtype != torch.int32 or extra_topk_idxs.dtype != torch.int32:
+        raise ValueError("kv and extra_kv share a dtype; the index lists are int32")
+    if out is None:
+        out = torch.empty_like(q)
+    need = sa_sparse_attn_workspace_size(B, S, H, D, K + K2, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if fp8:
+        rc = sa_sparse_attn_fwd_fp8_extra(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(topk_idxs), _dptr(topk_length),
+                                          _dptr(extra_kv), _dptr(extra_topk_idxs), _dptr(extra_topk_length),
+                                          float(softmax_scale), _dptr(out), B, S, H, T, K, T2, K2, int(num_splits),
+                                          _dptr(workspace), ws_bytes, _stream_ptr(stream))
+        _check("sa_sparse_attn_fwd_fp8_extra", rc)
+    else:
+        rc = sa_sparse_attn_fwd_extra(_dptr(q), _dptr(kv), _dptr(attn_sink), _dptr(topk_idxs), _dptr(topk_length),
+                                      _dptr(extra_kv), _dptr(extra_topk_idxs), _dptr(extra_topk_length),
+                                      float(softmax_scale), _dptr(out), B, S, H, D, T, K, T2, K2, int(num_splits),
+                                      _dptr(workspace), ws_bytes, _stream_ptr(stream))
+        _check("sa_sparse_attn_fwd_extra", rc)
     return out
 
 

@@ -168,6 +168,15 @@ struct TcParams {
     const float *sink;        // [H]
     const int32_t *idx;       // [tokens, K]
     const int32_t *topk_len;  // [tokens] valid-prefix length per token, or nullptr
+    // extra kv source: a token's slots are its K1 main slots (idx, kv), then
+    // its K2 extra slots (idx2 [tokens, K2], kv2 [B, T2, .], topk_len2 or
+    // nullptr); K = K1 + K2.  Extra row t2 of request b is row number
+    // BT + b*T2 + t2 in the slot lists (BT = B*T rounded up to even, so a
+    // row's parity is that of its index in its own source)
+    const void *kv2;
+    const int32_t *idx2;
+    const int32_t *topk_len2;
+    int64_t T2, K1, K2, BT;
     __nv_bfloat16 *o;         // [tokens, H, D]
     float *ws_o;              // [tokens, splits, H, D]
     float *ws_lse;            // [tokens, splits, H]
@@ -356,13 +365,14 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
     const float sink_t = tid < p.H ? __ldg(p.sink + tid) : 0.f;   // into sink_tab below
     // slot j of this token counts only below its topk length (clamped to
     // [0, K]); loaded beside the index list, applied when it is converted
-    const int32_t len_t = p.topk_len != nullptr ? __ldg(p.topk_len + tok) : int32_t(p.K);
+    const int32_t len_t = p.topk_len != nullptr ? __ldg(p.topk_len + tok) : int32_t(p.K1);
+    const int32_t len2_t = p.topk_len2 != nullptr ? __ldg(p.topk_len2 + tok) : int32_t(p.K2);
     if (p.mask == nullptr) {
-        const int32_t *irow = p.idx + tok * p.K + slot0;
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int j = (u * kWarpsAll + warp) * 32 + lane;
-            tv[u] = j < nslots ? __ldg(irow + j) : -1;
+            const int64_t g = slot0 + j;   // slot of the token: main slots, then extra ones
+            tv[u] = j >= nslots ? -1 : g < p.K1 ? __ldg(p.idx + tok * p.K1 + g) : __ldg(p.idx2 + tok * p.K2 + (g - p.K1));
         }
     } else {
         // key t is admitted iff bit (t + key_start) & 31 of word
@@ -432,8 +442,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
             const int ch = u * kWarpsAll + warp;
             if (ch < ntiles * 2) {
                 const int j = ch * 32 + lane;
-                const bool v = tv[u] >= 0 && int64_t(tv[u]) < p.T && slot0 + j < int64_t(len_t);
-                rowc[j] = v ? int32_t(b * p.T + tv[u]) : -1;
+                const int64_t g = slot0 + j;
+                const bool main = g < p.K1;
+                const bool v = tv[u] >= 0 && (main ? int64_t(tv[u]) < p.T && g < int64_t(len_t)
+                                                   : int64_t(tv[u]) < p.T2 && g - p.K1 < int64_t(len2_t));
+                rowc[j] = !v ? -1 : main ? int32_t(b * p.T + tv[u]) : int32_t(p.BT + b * p.T2 + tv[u]);
                 const uint32_t m = __ballot_sync(0xffffffffu, v);
                 if (lane == 0) reinterpret_cast<uint32_t *>(vmask)[ch] = m;
             }
@@ -516,6 +529,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 // through) of rows w, w + 3, ... into bf16 in the 128B-swizzled kv
                 // stage the MMA reads, then free the staging buffer.
                 const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
+                const uint8_t *kv8x = reinterpret_cast<const uint8_t *>(p.kv2);   // extra FP8 rows
                 const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
                 const int nwin = crank == 0 ? 16 : 20;            // windows of an even row
                 if (warp < kFirstGatherWarp + kF8CopyWarps) {
@@ -536,7 +550,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                             const int r = it / W, w = it - r * W;
                             if (r >= kBN) continue;
                             const int32_t row = rc[r];
-                            const int64_t rr = row >= 0 ? int64_t(row) : 0;
+                            // row in its own source (extra rows rebased past the even BT)
+                            const bool xr = row >= p.BT;
+                            const int64_t rr = row < 0 ? 0 : xr ? int64_t(row) - p.BT : int64_t(row);
                             const uint32_t n = row >= 0 ? 16u : 0u;
                             const int shift = int(rr & 1) * 8;
                             const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
@@ -549,8 +565,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                             // window), or nothing
                             const bool win = w < nw;
                             const bool scl = w == nw && (!shift || crank == 0);
-                            const uint8_t *src =
-                                kv8 + rr * kF8Row + (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
+                            const uint8_t *src = (xr ? kv8x : kv8) + rr * kF8Row +
+                                                 (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
                             const uint32_t dst = d + (win ? 16u * uint32_t(w) : uint32_t(C::STG_SCALE));
                             if (win || scl) ptx::cp_async_16(dst, src, win || shift ? n : (n >> 1));
                         }
@@ -660,6 +676,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 const int sub = lane / CPR, ch = lane % CPR;
                 const uint32_t dst_col = uint32_t(ch >> 3) * (kBN * 128);
                 const char *kvb = reinterpret_cast<const char *>(p.kv) + (int64_t(crank) * DC + ch * 8) * 2;
+                // extra rows: the same offset into the extra source, rebased past BT
+                const char *kvb2 = p.kv2 == nullptr ? kvb
+                                                     : reinterpret_cast<const char *>(p.kv2) +
+                                                           (int64_t(crank) * DC + ch * 8 - p.BT * p.D) * 2;
                 bool ok = true;
                 int a = 0;
                 for (; a < n_act; ++a) {
@@ -683,7 +703,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                         const int r = i * STEP + g * RPI + sub;   // warp g: row groups g, g + G, ...
                         if (STEP * ITERS > kBN && r >= kBN) break;
                         const int32_t row = rc[r];
-                        const char *src = kvb + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
+                        const char *src = (row >= p.BT ? kvb2 : kvb) + (row >= 0 ? int64_t(row) : 0) * p.D * 2;
                         const uint32_t dst = stage + dst_col + uint32_t(r) * 128u + uint32_t((ch & 7) ^ (r & 7)) * 16u;
                         ptx::cp_async_16(dst, src, row >= 0 ? 16u : 0u);
                     }
@@ -1576,9 +1596,12 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.ws_o = a.ws_o;
     p.ws_lse = a.ws_lse;
-    p.S = a.S; p.H = a.H; p.D = a.D; p.T = a.T; p.K = a.K;
+    p.S = a.S; p.H = a.H; p.D = a.D; p.T = a.T; p.K = a.K + a.K2;
+    p.K1 = a.K; p.K2 = a.K2; p.T2 = a.T2;
+    p.kv2 = a.kv2; p.idx2 = a.idx2; p.topk_len2 = a.topk_len2;
+    p.BT = (a.B * a.T + 1) / 2 * 2;
     p.num_splits = a.num_splits;
-    p.unit_slots = int(split_slots(a.K, a.num_splits));
+    p.unit_slots = int(split_slots(a.K + a.K2, a.num_splits));
     const int cs_fused = CL * a.num_splits;
     const bool fused = fused_combine<DC, CL, F8>(dev, a.num_splits);
     p.fused = fused ? 1 : 0;
@@ -1701,6 +1724,24 @@ __global__ void wait_timeout_selftest_kernel(long long max_cycles) {
 
 cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream) {
     wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(max_cycles);
+    return cudaGetLastError();
+}
+
+// Self-test of the fast drain: CTA 0 waits with a short limit on a phase
+// nothing completes, every other CTA with the full limit; all of them return
+// soon after CTA 0 records its timeout (the waits watch the error word).
+__global__ void wait_drain_selftest_kernel(long long first_cycles) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    (void)wait_bar(ptx::smem_u32(&bar), 0, blockIdx.x == 0 ? first_cycles : kWaitCycles);
+}
+
+cudaError_t launch_wait_drain_selftest(int ctas, long long first_cycles, cudaStream_t stream) {
+    wait_drain_selftest_kernel<<<ctas, 32, 0, stream>>>(first_cycles);
     return cudaGetLastError();
 }
 

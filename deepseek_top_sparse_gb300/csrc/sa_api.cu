@@ -147,42 +147,80 @@ int sa_sparse_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int6
     return sa::kernels_per_call(D, splits);
 }
 
-sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const float *attn_sink,
-                                         const int32_t *topk_idxs, const int32_t *topk_length,
-                                         float softmax_scale, void *o, int64_t B, int64_t S, int64_t H,
-                                         int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
-                                         size_t workspace_bytes, sa_stream_t stream) {
-    if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || K < 0) return SA_ERR_INVALID_ARG;
+namespace {
+
+// A second kv source (its K2 slots join each token's softmax after the K main
+// slots); K2 = 0 without one.
+struct ExtraSrc {
+    const void *kv = nullptr;
+    const int32_t *idx = nullptr;
+    const int32_t *len = nullptr;
+    int64_t T2 = 0, K2 = 0;
+};
+
+// Every check of the sparse_attn calls, then the launch(es).  kv (and the
+// extra kv) are bf16 rows of D values, or FP8 rows of 584 bytes (D = 512).
+sa_status attn_call(const void *q, const void *kv, bool fp8, const float *attn_sink, const int32_t *topk_idxs,
+                    const int32_t *topk_length, const ExtraSrc &x, float softmax_scale, void *o, int64_t B,
+                    int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
+                    size_t workspace_bytes, sa_stream_t stream) {
+    if (B < 0 || S < 0 || H < 0 || D < 0 || T < 0 || K < 0 || x.T2 < 0 || x.K2 < 0) return SA_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
     if (num_splits > 64) return SA_ERR_INVALID_ARG;
-    if (!attn_sizes_ok(B, S, H, D, K) || T < 1) return SA_ERR_SHAPE;
-    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    const int64_t Kt = K + x.K2;   // slots per token
+    if (!attn_sizes_ok(B, S, H, D, Kt) || (K > 0 && T < 1) || (x.K2 > 0 && x.T2 < 1)) return SA_ERR_SHAPE;
+    if ((B * T + 1) / 2 * 2 + B * x.T2 >= (int64_t(1) << 31)) return SA_ERR_SHAPE;   // 32-bit row numbers
     if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;   // q rows are 32-bit tensor-map coordinates
     if (B * S == 0) return SA_OK;
-    if (!q || !kv || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return SA_ERR_ALIGNMENT;
+    if (!q || !attn_sink || !o || (K > 0 && (!kv || !topk_idxs)) || (x.K2 > 0 && (!x.kv || !x.idx)))
+        return SA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(x.kv)) return SA_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3) ||
-        (reinterpret_cast<uintptr_t>(topk_length) & 3))
+        (reinterpret_cast<uintptr_t>(topk_length) & 3) || (reinterpret_cast<uintptr_t>(x.idx) & 3) ||
+        (reinterpret_cast<uintptr_t>(x.len) & 3))
         return SA_ERR_ALIGNMENT;
     DeviceInfo dev;
     const sa_status st = current_device(&dev);
     if (st != SA_OK) return st;
 
-    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms));
+    const int splits = clamp_splits(Kt, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, Kt, dev.sms));
     const size_t need = workspace_bytes_for(B, S, H, D, splits);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
 
     sa::AttnArgs a{};
-    a.q = q; a.kv = kv; a.sink = attn_sink; a.idx = topk_idxs; a.topk_len = topk_length;
+    a.q = q; a.kv = kv; a.kv_fp8 = fp8; a.sink = attn_sink; a.idx = topk_idxs; a.topk_len = topk_length;
+    a.kv2 = x.kv; a.idx2 = x.idx; a.topk_len2 = x.len; a.T2 = x.T2; a.K2 = x.K2;
     a.scale = softmax_scale; a.o = o;
     a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
     a.num_splits = splits;
     carve_workspace(a, workspace, B * S, H, D, splits);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the main kernel, then (for splits too many for one cluster) the combine
-    if (sa::launch_sparse_attn(a, dev.sms, s) != cudaSuccess) return SA_ERR_CUDA;
+    if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
     return SA_OK;
+}
+
+}  // namespace
+
+sa_status sa_sparse_attn_fwd_topk_length(const void *q, const void *kv, const float *attn_sink,
+                                         const int32_t *topk_idxs, const int32_t *topk_length,
+                                         float softmax_scale, void *o, int64_t B, int64_t S, int64_t H,
+                                         int64_t D, int64_t T, int64_t K, int num_splits, void *workspace,
+                                         size_t workspace_bytes, sa_stream_t stream) {
+    return attn_call(q, kv, false, attn_sink, topk_idxs, topk_length, ExtraSrc{}, softmax_scale, o, B, S, H, D, T,
+                     K, num_splits, workspace, workspace_bytes, stream);
+}
+
+sa_status sa_sparse_attn_fwd_extra(const void *q, const void *kv, const float *attn_sink, const int32_t *topk_idxs,
+                                   const int32_t *topk_length, const void *extra_kv, const int32_t *extra_topk_idxs,
+                                   const int32_t *extra_topk_length, float softmax_scale, void *o, int64_t B,
+                                   int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, int64_t T2, int64_t K2,
+                                   int num_splits, void *workspace, size_t workspace_bytes, sa_stream_t stream) {
+    ExtraSrc x;
+    x.kv = extra_kv; x.idx = extra_topk_idxs; x.len = extra_topk_length; x.T2 = T2; x.K2 = K2;
+    return attn_call(q, kv, false, attn_sink, topk_idxs, topk_length, x, softmax_scale, o, B, S, H, D, T, K,
+                     num_splits, workspace, workspace_bytes, stream);
 }
 
 int sa_sparse_attn_fp8_launch_count(int64_t B, int64_t S, int64_t H, int64_t K, int num_splits) {
@@ -198,37 +236,21 @@ sa_status sa_sparse_attn_fwd_fp8(const void *q, const uint8_t *kv_fp8, const flo
                                  const int32_t *topk_idxs, const int32_t *topk_length, float softmax_scale,
                                  void *o, int64_t B, int64_t S, int64_t H, int64_t T, int64_t K, int num_splits,
                                  void *workspace, size_t workspace_bytes, sa_stream_t stream) {
-    constexpr int64_t D = 512;
-    if (B < 0 || S < 0 || H < 0 || T < 0 || K < 0) return SA_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return SA_ERR_INVALID_ARG;
-    if (num_splits > 64) return SA_ERR_INVALID_ARG;
-    if (!attn_sizes_ok(B, S, H, D, K) || T < 1) return SA_ERR_SHAPE;
-    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
-    if (B * S * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
-    if (B * S == 0) return SA_OK;
-    if (!q || !kv_fp8 || !attn_sink || !topk_idxs || !o) return SA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(kv_fp8) || !aligned16(o)) return SA_ERR_ALIGNMENT;
-    if ((reinterpret_cast<uintptr_t>(topk_idxs) & 3) || (reinterpret_cast<uintptr_t>(attn_sink) & 3) ||
-        (reinterpret_cast<uintptr_t>(topk_length) & 3))
-        return SA_ERR_ALIGNMENT;
-    DeviceInfo dev;
-    const sa_status st = current_device(&dev);
-    if (st != SA_OK) return st;
+    return attn_call(q, kv_fp8, true, attn_sink, topk_idxs, topk_length, ExtraSrc{}, softmax_scale, o, B, S, H,
+                     512, T, K, num_splits, workspace, workspace_bytes, stream);
+}
 
-    const int splits = clamp_splits(K, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, K, dev.sms));
-    const size_t need = workspace_bytes_for(B, S, H, D, splits);
-    if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
-    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
-
-    sa::AttnArgs a{};
-    a.q = q; a.kv = kv_fp8; a.kv_fp8 = true; a.sink = attn_sink; a.idx = topk_idxs; a.topk_len = topk_length;
-    a.scale = softmax_scale; a.o = o;
-    a.B = B; a.S = S; a.H = H; a.D = D; a.T = T; a.K = K;
-    a.num_splits = splits;
-    carve_workspace(a, workspace, B * S, H, D, splits);
-    if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SA_ERR_CUDA;
-    return SA_OK;
+sa_status sa_sparse_attn_fwd_fp8_extra(const void *q, const uint8_t *kv_fp8, const float *attn_sink,
+                                       const int32_t *topk_idxs, const int32_t *topk_length,
+                                       const uint8_t *extra_kv_fp8, const int32_t *extra_topk_idxs,
+                                       const int32_t *extra_topk_length, float softmax_scale, void *o, int64_t B,
+                                       int64_t S, int64_t H, int64_t T, int64_t K, int64_t T2, int64_t K2,
+                                       int num_splits, void *workspace, size_t workspace_bytes,
+                                       sa_stream_t stream) {
+    ExtraSrc x;
+    x.kv = extra_kv_fp8; x.idx = extra_topk_idxs; x.len = extra_topk_length; x.T2 = T2; x.K2 = K2;
+    return attn_call(q, kv_fp8, true, attn_sink, topk_idxs, topk_length, x, softmax_scale, o, B, S, H, 512, T, K,
+                     num_splits, workspace, workspace_bytes, stream);
 }
 
 sa_status sa_sparse_attn_fwd_splits(const void *q, const void *kv, const float *attn_sink,
@@ -481,6 +503,27 @@ int sa_selftest_wait_timeout(long long max_cycles) {
     int before = 0;
     if (sa::read_device_error(&before, true) != cudaSuccess) return -1;   // start from a clear word
     if (sa::launch_wait_timeout_selftest(max_cycles, nullptr) != cudaSuccess) return -1;
+    int code = 0;
+    if (sa::read_device_error(&code, true) != cudaSuccess) return -1;
+    return code;
+}
+
+int sa_selftest_wait_drain(int ctas, long long first_cycles, float *elapsed_ms) {
+    if (ctas < 1 || ctas > 1024 || first_cycles < 1 || first_cycles > (1ll << 28) || elapsed_ms == nullptr)
+        return -1;
+    DeviceInfo dev;
+    if (current_device(&dev) != SA_OK) return -1;
+    int before = 0;
+    if (sa::read_device_error(&before, true) != cudaSuccess) return -1;   // start from a clear word
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return -1;
+    bool ok = cudaEventRecord(e0, nullptr) == cudaSuccess &&
+              sa::launch_wait_drain_selftest(ctas, first_cycles, nullptr) == cudaSuccess &&
+              cudaEventRecord(e1, nullptr) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
+              cudaEventElapsedTime(elapsed_ms, e0, e1) == cudaSuccess;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (!ok) return -1;
     int code = 0;
     if (sa::read_device_error(&code, true) != cudaSuccess) return -1;
     return code;

@@ -20,6 +20,7 @@ enum DeviceError : int {
 // records into it with atomicCAS(0 -> code) so the first failure sticks.
 cudaError_t read_device_error(int *value, bool clear);
 cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream);
+cudaError_t launch_wait_drain_selftest(int ctas, long long first_cycles, cudaStream_t stream);
 
 // ---- launchers (host side, enqueue only; arguments already validated) ----
 
@@ -32,7 +33,7 @@ struct AttnArgs {
     float scale;
     void *o;                // bf16 [B,S,H,D]
     int64_t B, S, H, D, T, K;
-    int num_splits;         // >= 1
+    int num_splits;         // >= 1 (planned over K + K2 slots)
     float *ws_o;            // fp32 [tokens, splits, H, D]   (splits > 1)
     float *ws_lse;          // fp32 [tokens, splits, H]      (splits > 1)
     // bit-mask mode (idx == nullptr, K == T): keys admitted by a packed mask
@@ -41,6 +42,12 @@ struct AttnArgs {
     int key_start_word = 0;           // 1: key offset read from mask[b, 0, mask_words - 1]
     bool kv_fp8 = false;              // kv rows in the FP8 format (D = 512)
     const int32_t *key_ends = nullptr;  // bit-mask mode: [B] live key end per request, or nullptr
+    // extra kv source: K2 more slots per token (idx2 [B,S,K2]) over kv2
+    // [B,T2,.] in kv's format, with an optional length topk_len2 [B,S]
+    const void *kv2 = nullptr;
+    const int32_t *idx2 = nullptr;
+    const int32_t *topk_len2 = nullptr;
+    int64_t T2 = 0, K2 = 0;
     // q / o hold io_S query rows per request and the call covers rows
     // io_s0 .. io_s0 + S - 1 of each (io_S = 0: io_S = S, io_s0 = 0)
     int64_t io_S = 0, io_s0 = 0;

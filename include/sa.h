@@ -162,6 +162,40 @@ sa_status sa_sparse_attn_fwd_fp8(const void *q, const uint8_t *kv_fp8, const flo
                                  void *o, int64_t B, int64_t S, int64_t H, int64_t T, int64_t K, int num_splits,
                                  void *workspace, size_t workspace_bytes, sa_stream_t stream);
 
+/* sparse_attn over two kv sources ("DeepSeek V4 源码剖析, 第5章" §5.6: the
+ * SM100 decode kernel keeps separate tensor maps extra_kv_nope /
+ * extra_kv_rope beside kv_nope / kv_rope; §5.13: extra_topk_length beside
+ * topk_length among the scheduler metadata's inputs).  The pages do not give
+ * the addressing; reading taken here: the extra source extra_kv [B, T2, D]
+ * (bf16, device, 16-byte aligned, in the main kv's format) has its own slot
+ * list extra_topk_idxs [B, S, K2] (int32, -1 or any index outside [0, T2) =
+ * invalid) and optional per-token length extra_topk_length [B, S] (NULL:
+ * every extra slot may count; same clamping as topk_length).  A token
+ * attends over its K main slots followed by its K2 extra slots in ONE
+ * softmax, with the sink counted once, so the result equals
+ * sa_sparse_attn_fwd_topk_length over the concatenated rows and slot lists.
+ * K >= 0, K2 >= 0, K + K2 >= 1; with K = 0, kv and topk_idxs may be NULL,
+ * with K2 = 0 the extra arguments may be NULL.  Splits, workspace and launch
+ * count are those of K + K2 slots: size the workspace with
+ * sa_sparse_attn_workspace_size(B, S, H, D, K + K2, num_splits).  Errors as
+ * sa_sparse_attn_fwd_topk_length; also SA_ERR_SHAPE when
+ * B*T (rounded up to even) + B*T2 >= 2^31. */
+sa_status sa_sparse_attn_fwd_extra(const void *q, const void *kv, const float *attn_sink, const int32_t *topk_idxs,
+                                   const int32_t *topk_length, const void *extra_kv, const int32_t *extra_topk_idxs,
+                                   const int32_t *extra_topk_length, float softmax_scale, void *o, int64_t B,
+                                   int64_t S, int64_t H, int64_t D, int64_t T, int64_t K, int64_t T2, int64_t K2,
+                                   int num_splits, void *workspace, size_t workspace_bytes, sa_stream_t stream);
+
+/* The same over FP8 kv caches (both sources in the 584-byte row format of
+ * sa_sparse_attn_fwd_fp8), D = 512. */
+sa_status sa_sparse_attn_fwd_fp8_extra(const void *q, const uint8_t *kv_fp8, const float *attn_sink,
+                                       const int32_t *topk_idxs, const int32_t *topk_length,
+                                       const uint8_t *extra_kv_fp8, const int32_t *extra_topk_idxs,
+                                       const int32_t *extra_topk_length, float softmax_scale, void *o, int64_t B,
+                                       int64_t S, int64_t H, int64_t T, int64_t K, int64_t T2, int64_t K2,
+                                       int num_splits, void *workspace, size_t workspace_bytes,
+                                       sa_stream_t stream);
+
 /* Kernels one sa_sparse_attn_fwd_fp8 call enqueues (1 or 2); 0 on
  * unsupported sizes. */
 int sa_sparse_attn_fp8_launch_count(int64_t B, int64_t S, int64_t H, int64_t K, int num_splits);
@@ -327,11 +361,14 @@ size_t sa_topk_masked_attn_workspace_size(int64_t B, int64_t max_q_len, int64_t 
 /* diagnostics                                                              */
 /* ------------------------------------------------------------------------ */
 
-/* Every wait inside the kernels is bounded; a wait that runs out records a
- * nonzero code in a device-side word and the kernel returns early (its output
- * is then undefined).  This call synchronises the current device, returns
- * that word (0 = no failure since the last clear) and clears it if `clear`.
- * Returns -1 if the word cannot be read. */
+/* Every mbarrier wait inside the kernels is bounded (about 0.1 s of SM
+ * clock); a wait that runs out records a nonzero code in a device-side word
+ * and its kernel returns early (its output is then undefined).  Once the word
+ * is nonzero, every wait of every kernel on the device gives up within about
+ * 1024 polls, so a failing launch drains quickly; the word stays set (and
+ * later launches fail fast) until it is cleared here.  This call synchronises
+ * the current device, returns that word (0 = no failure since the last
+ * clear) and clears it if `clear`.  Returns -1 if the word cannot be read. */
 int sa_device_error(int clear);
 
 /* Self-test of that mechanism, without any fault: launches one warp that
@@ -343,6 +380,17 @@ int sa_device_error(int clear);
  * Any earlier code is cleared first.  The pages have no counterpart of this
  * call: it exists to test failure detection on a shared GPU. */
 int sa_selftest_wait_timeout(long long max_cycles);
+
+/* Self-test of the fast drain, without any fault: launches `ctas` CTAs
+ * (1 .. 1024) of one waiting warp each.  CTA 0 waits on a barrier phase that
+ * nothing completes with a limit of `first_cycles` (1 .. 2^28); every other
+ * CTA waits likewise with the kernels' full limit (~0.1 s), and must give up
+ * as soon as CTA 0 has recorded its timeout.  Writes the elapsed time of the
+ * launch in milliseconds (CUDA events) to *elapsed_ms, synchronises the
+ * current device and returns the recorded code (1 = timed out, expected),
+ * leaving the word clear; -1 on a bad argument or a CUDA error.  The pages
+ * have no counterpart of this call. */
+int sa_selftest_wait_drain(int ctas, long long first_cycles, float *elapsed_ms);
 
 #ifdef __cplusplus
 }

@@ -54,6 +54,10 @@ def test_selftest_validates_its_limit_on_the_host():
     # argument checks happen before any device work (no GPU needed)
     assert binding.sa_selftest_wait_timeout(0) == -1
     assert binding.sa_selftest_wait_timeout(-5) == -1
+    assert binding.sa_selftest_wait_drain(0, 1000)[0] == -1
+    assert binding.sa_selftest_wait_drain(1025, 1000)[0] == -1
+    assert binding.sa_selftest_wait_drain(4, 0)[0] == -1
+    assert binding.sa_selftest_wait_drain(4, 1 << 29)[0] == -1
 
 
 def test_status_strings():
@@ -223,3 +227,26 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         binding.load(build_if_missing=False)
+
+
+def test_extra_source_arguments_are_checked_on_the_host():
+    # argument checks happen before any device work (no GPU needed)
+    buf = ctypes.create_string_buffer(64)
+    base = ctypes.addressof(buf)
+    a16 = (base + 15) // 16 * 16
+    args = dict(q=a16, kv=a16, attn_sink=a16, topk_idxs=a16, topk_length=None, extra_kv=a16, extra_topk_idxs=a16,
+                extra_topk_length=None, softmax_scale=0.1, o=a16, B=1, S=1, H=8, D=64, T=4, K=2, T2=4, K2=2,
+                num_splits=0, workspace=None, workspace_bytes=0, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return binding.sa_status_string(binding.sa_sparse_attn_fwd_extra(*a.values()))
+
+    assert call(K2=-1) == "SA_ERR_INVALID_ARG"
+    assert call(K=0, K2=0) == "SA_ERR_SHAPE"
+    assert call(K2=3, T2=0) == "SA_ERR_SHAPE"
+    assert call(extra_kv=None) == "SA_ERR_INVALID_ARG"
+    assert call(extra_kv=a16 + 4) == "SA_ERR_ALIGNMENT"
+    assert call(extra_topk_idxs=a16 + 2) == "SA_ERR_ALIGNMENT"
+    assert call(B=1 << 20, T=1 << 11, T2=1 << 11) == "SA_ERR_SHAPE"

@@ -34,3 +34,15 @@ def test_context_stays_usable_after_a_timeout():
 def test_selftest_rejects_bad_limits():
     assert binding.sa_selftest_wait_timeout(0) == -1
     assert binding.sa_selftest_wait_timeout(1 << 29) == -1
+
+
+def test_one_timeout_drains_every_waiting_cta_quickly():
+    # CTA 0 gives up after ~1 ms; 511 other CTAs wait with the kernels' full
+    # limit (~0.1 s each) and must return as soon as CTA 0 has recorded its
+    # timeout, because every bounded wait also watches the error word
+    code, ms = binding.sa_selftest_wait_drain(512, 2_000_000)
+    assert code == WAIT_TIMED_OUT
+    assert ms < 40.0, f"drain took {ms:.1f} ms"
+    assert binding.sa_device_error(True) == 0
+    # and the context is still usable
+    test_context_stays_usable_after_a_timeout()
