@@ -1031,12 +1031,16 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                     break;
                 }
                 {
-                    uint8_t *ra = p_rows(sb) + g8 * 128 + qu * 4;
+                    // four stmatrix.x4, each the 8x8 blocks (rA, k), (rB, k),
+                    // (rA, k+1), (rB, k+1): lane 8i + j addresses row j of
+                    // block i, 16-byte chunk k (+1) of the swizzled row
+                    const int blk = lane >> 3, jr = lane & 7;
+                    const uint32_t row_base = ptx::smem_u32(p_rows(sb)) + uint32_t((blk & 1) * 1024 + jr * 128);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int c = (k ^ g8) * 16;
-                        *reinterpret_cast<uint32_t *>(ra + c) = pw[2 * k];
-                        *reinterpret_cast<uint32_t *>(ra + 1024 + c) = pw[2 * k + 1];
+                    for (int k = 0; k < 8; k += 2) {
+                        const int c = k + (blk >> 1);
+                        ptx::stmatrix_x4(row_base + uint32_t(((c ^ jr) & 7) << 4), pw[2 * k], pw[2 * k + 1],
+                                         pw[2 * k + 2], pw[2 * k + 3]);
                     }
                 }
                 if constexpr (CL == 2) {

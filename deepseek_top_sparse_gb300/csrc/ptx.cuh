@@ -186,6 +186,16 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Four 8x8 matrices of 16-bit values from registers to shared memory: for
+// matrix i, thread t holds row t/4, columns 2(t%4) and 2(t%4)+1 in r_i (low
+// half = the lower column), and thread 8i + j gives the address of row j
+// (16 contiguous bytes).
+__device__ __forceinline__ void stmatrix_x4(uint32_t row_addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(row_addr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // ------------------------------------------------------------- proxies
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
