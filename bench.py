@@ -484,14 +484,32 @@ def run_gpu(args):
             assert binding.sa_device_error(True) == 0
             dms = sum(d_ms) / len(d_ms)
             _, tf_m, _, _ = _peaks()
+            # the consumer's contraction: a dense masked attention computes
+            # QK^T and P.V for every key of a query up to its last admitted
+            # one (4 H D flops a key); compulsory HBM bytes: q, o, kv, mask
+            last = torch.where((tk >= 0) & (tk < Tm), tk, torch.full_like(tk, -1)).amax(dim=-1)
+            dense_keys = float((last + 1).clamp(min=0).sum())
+            fl_d = 4.0 * Hm * Dm * dense_keys
+            io_b = 2.0 * qm.numel() * 2 + kvm.numel() * 2 + mbuf.numel() * 4
+            sec_m = dms * 1e-3
+            roof_d = max(fl_d / (tf_m * 1e12), io_b / (hbm * 1e9))
+            d_bound = "tensor" if fl_d / (tf_m * 1e12) >= io_b / (hbm * 1e9) else "hbm"
+            # the sparse_attn formula (a gathered 2D-byte row per admitted pair)
             fl_m = 4.0 * Hm * Dm * admitted
             gb_m = float(admitted) * Dm * 2
             roof_m = max(fl_m / (tf_m * 1e12), gb_m / (hbm * 1e9))
             mask_obj["consumer"] = {
                 "op": "masked_dense_attn", "us_per_call": dms * 1e3,
-                "value": mi.batch * mi.max_q_len / (dms * 1e-3), "unit": UNIT,
-                "admitted_keys": admitted, "gathered_kv_gbs": gb_m / (dms * 1e-3) / 1e9,
-                "roofline_frac": roof_m / (dms * 1e-3), "bound": "hbm" if gb_m / hbm >= fl_m / tf_m / 1e3 else "tensor",
+                "value": mi.batch * mi.max_q_len / sec_m, "unit": UNIT,
+                "admitted_keys": admitted, "dense_keys": dense_keys,
+                "roofline": {"bound": d_bound, "achieved": fl_d / sec_m / 1e12 if d_bound == "tensor" else io_b / sec_m / 1e9,
+                             "peak": tf_m if d_bound == "tensor" else hbm,
+                             "unit": "TFLOP/s" if d_bound == "tensor" else "GB/s", "frac": roof_d / sec_m,
+                             "work": "dense QK^T and P.V up to each query's last admitted key (4*H*D flops a key); "
+                                     "HBM: q, o, kv and mask once"},
+                "pair_formula": {"gathered_kv_gbs": gb_m / sec_m / 1e9, "frac": roof_m / sec_m,
+                                 "note": "admitted pairs x D x 2 bytes against HBM, the sparse_attn formula; the dense "
+                                         "consumer reads each kv tile once per 128 / H packed queries, so this exceeds 1"},
                 "launches_per_call": binding.sa_masked_dense_attn_launch_count(mi.batch, mi.max_q_len, Hm, Dm, Tm),
                 "l2": "flushed between calls"}
 

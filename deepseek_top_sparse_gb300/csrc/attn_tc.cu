@@ -377,12 +377,13 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
     } else {
         // key t is admitted iff bit (t + key_start) & 31 of word
         // (t + key_start) >> 5 of the token's mask row is set; positions
-        // outside the row admit nothing
+        // outside the row, and with key_start_word the row's last word (the
+        // reserved key_start column), admit nothing
         const uint32_t *mrow = p.mask + (b * p.mask_rows + (tok - b * p.S)) * p.mask_words;
         const int64_t key_start =
             p.key_start_word ? int64_t(int32_t(__ldg(p.mask + b * p.mask_rows * p.mask_words + p.mask_words - 1)))
                              : 0;
-        const int64_t row_bits = p.mask_words * 32;
+        const int64_t row_bits = (p.mask_words - p.key_start_word) * 32;
         const int64_t key_end = p.key_ends != nullptr ? int64_t(__ldg(p.key_ends + b)) : row_bits;
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
@@ -1748,6 +1749,25 @@ cudaError_t launch_wait_drain_selftest(int ctas, long long first_cycles, cudaStr
     wait_drain_selftest_kernel<<<ctas, 32, 0, stream>>>(first_cycles);
     return cudaGetLastError();
 }
+
+cudaError_t device_error_word(int **ptr) {
+    static std::once_flag once[kMaxDev];
+    static int *addr[kMaxDev];
+    static cudaError_t err[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        void *a = nullptr;
+        err[dev] = cudaGetSymbolAddress(&a, g_device_error);
+        addr[dev] = static_cast<int *>(a);
+    });
+    *ptr = addr[dev];
+    return err[dev];
+}
+
+void *tensor_map_encode_fn() { return reinterpret_cast<void *>(tensor_map_encoder()); }
 
 cudaError_t read_device_error(int *value, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();

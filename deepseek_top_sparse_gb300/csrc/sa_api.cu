@@ -270,14 +270,36 @@ sa_status sa_sparse_attn_fwd(const void *q, const void *kv, const float *attn_si
                                      K, 0, workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+// Split count of the mask consumer: the packed kernel's plan for D <= 256,
+// sparse_attn's (the T keys playing the part of the K slots) for D = 512; 0
+// when the sizes cannot be planned.
+int masked_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int num_splits, int sms) {
+    if (sa::masked_dense_packed(D)) return sa::masked_dense_splits(B, S, H, D, T, num_splits, sms);
+    return clamp_splits(T, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, T, sms));
+}
+
+}  // namespace
+
 size_t sa_masked_dense_attn_workspace_size(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T,
                                            int num_splits) {
-    // the T keys of a token play the part of its K slots
-    return sa_sparse_attn_workspace_size(B, S, H, D, T, num_splits);
+    if (!attn_sizes_ok(B, S, H, D, T) || num_splits > 64) return 0;
+    DeviceInfo dev{};
+    if (num_splits <= 0 && current_device(&dev) != SA_OK) return 0;   // the plan needs the SM count
+    const int splits = masked_splits(B, S, H, D, T, num_splits, dev.sms);
+    return splits > 0 ? workspace_bytes_for(B, S, H, D, splits) : 0;
 }
 
 int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int num_splits) {
-    return sa_sparse_attn_launch_count(B, S, H, D, T, num_splits);
+    if (!attn_sizes_ok(B, S, H, D, T) || num_splits > 64) return 0;
+    if (B * S == 0) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev) != SA_OK) return 0;
+    const int splits = masked_splits(B, S, H, D, T, num_splits, dev.sms);
+    if (splits <= 0) return 0;
+    if (sa::masked_dense_packed(D)) return splits > 1 ? 2 : 1;
+    return sa::kernels_per_call(D, splits);
 }
 
 namespace {
@@ -300,7 +322,7 @@ sa_status masked_window(const void *q, const void *kv, const float *attn_sink, c
     if (num_splits > 64 || (key_start_word != 0 && key_start_word != 1)) return SA_ERR_INVALID_ARG;
     if (!attn_sizes_ok(B, S, H, D, T) || T < 1) return SA_ERR_SHAPE;
     if (q0 + S > S_total) return SA_ERR_SHAPE;
-    if (B * T >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
+    if (B * T + 256 >= (int64_t(1) << 31)) return SA_ERR_SHAPE;   // 32-bit key-tile coordinates
     if (B * S_total * H >= (int64_t(1) << 31)) return SA_ERR_SHAPE;
     if (mask_rows < S || mask_words < 1 || (mask_words & 3)) return SA_ERR_SHAPE;
     if (B * S == 0) return SA_OK;
@@ -312,7 +334,8 @@ sa_status masked_window(const void *q, const void *kv, const float *attn_sink, c
     const sa_status st = current_device(&dev);
     if (st != SA_OK) return st;
 
-    const int splits = clamp_splits(T, num_splits > 0 ? num_splits : plan_splits(B, S, H, D, T, dev.sms));
+    const int splits = masked_splits(B, S, H, D, T, num_splits, dev.sms);
+    if (splits <= 0) return SA_ERR_SHAPE;
     const size_t need = workspace_bytes_for(B, S, H, D, splits);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SA_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255)) return SA_ERR_ALIGNMENT;
@@ -327,9 +350,10 @@ sa_status masked_window(const void *q, const void *kv, const float *attn_sink, c
     a.mask = mask; a.mask_rows = mask_rows; a.mask_words = mask_words; a.key_start_word = key_start_word;
     a.key_ends = key_ends;
     carve_workspace(a, workspace, B * S, H, D, splits);
-    if (sa::launch_sparse_attn(a, dev.sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SA_ERR_CUDA;
-    return SA_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = sa::masked_dense_packed(D) ? sa::launch_masked_dense(a, cs)
+                                                     : sa::launch_sparse_attn(a, dev.sms, cs);
+    return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 }  // namespace

@@ -19,6 +19,12 @@ enum DeviceError : int {
 // The device error word lives in attn_tc.cu; every kernel that can fail
 // records into it with atomicCAS(0 -> code) so the first failure sticks.
 cudaError_t read_device_error(int *value, bool clear);
+// Device address of the error word on the current device (for kernels of the
+// other translation units, which record into the same word).
+cudaError_t device_error_word(int **ptr);
+// cuTensorMapEncodeTiled from the driver (nullptr when unavailable), as a
+// PFN_cuTensorMapEncodeTiled_v12000.
+void *tensor_map_encode_fn();
 cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream);
 cudaError_t launch_wait_drain_selftest(int ctas, long long first_cycles, cudaStream_t stream);
 
@@ -63,6 +69,16 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream);
 // Kernels one sparse_attn call enqueues on the current device: 1, or 2 when
 // the splits are too many to combine inside the main kernel (0 on error).
 int kernels_per_call(int64_t D, int num_splits, bool kv_fp8 = false);
+
+// The packed consumer of the mask (D = 64, 128 or 256): G = 128 / H query
+// tokens share the 128 MMA rows of a work unit, key tiles are dense.
+bool masked_dense_packed(int64_t D);
+// Its split count for these sizes (num_splits <= 0: planned), 0 when the key
+// range cannot be split into at most 64 units.
+int masked_dense_splits(int64_t B, int64_t S, int64_t H, int64_t D, int64_t T, int num_splits, int num_sms);
+// The packed consumer, then the combine kernel when a.num_splits > 1 (the
+// workspace layout of the sparse_attn splits).
+cudaError_t launch_masked_dense(const AttnArgs &a, cudaStream_t stream);
 
 struct MaskArgs {
     const int32_t *topk;

@@ -29,9 +29,14 @@
 
 namespace {
 
-// 32 MiB: enough for the library's own split plan at any batch size on a
-// 152-SM GPU with H <= 128 and D <= 512 (the plan never uses more CTAs than
-// SMs, which bounds splits x tokens x H x D x 4 bytes to about 20 MB).
+// 32 MiB.  With the library's own split plan (num_splits = 0) and K <= 2048
+// slots (one work unit per split) a split call never runs more units than
+// the GPU has CTA slots, one per SM (half of them for D = 512), so on a
+// 152-SM GB300 the partials take at most 152 x 128 x 256 x 4 bytes, about
+// 20 MB, for H <= 128.  Larger K forces at least ceil(K / 2048) splits per
+// token whatever the batch, and an explicit num_splits can ask for up to
+// 64: such plans can exceed the array, and the call then returns
+// SA_ERR_WORKSPACE.
 constexpr size_t kStaticWsBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
@@ -49,20 +54,15 @@ extern "C" sa_status sa_sparse_attn_fwd_static_ws(const void *q, const void *kv,
                                                  int64_t K, int num_splits, sa_stream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SA_ERR_CUDA;
-    // Workspace this call needs under the library's split plan (0 when the
-    // plan makes no split, or when the sizes are invalid -- then the regular
-    // validation below reports them); reject anything the array cannot hold.
-    const size_t need = sa_sparse_attn_workspace_size(B, S, H, D, K, num_splits);
-    if (need > kStaticWsBytes) return SA_ERR_WORKSPACE;
-    if (need == 0)
-        return sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
-                                         num_splits, nullptr, 0, stream);
     std::call_once(g_ws_once[dev], [dev] {
         void *p = nullptr;
         g_ws_err[dev] = cudaGetSymbolAddress(&p, g_static_ws);
         g_ws_ptr[dev] = p;
     });
     if (g_ws_err[dev] != cudaSuccess || g_ws_ptr[dev] == nullptr) return SA_ERR_CUDA;
+    // The regular entry point validates every argument first (so an invalid
+    // argument is reported as such), then compares the planned workspace with
+    // the array's size.
     return sa_sparse_attn_fwd_splits(q, kv, attn_sink, topk_idxs, softmax_scale, o, B, S, H, D, T, K,
                                      num_splits, g_ws_ptr[dev], kStaticWsBytes, stream);
 }

@@ -279,9 +279,16 @@ int sa_masked_dense_attn_launch_count(int64_t B, int64_t S, int64_t H, int64_t D
  *               ks_b = (int32) mask[b, 0, mask_words - 1], the reserved word
  *               sa_build_topk_mask writes (T keys of a context chunk that
  *               starts at absolute position ks_b).
- * Key t of request b is admitted iff 0 <= p < 32 * mask_words and bit p & 31
- * of word p >> 5 of the row is set, p = t (+ ks_b); the result is then
- * sa_sparse_attn_fwd's with the admitted keys as the token's slot list.
+ * Key t of request b is admitted iff 0 <= p < 32 * (mask_words -
+ * key_start_word) and bit p & 31 of word p >> 5 of the row is set, p = t
+ * (+ ks_b): with key_start_word the last word of every row is the reserved
+ * column and admits nothing.  Padding words past the builder's live words
+ * are read as key bits if p reaches them (T + ks_b past the max_key_len the
+ * mask was built for); the window form's key_ends bounds them.  The result
+ * is sa_sparse_attn_fwd's with the admitted keys as the token's slot list.
+ * kv must hold finite values: for D <= 256 the G = 128 / H query tokens of
+ * a group share dense key tiles, and the keys a row does not admit enter
+ * its P.V with weight 0.
  * num_splits: 1..64 key ranges per token (<= 0: planned); workspace as in
  * sa_sparse_attn_fwd_splits, sized by sa_masked_dense_attn_workspace_size.
  * Errors as sa_sparse_attn_fwd_splits, plus SA_ERR_SHAPE for mask_rows < S,

@@ -45,7 +45,8 @@
  *   R16 the reserved word of row 0 holds the raw bits of key_starts[b].
  *   R19 a per-token topk_length keeps only the slots j < clamp(len, 0, K).
  *   R21 the mask consumer admits key t iff bit t (+ key_start) of the row is
- *       set, within the row's 32 * W positions.
+ *       set, within the row's 32 * W positions; in the offset form the last
+ *       word of a row is the reserved key_start column and admits nothing.
  *   R22 FP8 row byte order: 448 E4M3 codes, 64 bf16 RoPE dims, 8 E8M0 scales.
  *   R24 a mask window holds query rows q0.. of each request; a live key end
  *       bounds both the words written and the keys the consumer admits.
@@ -386,7 +387,9 @@ int oracle_sparse_attn(const uint16_t *q, const uint16_t *kv, const float *attn_
 /* ((t + key_offset[b]) & 31) of word ((t + key_offset[b]) >> 5) in row      */
 /* mask[b, s, :] is set.  Same softmax-with-sink as above over the admitted  */
 /* keys.  key_offset may be NULL (all zero, `dense_mask_mod`); a non-NULL    */
-/* offset is the chunked-context reading (`offset_dense_mask_mod`).          */
+/* offset is the chunked-context reading (`offset_dense_mask_mod`), whose    */
+/* key start sits in the last word of row 0 (R16): with an offset, the last  */
+/* word of every row is that reserved column, never a key word (R21).        */
 /* key_ends (or NULL): a key at or past request b's live end key_ends[b]     */
 /* (in mask positions, i.e. after the offset) is never admitted (R24).       */
 /* ------------------------------------------------------------------------ */
@@ -399,6 +402,7 @@ int oracle_masked_dense_attn(const uint16_t *q, const uint16_t *kv, const float 
     double *logit = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     for (int64_t b = 0; b < B; ++b) {
         const int64_t off = key_offset ? key_offset[b] : 0;
+        const int64_t key_words = key_offset ? mask_words - 1 : mask_words;
         for (int64_t s = 0; s < S; ++s) {
             const uint32_t *row = mask + (b * mask_rows + s) * mask_words;
             for (int64_t h = 0; h < H; ++h) {
@@ -407,7 +411,7 @@ int oracle_masked_dense_attn(const uint16_t *q, const uint16_t *kv, const float 
                 const uint16_t *qh = q + ((b * S + s) * H + h) * D;
                 for (int64_t t = 0; t < T; ++t) {
                     int64_t key = t + off;
-                    int on = key >= 0 && (key >> 5) < mask_words &&
+                    int on = key >= 0 && (key >> 5) < key_words &&
                              (key_ends == NULL || key < key_ends[b]) &&
                              ((row[key >> 5] >> (key & 31)) & 1u);
                     if (!on) {

@@ -156,7 +156,7 @@ def test_masked_dense_entry_validates_before_any_device_work():
     assert f(**dict(base, mask=8)) == 3               # mask not 16-byte aligned
     assert f(**dict(base, q=24)) == 3
     assert f(**dict(base, B=0)) == 0
-    # the T keys of a token are split like K slots
+    # an explicit split count gives sparse_attn's workspace layout for that many splits
     assert binding.sa_masked_dense_attn_workspace_size(2, 3, 8, 64, 256, 2) == \
         binding.sa_sparse_attn_workspace_size(2, 3, 8, 64, 256, 2)
     assert binding.sa_masked_dense_attn_workspace_size(1, 1, 8, 96, 256, 2) == 0

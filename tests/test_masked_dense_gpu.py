@@ -71,6 +71,26 @@ def test_random_masks(B, S, H, D, T, density, splits):
     assert_close(o, oracle.masked_dense_attn(q, kv, sink, mask, scale), f"B{B} S{S} H{H} D{D} T{T}")
 
 
+@pytest.mark.parametrize("B,S,H,D,T,density,splits", [
+    (3, 37, 8, 64, 1000, 0.25, 0),     # 16 tokens a unit, ragged last group, 3 requests
+    (2, 11, 3, 64, 513, 0.3, 0),       # H = 3: 42 tokens on 126 of the 128 rows
+    (2, 9, 24, 128, 700, 0.2, 2),      # 5 tokens of 24 heads, 2 key splits
+    (1, 6, 1, 256, 2000, 0.1, 0),      # one head: 128 tokens a unit, 6 of them live
+    (2, 5, 128, 128, 450, 0.5, 0),     # one token a unit
+    (1, 40, 16, 64, 130, 1.0, 0),      # every key admitted, the last tile holds 2 keys
+    (2, 33, 8, 64, 3000, 0.002, 0),    # most key tiles admit nothing and are skipped
+])
+def test_packed_query_groups(B, S, H, D, T, density, splits):
+    # the consumer for D <= 256 packs 128 / H query tokens into one unit's
+    # MMA rows; groups straddle neither requests nor the window
+    q, kv, sink = _inputs(B, S, H, D, T, seed=7 * S + H)
+    words = workloads.ceil_div(workloads.ceil_div(T, 32), 4) * 4
+    mask = _random_mask(B, S + 3, words, density, seed=S + T)
+    scale = D ** -0.5
+    o = _gpu(q, kv, sink, mask, scale, num_splits=splits)
+    assert_close(o, oracle.masked_dense_attn(q, kv, sink, mask, scale), f"B{B} S{S} H{H} D{D} T{T}")
+
+
 def test_split_count_does_not_change_the_result():
     q, kv, sink = _inputs(1, 4, 128, 512, 3000, seed=5)
     mask = _random_mask(1, 4, 96, 0.3, seed=6)
@@ -117,6 +137,19 @@ def test_key_start_word_offsets_the_bit_test(key_starts):
     o = _gpu(q, kv, sink, mask, D ** -0.5, key_start_word=True)
     want = oracle.masked_dense_attn(q, kv, sink, mask, D ** -0.5, key_offset=list(key_starts))
     assert_close(o, want, f"key_starts={key_starts}")
+
+
+def test_reserved_word_is_never_a_key_bit():
+    # key_start = -1 fills the reserved word of row 0 with ones; the chunk's
+    # keys reach its positions, and the consumer must admit none of them
+    B, S, H, D, T = 1, 3, 8, 64, 300
+    q, kv, sink = _inputs(B, S, H, D, T, seed=17)
+    rng = np.random.default_rng(18)
+    topk = rng.integers(-2, 200, size=(S, 70)).astype(np.int32)
+    mask = oracle.build_topk_mask(topk, np.array([0, S], np.int32), B, S, 200, key_starts=np.array([-1], np.int32))
+    assert mask[0, 0, -1] == 0xFFFFFFFF and 32 * (mask.shape[2] - 1) < T - 1
+    o = _gpu(q, kv, sink, mask, D ** -0.5, key_start_word=True)
+    assert_close(o, oracle.masked_dense_attn(q, kv, sink, mask, D ** -0.5, key_offset=[-1]), "reserved word")
 
 
 def test_zero_and_negative_scale():

@@ -300,6 +300,23 @@ def test_masked_dense_key_offset_reads_absolute_positions():
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
 
 
+def test_masked_dense_offset_form_never_reads_the_reserved_word():
+    # key_starts = -1 puts 0xFFFFFFFF into the reserved last word of row 0;
+    # a chunk of 128 keys at position -1 reaches mask positions 96..126 of
+    # that word.  The offset form admits exactly the row's indices shifted by
+    # the start: sparse attention over idx + 1, nothing from the reserved word.
+    inp = workloads.random_attn(1, 2, 2, 8, 128, 20, p_invalid=0.1, seed=41)
+    idx = inp.topk_idxs.clone()
+    idx[idx >= 64] = -1                          # the mask covers 64 keys
+    m = oracle.build_topk_mask(idx.reshape(2, -1).numpy(), np.array([0, 2], np.int32), 1, 2, 64,
+                               key_starts=np.array([-1], np.int32))
+    assert m.shape == (1, 128, 4) and m[0, 0, 3] == 0xFFFFFFFF
+    got = oracle.masked_dense_attn(inp.q, inp.kv, inp.attn_sink, m, inp.softmax_scale, key_offset=[-1])
+    shifted = torch.where(idx >= 0, idx + 1, idx)
+    want = oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, shifted, inp.softmax_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
 def test_tiny_workload_shape_and_structure():
     inp = workloads.tiny()
     assert inp.shape == dict(B=1, S=4, H=8, D=64, T=256, K=64)

@@ -70,3 +70,44 @@ def test_static_workspace_rejects_plans_larger_than_the_array():
                                               d.topk_idxs.data_ptr(), d.softmax_scale, d.q.data_ptr(), B, S, H, D,
                                               4096, 4096, 64, torch.cuda.current_stream().cuda_stream)
     assert binding.sa_status_string(rc) == "SA_ERR_WORKSPACE"
+
+
+def test_static_workspace_reports_invalid_arguments_before_the_size_check():
+    # num_splits above 64 is an invalid argument, also when the plan it asks
+    # for would not fit the array
+    d = workloads.random_attn(16, 8, 128, 512, 4096, 4096, p_invalid=0.0, seed=3).to("cuda")
+    B, S, H, D = d.q.shape
+    stream = torch.cuda.current_stream().cuda_stream
+    for ns in (65, 1000):
+        rc = binding.sa_sparse_attn_fwd_static_ws(d.q.data_ptr(), d.kv.data_ptr(), d.attn_sink.data_ptr(),
+                                                  d.topk_idxs.data_ptr(), d.softmax_scale, d.q.data_ptr(), B, S,
+                                                  H, D, 4096, 4096, ns, stream)
+        assert binding.sa_status_string(rc) == "SA_ERR_INVALID_ARG"
+    rc = binding.sa_sparse_attn_fwd_static_ws(d.q.data_ptr(), d.kv.data_ptr(), d.attn_sink.data_ptr(),
+                                              d.topk_idxs.data_ptr(), float("nan"), d.q.data_ptr(), B, S, H, D,
+                                              4096, 4096, 64, stream)
+    assert binding.sa_status_string(rc) == "SA_ERR_INVALID_ARG"
+
+
+def test_static_workspace_with_more_than_2048_slots():
+    # K > 2048 forces ceil(K / 2048) splits whatever the batch: 64 tokens x 2
+    # splits x 128 x 512 x 4 bytes exceed the array, 16 tokens fit and match
+    # the regular entry point
+    stream = torch.cuda.current_stream().cuda_stream
+    big = workloads.random_attn(64, 1, 128, 512, 3000, 2560, p_invalid=0.1, seed=11).to("cuda")
+    B, S, H, D = big.q.shape
+    assert binding.sa_sparse_attn_workspace_size(B, S, H, D, 2560, 0) > (32 << 20)
+    out = torch.full_like(big.q, float("nan"))
+    rc = binding.sa_sparse_attn_fwd_static_ws(big.q.data_ptr(), big.kv.data_ptr(), big.attn_sink.data_ptr(),
+                                              big.topk_idxs.data_ptr(), big.softmax_scale, out.data_ptr(), B, S, H,
+                                              D, 3000, 2560, 0, stream)
+    assert binding.sa_status_string(rc) == "SA_ERR_WORKSPACE"
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all(), "a rejected call writes no output"
+    small = workloads.random_attn(16, 1, 128, 512, 3000, 2560, p_invalid=0.1, seed=12).to("cuda")
+    assert binding.sa_sparse_attn_workspace_size(16, 1, 128, 512, 2560, 0) <= (32 << 20)
+    ref = _regular(small, 0)
+    got = _static(small, 0)
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    _close(got, ref)
