@@ -1167,7 +1167,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
     //     own granules: its weighted O plus the other splits' from L2.
     ptx::tc_fence_before();
     __syncthreads();
-    if (p.fused) ptx::cluster_sync();   // every split's log-sum-exp is in the table
     ptx::tc_fence_after();
     {
         constexpr int CW = DC / 4;                        // columns of a warp's slice
@@ -1266,6 +1265,42 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 ptx::bulk_wait_read_all();
             }
         } else {
+            // Right after its last P.V this split stores the granules other
+            // splits finish, as O / l (0 for an empty split), while slower
+            // CTAs of the cluster are still in their main loops; one cluster
+            // barrier then covers those stores and every split's
+            // log-sum-exp in the tables, and the weights are applied on receipt.
+            const int gs0 = split * NG / ns, gs1 = (split + 1) * NG / ns;   // this split's granules
+            const bool mine = gran >= gs0 && gran < gs1;
+            const float inv_l = (n_act > 0 && st.y > 0.f) ? 1.f / st.y : 0.f;
+            if (!mine) {
+#pragma unroll 1
+                for (int cc = 0; cc < CW / CC; ++cc) {
+                    float x[CC];
+                    load_chunk(cc, x);
+                    if (rv) stage_f32(0, c_slice + cc * CC, x, inv_l);
+                }
+            }
+            publish();
+            if (tid == 0) {
+                for (int k = 0; k < 2 * NG; ++k)
+                    if (k / 2 < gs0 || k / 2 >= gs1)
+                        ptx::tma_store_2d(&wmap, sbase + k * BOX, int32_t(crank) * DC + 32 * k, y_ws);
+                ptx::bulk_commit();
+                ptx::bulk_wait_all();              // written, not just read
+                ptx::fence_proxy_async_global();   // async-proxy writes before the barrier's release
+            }
+            float acc[CW];
+            if (mine) {
+#pragma unroll
+                for (int cc = 0; cc < CW / CC; ++cc) {
+                    float x[CC];
+                    load_chunk(cc, x);
+#pragma unroll
+                    for (int i2 = 0; i2 < CC; ++i2) acc[cc * CC + i2] = x[i2] * inv_l;
+                }
+            }
+            ptx::cluster_sync();   // every split's partials in the workspace, its log-sum-exp in the tables
             // final weight of every split for row hr (the combine kernel's formula)
             const float *tab = reinterpret_cast<const float *>(smem + C::OFF_LSE);   // [split][row]
             float mx = -INFINITY;
@@ -1281,45 +1316,21 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 den += exp2f(sink2 - M);
             }
             const float fn = isnan(sink2) ? NAN : 1.f;
-            const float lo = tab[split * kM + hr];
-            // this split's O, weighted: w_s / l_s (0 for an empty split)
-            const float g = (zero || lo == -INFINITY) ? 0.f * fn : exp2f(lo - M) / den / st.y * fn;
-            const int gs0 = split * NG / ns, gs1 = (split + 1) * NG / ns;   // this split's granules
-            const bool mine = gran >= gs0 && gran < gs1;
-            if (!mine) {
-#pragma unroll 1
-                for (int cc = 0; cc < CW / CC; ++cc) {
-                    float x[CC];
-                    load_chunk(cc, x);
-                    if (rv) stage_f32(0, c_slice + cc * CC, x, g);
-                }
+            auto weight = [&](int t) {   // w_t / den (0 for an empty split)
+                const float lt = tab[t * kM + hr];
+                return (zero || lt == -INFINITY) ? 0.f : exp2f(lt - M) / den;
+            };
+            if (mine) {
+                const float w_own = weight(split);
+#pragma unroll
+                for (int i2 = 0; i2 < CW; ++i2) acc[i2] *= w_own;
             }
-            publish();
-            if (tid == 0) {
-                for (int k = 0; k < 2 * NG; ++k)
-                    if (k / 2 < gs0 || k / 2 >= gs1)
-                        ptx::tma_store_2d(&wmap, sbase + k * BOX, int32_t(crank) * DC + 32 * k, y_ws);
-                ptx::bulk_commit();
-                ptx::bulk_wait_all();              // written, not just read
-                ptx::fence_proxy_async_global();   // async-proxy writes before the barrier's release
-            }
-            ptx::cluster_sync();   // every split's weighted granules are in the workspace
-            // the other splits' weighted partials of this split's granules, a
-            // round of as many splits as the receive area holds at a time,
-            // added to this split's own
+            // the other splits' partials of this split's granules, a round of
+            // as many splits as the receive area holds at a time, added to
+            // this split's own with their weights
             const int nsub = 2 * (gs1 - gs0);                                // 32-column boxes per split
             const int hbase = (C::OFF_STAT - NG * BOX) / 1024 * 1024;          // bf16 staging, above the receive area
             const int per_round = nsub > 0 ? hbase / (nsub * BOX) : 1;
-            float acc[CW];
-            if (mine) {
-#pragma unroll
-                for (int cc = 0; cc < CW / CC; ++cc) {
-                    float x[CC];
-                    load_chunk(cc, x);
-#pragma unroll
-                    for (int i2 = 0; i2 < CC; ++i2) acc[cc * CC + i2] = x[i2] * g;
-                }
-            }
             bool rok = true;
             int done = 0, round = 0;
             while (nsub > 0 && done < ns - 1) {
@@ -1337,16 +1348,18 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 rok = rok && wait_all(rcv_bar, uint32_t(round) & 1u);
                 if (mine && rok) {
                     for (int t2 = 0; t2 < cnt; ++t2) {
+                        const int oth = done + t2 < split ? done + t2 : done + t2 + 1;
+                        const float wt = weight(oth);
 #pragma unroll
                         for (int v2 = 0; v2 < CW / 4; ++v2) {
                             const int c = c_slice + 4 * v2;                     // column of this CTA
                             const int k = (c - 64 * gs0) / 32;                  // box among this split's
                             const float4 w4 = *reinterpret_cast<const float4 *>(
                                 smem + (t2 * nsub + k) * BOX + hr * 128 + (((((c % 32) / 4) ^ hr) & 7) << 4));
-                            acc[4 * v2] += w4.x;
-                            acc[4 * v2 + 1] += w4.y;
-                            acc[4 * v2 + 2] += w4.z;
-                            acc[4 * v2 + 3] += w4.w;
+                            acc[4 * v2] = fmaf(wt, w4.x, acc[4 * v2]);
+                            acc[4 * v2 + 1] = fmaf(wt, w4.y, acc[4 * v2 + 1]);
+                            acc[4 * v2 + 2] = fmaf(wt, w4.z, acc[4 * v2 + 2]);
+                            acc[4 * v2 + 3] = fmaf(wt, w4.w, acc[4 * v2 + 3]);
                         }
                     }
                 }
@@ -1360,7 +1373,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 for (int cc = 0; cc < CW / CC; ++cc) {
                     float x[CC];
 #pragma unroll
-                    for (int i2 = 0; i2 < CC; ++i2) x[i2] = rok ? acc[cc * CC + i2] : NAN;
+                    for (int i2 = 0; i2 < CC; ++i2) x[i2] = rok ? acc[cc * CC + i2] * fn : NAN;
                     stage_bf16(hbase, c_slice + cc * CC, x, 1.f);
                 }
             }
