@@ -145,6 +145,7 @@ KERNEL_SOURCES = ["deepseek_top_sparse_gb300/csrc/attn_tc.cu", "deepseek_top_spa
 
 
 MASK_SOURCES = ["deepseek_top_sparse_gb300/csrc/mask_build.cu"]
+CONSUMER_SOURCES = ["deepseek_top_sparse_gb300/csrc/masked_dense.cu", "deepseek_top_sparse_gb300/csrc/ptx.cuh"]
 
 
 def _attn_kernel_sources():
@@ -506,7 +507,8 @@ def run_gpu(args):
                              "peak": tf_m if d_bound == "tensor" else hbm,
                              "unit": "TFLOP/s" if d_bound == "tensor" else "GB/s", "frac": roof_d / sec_m,
                              "work": "dense QK^T and P.V up to each query's last admitted key (4*H*D flops a key); "
-                                     "HBM: q, o, kv and mask once"},
+                                     "HBM: q, o, kv and mask once",
+                             "traffic": _profile_traffic("masked_dense", _source_hash(CONSUMER_SOURCES))},
                 "pair_formula": {"gathered_kv_gbs": gb_m / sec_m / 1e9, "frac": roof_m / sec_m,
                                  "note": "admitted pairs x D x 2 bytes against HBM, the sparse_attn formula; the dense "
                                          "consumer reads each kv tile once per 128 / H packed queries, so this exceeds 1"},
