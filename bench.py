@@ -152,9 +152,11 @@ def _attn_kernel_sources():
     return [p for p in KERNEL_SOURCES if os.path.exists(os.path.join(ROOT, p))]
 
 
-def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None):
+def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None, spread: bool = False):
     """Time the oracle (as it stands) on whole tokens of the workload until
-    about budget_s of wall time; returns (tokens/s, tokens, seconds, threads)."""
+    about budget_s of wall time; returns (tokens/s, tokens, seconds, threads).
+    spread: take the tokens in a scattered order over the whole batch (a
+    multiplicative hash of the position) instead of from its start."""
     import numpy as np
 
     import oracle
@@ -165,7 +167,8 @@ def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None):
     done, elapsed, start_tok = 0, 0.0, 0
     chunk = max(1, min(ntok, threads, max_tokens or ntok))
     while done == 0 or (elapsed < budget_s and (max_tokens is None or done < max_tokens)):
-        tok = np.arange(start_tok, start_tok + chunk, dtype=np.int64) % ntok
+        tok = np.arange(start_tok, start_tok + chunk, dtype=np.int64)
+        tok = (tok * 2654435761) % ntok if spread else tok % ntok
         t0 = time.perf_counter()
         oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, tokens=tok,
                            nthreads=threads)
@@ -297,6 +300,20 @@ def run_gpu(args):
         e_ms.append(a.elapsed_time(b))
     e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), device=dev)
 
+    # ---- the same call's median over 200 cold calls (the line's value stays
+    # the mean of exactly the K timed steps)
+    med_ms = []
+    for _ in range(200):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        med_ms.append(a.elapsed_time(b))
+    assert binding.sa_device_error(True) == 0
+    ms_med = max_over_ranks(statistics.median(med_ms), device=dev)
+
     # ---- the same decode call, hot L2, through a captured CUDA graph of 100
     # calls (launch overhead amortised)
     hot_obj = None
@@ -368,6 +385,49 @@ def run_gpu(args):
                            "compute_frac": fl / (tf_o * 1e12) / (ms_o * 1e-3),
                            "l2": "flushed between calls"}
             assert binding.sa_device_error(True) == 0
+            if name == "v4_prefill":
+                # the prefill's own CPU baseline (tokens scattered over the
+                # sequence: early tokens hold fewer valid slots) and its end to
+                # end time: q and indices in from pinned host memory, o out
+                cv, cn, csec, cth = cpu_oracle_time(wc, min(args.cpu_budget, 6.0), spread=True)
+                other[name]["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
+                                               "sample": f"{cn} query tokens x 128 heads scattered over the "
+                                                         f"4096-token prefill, {csec:.1f} s"}
+                q_b = wc.q.numel() * 2
+                i_off = (q_b + 255) // 256 * 256
+                st_b = i_off + wc.topk_idxs.numel() * 4
+                st_h = torch.empty(st_b, dtype=torch.uint8).pin_memory()
+                st_h[:q_b].copy_(wc.q.contiguous().view(torch.uint8).reshape(-1))
+                st_h[i_off:].copy_(wc.topk_idxs.contiguous().view(torch.uint8).reshape(-1))
+                st_d = torch.empty(st_b, dtype=torch.uint8, device=dev)
+                qp = st_d[:q_b].view(torch.bfloat16).view(wc.q.shape)
+                ip = st_d[i_off:].view(torch.int32).view(wc.topk_idxs.shape)
+                oh = torch.empty(wc.q.shape, dtype=torch.bfloat16).pin_memory()
+
+                def pe2e():
+                    st_d.copy_(st_h, non_blocking=True)
+                    binding.sparse_attn(qp, wd.kv, wd.attn_sink, ip, wd.softmax_scale, out=outo, workspace=wso)
+                    oh.copy_(outo, non_blocking=True)
+
+                for _ in range(2):
+                    flush.zero_()
+                    pe2e()
+                torch.cuda.synchronize()
+                te = []
+                for _ in range(4):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    pe2e()
+                    b.record(stream)
+                    b.synchronize()
+                    te.append(a.elapsed_time(b))
+                assert binding.sa_device_error(True) == 0
+                ems = sum(te) / len(te)
+                other[name]["e2e"] = {"value": Bo * So / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": st_b,
+                                      "d2h_bytes_per_step": outo.numel() * 2,
+                                      "note": "kv resident; q and indices in as one pinned buffer, o out, each step"}
+                del st_h, st_d, oh
 
     # ---- the ratio-4 decode over an FP8 kv cache (584-byte rows), cold L2
     if rank == 0 and not args.no_extra:
@@ -549,6 +609,8 @@ def run_gpu(args):
                 "h2d_bytes_per_step": stage_bytes,
                 "d2h_bytes_per_step": out.numel() * 2,
                 "note": "kv cache resident in HBM; q and indices copied in as one pinned buffer, o copied out, each step"},
+        "median_200": {"ms_per_call": ms_med, "value": tokens * ws / (ms_med * 1e-3),
+                       "note": "median of 200 further cold calls, each between L2 flushes"},
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_loop": wall,
         "mask_build": mask_obj,
