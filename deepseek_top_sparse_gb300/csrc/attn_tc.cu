@@ -385,12 +385,27 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                              : 0;
         const int64_t row_bits = (p.mask_words - p.key_start_word) * 32;
         const int64_t key_end = p.key_ends != nullptr ? int64_t(__ldg(p.key_ends + b)) : row_bits;
+        // The unit's mask words (at most 65) read as whole 16-byte vectors of
+        // the row and staged in kv stage 0, which the gather fills only after
+        // the prologue: vectors w_lo, w_lo + 4, ... cover positions
+        // [slot0 + key_start, + nslots); vectors outside the row read as 0.
+        uint32_t *mw = reinterpret_cast<uint32_t *>(smem + C::OFF_KV);
+        const int64_t p_lo = slot0 + key_start;
+        const int64_t w_lo = (p_lo >> 5) & ~int64_t(3);
+        const int nvec = nslots > 0 ? int((((p_lo + nslots - 1) >> 5) - w_lo) / 4 + 1) : 0;
+        if (tid < nvec) {
+            const int64_t w = w_lo + 4 * tid;
+            const uint4 v = (w >= 0 && w + 4 <= p.mask_words) ? __ldg(reinterpret_cast<const uint4 *>(mrow + w))
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4 *>(mw)[tid] = v;
+        }
+        __syncthreads();
 #pragma unroll
         for (int u = 0; u < kSteps; ++u) {
             const int j = (u * kWarpsAll + warp) * 32 + lane;
             const int64_t key = slot0 + j + key_start;
             const bool on = j < nslots && key >= 0 && key < row_bits && key < key_end &&
-                            ((__ldg(mrow + (key >> 5)) >> (key & 31)) & 1u);
+                            ((mw[(key >> 5) - w_lo] >> (key & 31)) & 1u);
             tv[u] = on ? int32_t(slot0 + j) : -1;
         }
     }
