@@ -394,11 +394,25 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
 
         // the row's mask bits for key tile t: bit c of word k admits key
         // t * BN + 32k + c (mask position p0 + 32k + c, p0 = t * BN + ks)
+        // fast path (a tile whose positions start on a multiple of BN and lie
+        // inside the row's admissible range and the T keys): one aligned
+        // NW-word vector load, no shifts and no clipping
+        const bool aligned_ks = (ks % BN) == 0;
         auto tile_bits = [&](int t, uint32_t (&w)[NW]) {
 #pragma unroll
             for (int k = 0; k < NW; ++k) w[k] = 0u;
             if (t < 0 || mrow == nullptr) return;
             const int64_t p0 = int64_t(t) * BN + ks;
+            if (aligned_ks && p0 >= 0 && p0 + BN <= plim && int64_t(t + 1) * BN <= p.T) {
+                if constexpr (NW == 4) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(mrow + (p0 >> 5)));
+                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                } else {
+                    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(mrow + (p0 >> 5)));
+                    w[0] = v.x; w[1] = v.y;
+                }
+                return;
+            }
             const int64_t w0 = p0 >> 5;                 // floor
             const uint32_t sh = uint32_t(p0 & 31);
             const int64_t ca = w0 & ~int64_t(3);
