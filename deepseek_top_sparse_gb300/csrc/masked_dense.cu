@@ -97,7 +97,7 @@ struct MdParams {
     int *err;                   // the library's device error word
     int64_t mask_rows, W, T;
     int key_start_word;
-    int S, io_S, io_s0, H, G, groups, ns, tps, nt;
+    int B, S, io_S, io_s0, H, G, groups, ns, tps, nt;
     float scale_log2;
 };
 
@@ -215,12 +215,14 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
 
-    // ---- the unit
+    // ---- the unit.  Groups launch last-first (the requests interleaved):
+    // later queries usually see more keys, and the heaviest units starting
+    // first leave the lightest for the last wave.
     const int unit = blockIdx.x;
     const int split = unit % p.ns;
     const int grp = unit / p.ns;
-    const int b = grp / p.groups;
-    const int s0 = (grp - b * p.groups) * p.G;        // first query token of the group (window row)
+    const int b = grp % p.B;
+    const int s0 = (p.groups - 1 - grp / p.B) * p.G;  // first query token of the group (window row)
     const int gv = min(p.G, p.S - s0);                // tokens of the group
     const int k0 = split * p.tps;                     // key tiles [k0, k1)
     const int k1 = min(k0 + p.tps, p.nt);
@@ -681,6 +683,7 @@ cudaError_t launch_md(const AttnArgs &a, cudaStream_t stream) {
     p.W = a.mask_words;
     p.T = a.T;
     p.key_start_word = a.key_start_word;
+    p.B = int(a.B);
     p.S = int(a.S);
     p.io_S = int(io_S);
     p.io_s0 = int(a.io_s0);
