@@ -51,17 +51,20 @@ constexpr long long kWaitCycles = 200000000ll;   // ~0.1 s at 2 GHz per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;      // O and l are rescaled once the row maximum grows by more
 
-// D = 64 runs two CTAs per SM (64-key tiles, 256 TMEM columns each), so each
-// SM sub-partition interleaves two softmax warps; D = 128 and 256 run one.
+// D = 64 runs two CTAs per SM (128-key tiles with one S and one P buffer in
+// 256 TMEM columns each), so each SM sub-partition interleaves two softmax
+// warps; D = 128 (128-key tiles) and 256 (64-key tiles) run one CTA with two
+// S and two P buffers.
 template <int D>
 struct Md {
     static constexpr int CPS = D == 64 ? 2 : 1;      // CTAs per SM
-    static constexpr int BN = D == 128 ? 128 : 64;   // keys per tile
+    static constexpr int BN = D <= 128 ? 128 : 64;   // keys per tile
+    static constexpr int NB = D == 64 ? 1 : 2;       // S and P buffers
     static constexpr int NCH = D / 64;               // 128-byte column chunks of a row
     static constexpr int NW = BN / 32;               // mask words per tile
     static constexpr int Q_BYTES = kRows * D * 2;
     static constexpr int STAGE = BN * D * 2;
-    static constexpr int NS = D == 64 ? 6 : (D == 128 ? 5 : 4);
+    static constexpr int NS = D == 64 ? 4 : (D == 128 ? 5 : 4);
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + Q_BYTES;
     static constexpr int OFF_BITS = OFF_KV + NS * STAGE;
@@ -69,7 +72,7 @@ struct Md {
     // mbarriers
     static constexpr int B_KV_FULL = 0;              // [NS] TMA bytes landed
     static constexpr int B_KV_EMPTY = NS;            // [NS] the P.V that read the stage is done
-    static constexpr int B_S_FULL = 2 * NS;          // [2] S buffer written
+    static constexpr int B_S_FULL = 2 * NS;          // [2] S buffer written (NB used)
     static constexpr int B_S_EMPTY = 2 * NS + 2;     // [2] S buffer read by the 4 softmax warps
     static constexpr int B_P_FULL = 2 * NS + 4;      // [2] P buffer written by the 4 softmax warps
     static constexpr int B_PV_DONE = 2 * NS + 6;     // [2] the P.V of that P buffer is done
@@ -80,10 +83,10 @@ struct Md {
     static constexpr int SMEM = OFF_TSLOT + 16 + 1024;   // + slack to align the base to 1 KB
     // TMEM columns
     static constexpr int O_COL = 0;
-    static constexpr int S_COL = D;                  // two buffers of BN fp32 columns
-    static constexpr int P_COL = D + 2 * BN;         // two buffers of BN / 2 columns (bf16 pairs)
+    static constexpr int S_COL = D;                  // NB buffers of BN fp32 columns
+    static constexpr int P_COL = D + NB * BN;        // NB buffers of BN / 2 columns (bf16 pairs)
     static constexpr int TMEM_COLS = CPS == 2 ? 256 : 512;
-    static_assert(P_COL + BN <= TMEM_COLS, "TMEM budget");
+    static_assert(P_COL + NB * BN / 2 <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM * CPS <= 227 * 1024, "shared memory budget");
     static_assert(Q_BYTES % 1024 == 0 && STAGE % 1024 == 0, "1 KB swizzle alignment");
 };
@@ -344,9 +347,9 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             const uint32_t qa = ptx::smem_u32(smem + C::OFF_Q);
             auto kv_addr = [&](int n) { return ptx::smem_u32(smem + C::OFF_KV + (n % C::NS) * C::STAGE); };
             auto qk = [&](int n) -> bool {
-                const int sb = n & 1;
+                const int sb = n % C::NB;
                 if (!wait_bar(bar(C::B_KV_FULL + n % C::NS), (n / C::NS) & 1, p.err)) return false;
-                if (n >= 2 && !wait_bar(bar(C::B_S_EMPTY + sb), ((n >> 1) - 1) & 1, p.err)) return false;
+                if (n >= C::NB && !wait_bar(bar(C::B_S_EMPTY + sb), ((n / C::NB) - 1) & 1, p.err)) return false;
                 ptx::tc_fence_after();
                 const uint32_t ka = kv_addr(n);
 #pragma unroll
@@ -359,8 +362,8 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
                 return true;
             };
             auto pv = [&](int m) -> bool {
-                const int sb = m & 1;
-                if (!wait_bar(bar(C::B_P_FULL + sb), (m >> 1) & 1, p.err)) return false;
+                const int sb = m % C::NB;
+                if (!wait_bar(bar(C::B_P_FULL + sb), (m / C::NB) & 1, p.err)) return false;
                 ptx::tc_fence_after();
                 const uint32_t va = kv_addr(m);
 #pragma unroll
@@ -453,8 +456,8 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             const int t_nxt = itr.next();
             uint32_t wn[NW];
             tile_bits(t_nxt, wn);                       // prefetch the next tile's words
-            const int sb = n & 1;
-            if (!wait_all(bar(C::B_S_FULL + sb), (n >> 1) & 1, p.err)) { ok = false; break; }
+            const int sb = n % C::NB;
+            if (!wait_all(bar(C::B_S_FULL + sb), (n / C::NB) & 1, p.err)) { ok = false; break; }
             ptx::tc_fence_after();
             float s[BN];
             {
@@ -501,7 +504,7 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             }
             if (n > 0 && __any_sync(0xffffffffu, f != 1.f)) {
                 // O holds P.V of the earlier tiles: wait for the last one, scale
-                if (!wait_all(bar(C::B_PV_DONE + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.err)) { ok = false; break; }
+                if (!wait_all(bar(C::B_PV_DONE + (n - 1) % C::NB), ((n - 1) / C::NB) & 1, p.err)) { ok = false; break; }
                 ptx::tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -518,29 +521,28 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             const float nm = m_run == -INFINITY ? 0.f : -m_run;
             const uint64_t sc2 = f2(sc, sc), nm2 = f2(nm, nm);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // packed partial sums
-            uint32_t pw[BN / 2];
-#pragma unroll
-            for (int c = 0; c < BN / 2; ++c) {
-                const uint64_t xy = f2(s[2 * c], s[2 * c + 1]);
-                float z0, z1;
-                f2_split(POS ? ffma2(xy, sc2, nm2) : fadd2(xy, nm2), z0, z1);
-                const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-                acc[c & 3] = fadd2(acc[c & 3], f2(p0, p1));
-                pw[c] = pack_bf16(p0, p1);
-            }
-            float l0, l1, l2, l3;
-            f2_split(fadd2(acc[0], acc[1]), l0, l1);
-            f2_split(fadd2(acc[2], acc[3]), l2, l3);
-            // P buffer sb is free once the P.V of tile n - 2 is done
-            if (n >= 2 && !wait_all(bar(C::B_PV_DONE + sb), ((n >> 1) - 1) & 1, p.err)) { ok = false; break; }
+            // P buffer sb is free once the P.V of tile n - NB is done
+            if (n >= C::NB && !wait_all(bar(C::B_PV_DONE + sb), ((n / C::NB) - 1) & 1, p.err)) { ok = false; break; }
             ptx::tc_fence_after();
+            // 64 keys at a time, each half stored to TMEM as soon as it is packed
 #pragma unroll
             for (int k = 0; k < BN / 64; ++k) {
                 uint32_t q32[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) q32[j] = pw[32 * k + j];
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const int c = 32 * k + c2;
+                    const uint64_t xy = f2(s[2 * c], s[2 * c + 1]);
+                    float z0, z1;
+                    f2_split(POS ? ffma2(xy, sc2, nm2) : fadd2(xy, nm2), z0, z1);
+                    const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+                    acc[c & 3] = fadd2(acc[c & 3], f2(p0, p1));
+                    q32[c2] = pack_bf16(p0, p1);
+                }
                 ptx::tmem_st32(lane_base + C::P_COL + sb * (BN / 2) + 32 * k, q32);
             }
+            float l0, l1, l2, l3;
+            f2_split(fadd2(acc[0], acc[1]), l0, l1);
+            f2_split(fadd2(acc[2], acc[3]), l2, l3);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
