@@ -11,18 +11,18 @@
 // consecutive query tokens, key split); a key tile is BN consecutive keys of
 // kv[b], loaded whole by TMA -- the keys are dense, nothing is gathered.
 //
-// Per CTA (one unit, 6 warps):
+// Per CTA (one unit, 8 warps):
 //   all warps  (prologue) read the group's mask rows over the unit's key range
 //              with 16-byte loads and mark, in a shared bitmap, every key tile
 //              in which some row admits a key; only those tiles are loaded and
 //              computed;
-//   warp 0     TMA: Q once (128 rows x D), then the marked key tiles through an
+//   warp 4     TMA: Q once (128 rows x D), then the marked key tiles through an
 //              NS-stage ring;
-//   warp 1     tcgen05.mma: S = Q K^T into one of two TMEM S buffers (one tile
-//              ahead of the softmax), O += P V with P (bf16) read from one of
-//              two TMEM P buffers and V the same stage read MN-major; O stays
-//              in TMEM for the unit;
-//   warps 2..5 softmax, one thread per row (lane quarter = warp % 4): the
+//   warp 5     tcgen05.mma: S = Q K^T into a TMEM S buffer (one tile ahead of
+//              the softmax), O += P V with P (bf16) read from a TMEM P buffer
+//              and V the same stage read MN-major; O stays in TMEM for the
+//              unit (warps 6 and 7 only help with the prologue);
+//   warps 0..3 softmax, one thread per row (lane quarter = warp): the
 //              row's mask words for the tile (16-byte loads, prefetched one
 //              tile ahead), masked row maximum, lazy rescale of O (only when
 //              the maximum grows by more than 2^8), P = 2^(x - m) into TMEM;
@@ -44,7 +44,14 @@ namespace sa {
 namespace {
 
 constexpr int kRows = 128;               // MMA rows (TMEM lanes): G tokens x H heads
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+// D = 64 (two CTAs per SM): launched at 128 registers a thread; after the
+// prologue the softmax warpgroup grows to 200 and the other warpgroup shrinks
+// to 56: 128 * 200 + 128 * 56 = 256 * 128.
+constexpr int kLaunchRegs = 128;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kOtherRegs = 56;
+static_assert(128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kMaxTiles = 8192;          // key tiles per work unit (the host enforces it)
 constexpr int kBitmapWords = kMaxTiles / 32;
 constexpr long long kWaitCycles = 200000000ll;   // ~0.1 s at 2 GHz per wait
@@ -259,14 +266,14 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
         ptx::mbar_init(bar(C::B_MMA_DONE), 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_u32(tslot), C::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     for (int i = tid; i < nbw; i += kThreads) bitmap[i] = 0u;
     __syncthreads();
     const int64_t qrow0 = (int64_t(b) * p.io_S + p.io_s0 + s0) * p.H;
-    if (warp == 0 && lane == 0) {
+    if (warp == 4 && lane == 0) {
         ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
@@ -314,8 +321,9 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
     const uint32_t tbase = *tslot;
     int n_act = 0;
     for (int i = 0; i < nbw; ++i) n_act += __popc(bitmap[i]);
-
-    if (warp == 0) {
+    if (warp >= 4) {
+      if constexpr (C::CPS == 2) ptx::setmaxnreg_dec<kOtherRegs>();
+      if (warp == 4) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             TileIter itr(bitmap, nbw, k0);
@@ -339,7 +347,7 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+      } else if (warp == 5) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kRows, BN, false);
@@ -387,9 +395,11 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             ptx::mma_commit(bar(C::B_MMA_DONE));   // arrives once every MMA issued above has completed
         }
         __syncwarp();
+      }
     } else {
         // ------------------------------------------------------------ softmax
-        const int q4 = warp & 3;
+        if constexpr (C::CPS == 2) ptx::setmaxnreg_inc<kSoftmaxRegs>();
+        const int q4 = warp;
         const int r = q4 * 32 + lane;                  // this thread's row
         const int tok = r / p.H, h = r - tok * p.H;
         const bool row_ok = r < p.G * p.H && tok < gv;
@@ -624,7 +634,7 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
     // ---------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 5) {
         drain_wait(bar(C::B_MMA_DONE), 0);   // no MMA of this CTA is still running
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, C::TMEM_COLS);
