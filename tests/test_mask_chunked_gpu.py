@@ -80,12 +80,14 @@ def _attn_inputs(B, Q, H, D, T, seed):
             torch.randn(H, generator=g))
 
 
+@pytest.mark.parametrize("H,D", [(8, 64), (16, 128), (32, 256)])
 @pytest.mark.parametrize("with_ks", [False, True])
 @pytest.mark.parametrize("cap", [0, 60000, 30000])
-def test_windowed_build_and_consume_matches_the_whole_mask_oracle(cap, with_ks):
+def test_windowed_build_and_consume_matches_the_whole_mask_oracle(cap, with_ks, H, D):
     # max_q 300 queries, 700 key positions; cap 60000 B -> windows of 256
-    # rows, 30000 B -> windows of 128 rows, 0 -> the whole mask at once
-    B, Q, H, D, keys, K = 2, 300, 8, 64, 700, 50
+    # rows, 30000 B -> windows of 128 rows, 0 -> the whole mask at once; the
+    # packed consumer with one (D = 64) or two (D = 128, 256) S / P buffers
+    B, Q, keys, K = 2, 300, 700, 50
     _, q_lens, topk, cu = _case(73 + cap, B, Q, keys, K)
     ks = np.array([0, 0], np.int32) if not with_ks else np.array([100, 37], np.int32)
     T = keys - int(ks.max())                  # kv[b] holds mask positions ks_b .. ks_b + T - 1

@@ -139,6 +139,22 @@ def test_key_start_word_offsets_the_bit_test(key_starts):
     assert_close(o, want, f"key_starts={key_starts}")
 
 
+@pytest.mark.parametrize("D,key_starts", [(64, (256, 384)), (128, (128, 0)), (256, (640, 64))])
+def test_key_start_multiple_of_the_tile(D, key_starts):
+    # key offsets that are multiples of the key tile take the packed
+    # consumer's one-vector path for the mask words of every whole tile
+    B, S, H, T = 2, 5, 8, 700
+    q, kv, sink = _inputs(B, S, H, D, T, seed=19 + D)
+    rng = np.random.default_rng(20)
+    max_key = 1500
+    topk = rng.integers(-3, max_key, size=(B * S, 300)).astype(np.int32)
+    cu = np.arange(0, B * S + 1, S, dtype=np.int32)
+    mask = oracle.build_topk_mask(topk, cu, B, S, max_key, key_starts=np.array(key_starts, np.int32))
+    o = _gpu(q, kv, sink, mask, D ** -0.5, key_start_word=True)
+    want = oracle.masked_dense_attn(q, kv, sink, mask, D ** -0.5, key_offset=list(key_starts))
+    assert_close(o, want, f"D={D} key_starts={key_starts}")
+
+
 def test_reserved_word_is_never_a_key_bit():
     # key_start = -1 fills the reserved word of row 0 with ones; the chunk's
     # keys reach its positions, and the consumer must admit none of them
