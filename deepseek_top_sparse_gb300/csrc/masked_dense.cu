@@ -18,16 +18,21 @@
 //              computed;
 //   warp 4     TMA: Q once (128 rows x D), then the marked key tiles through an
 //              NS-stage ring;
-//   warp 5     tcgen05.mma: S = Q K^T into a TMEM S buffer (one tile ahead of
-//              the softmax), O += P V with P (bf16) read from a TMEM P buffer
-//              and V the same stage read MN-major; O stays in TMEM for the
-//              unit (warps 6 and 7 only help with the prologue);
+//   warp 5     tcgen05.mma: S = Q K^T into one of NB TMEM S buffers (ahead of
+//              the softmax), O += P V with P (bf16) read from one of NB TMEM P
+//              buffers and V the same stage read MN-major; O stays in TMEM for
+//              the unit (warps 6 and 7 only help with the prologue);
 //   warps 0..3 softmax, one thread per row (lane quarter = warp): the
-//              row's mask words for the tile (16-byte loads, prefetched one
-//              tile ahead), masked row maximum, lazy rescale of O (only when
-//              the maximum grows by more than 2^8), P = 2^(x - m) into TMEM;
-//              then the epilogue (o = O / (l + sink term), bf16, or the split
-//              partials for the combine kernel).
+//              row's mask words for the tile (prefetched one tile ahead: one
+//              aligned vector load when the tile's positions start on a
+//              multiple of BN inside the admissible range, else two 16-byte
+//              vectors and a funnel shift), masked row maximum, lazy rescale
+//              of O (only when the maximum grows by more than 2^8),
+//              P = 2^(x - m) into TMEM; then the epilogue (o = O / (l + sink
+//              term), bf16, or the split partials for the combine kernel).
+//
+// Units launch with the query groups last-first (the requests interleaved):
+// later queries usually see more keys, so the heaviest units start first.
 //
 // Every mbarrier wait is bounded by clock64 and gives up early once any wait
 // has recorded an error in the library's device error word; before it exits a
