@@ -99,7 +99,11 @@ struct Cfg {
     static_assert(DC == 64 || DC == 128 || DC == 256, "per-CTA head-dim slice");
     static_assert(!F8 || (DC == 256 && CL == 2), "FP8 rows only at D = 512 (two 256-column halves)");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
-    static constexpr int NS = F8 ? 3 : 4;   // kv ring depth (bf16 stages the MMA reads)
+    static constexpr int NS = F8 ? 3 : 5;   // kv ring depth (bf16 stages the MMA reads)
+    // partner partial-logit buffers per lane quarter: one for the bf16 pair
+    // (its owner consumes them at the start of a tile, before the sender can
+    // need the buffer again), which leaves room for the fifth kv stage
+    static constexpr int XB = (CL == 2 && !F8) ? 1 : 2;
     // FP8: the raw bytes of a tile land in one of NF staging buffers (one
     // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
     // values at [0, 320), its scale bytes at 320) and are widened to bf16
@@ -130,7 +134,7 @@ struct Cfg {
     static constexpr int OFF_P = OFF_STG + NF * STG_BYTES;
     static_assert(OFF_P % 1024 == 0, "P buffers keep the 1 KB swizzle alignment");
     static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_F = OFF_X + (CL == 2 ? 2 * 4 * XQ : 0);
+    static constexpr int OFF_F = OFF_X + (CL == 2 ? XB * 4 * XQ : 0);
     static constexpr int OFF_IDX = OFF_F + (CL == 2 ? 2 * 4 * FQ : 0);
     static constexpr int OFF_VALID = OFF_IDX + kMaxUnitSlots * 4;
     static constexpr int OFF_LIST = OFF_VALID + kMaxUnitTiles * 8;
@@ -907,8 +911,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
             for (int a = 0; a < n_act; ++a) {
                 const int sb = a & 1;
                 const uint32_t ph = uint32_t(a >> 1) & 1u;
+                const int xb = a % C::XB;                          // partner partials buffer
+                const uint32_t xph = uint32_t(a / C::XB) & 1u;
                 if constexpr (CL == 2) {
-                    if (lane == 0) ptx::mbar_arrive_expect_tx(x_full(sb, quarter), C::XQ);
+                    if (lane == 0) ptx::mbar_arrive_expect_tx(x_full(xb, quarter), C::XQ);
                 }
                 if (!wait_all(s_full(sb), ph)) {
                     ok = false;
@@ -928,21 +934,21 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 if (lane == 0) ptx::mbar_arrive(s_empty(sb));
                 if constexpr (CL == 2) {
                     // + the partner's partial logits of the same rows and columns
-                    if (!wait_all<true>(x_full(sb, quarter), ph)) {
+                    if (!wait_all<true>(x_full(xb, quarter), xph)) {
                         ok = false;
                         break;
                     }
-                    const uint8_t *xb = smem + C::OFF_X + (sb * 4 + quarter) * C::XQ + lane * 16;
+                    const uint8_t *xp = smem + C::OFF_X + (xb * 4 + quarter) * C::XQ + lane * 16;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float4 v = *reinterpret_cast<const float4 *>(xb + k * 512);
+                        const float4 v = *reinterpret_cast<const float4 *>(xp + k * 512);
                         s[4 * k] += v.x;
                         s[4 * k + 1] += v.y;
                         s[4 * k + 2] += v.z;
                         s[4 * k + 3] += v.w;
                     }
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_remote_relaxed(remote(x_empty(sb, quarter)));
+                    if (lane == 0) ptx::mbar_arrive_remote_relaxed(remote(x_empty(xb, quarter)));
                 }
                 // Row maxima of scale * s over the valid columns.  With a
                 // positive scale (the usual case) invalid slots become -inf,
@@ -1105,8 +1111,9 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(s_empty(jb));
-                if (j2 >= 2 && !wait_all(x_empty(jb, quarter), uint32_t((j2 >> 1) - 1) & 1u)) return false;
-                const uint32_t dst = remote(x_buf(jb)) + uint32_t(lane * 16), fbar = remote(x_full(jb, quarter));
+                const int xj = j2 % C::XB;
+                if (j2 >= C::XB && !wait_all(x_empty(xj, quarter), uint32_t((j2 / C::XB) - 1) & 1u)) return false;
+                const uint32_t dst = remote(x_buf(xj)) + uint32_t(lane * 16), fbar = remote(x_full(xj, quarter));
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     ptx::st_async_v4(dst + uint32_t(k * 512), r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3], fbar);
