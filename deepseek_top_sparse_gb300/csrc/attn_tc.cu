@@ -100,15 +100,16 @@ struct Cfg {
     static_assert(!F8 || (DC == 256 && CL == 2), "FP8 rows only at D = 512 (two 256-column halves)");
     static constexpr int STAGE_BYTES = kBN * DC * 2;
     static constexpr int NS = F8 ? 3 : 5;   // kv ring depth (bf16 stages the MMA reads)
-    // partner partial-logit buffers per lane quarter: one for the bf16 pair
-    // (its owner consumes them at the start of a tile, before the sender can
-    // need the buffer again), which leaves room for the fifth kv stage
-    static constexpr int XB = (CL == 2 && !F8) ? 1 : 2;
+    // partner partial-logit buffers per lane quarter: one for a pair (its
+    // owner consumes them at the start of a tile, before the sender can need
+    // the buffer again), which leaves room for the fifth bf16 kv stage or the
+    // third FP8 staging buffer
+    static constexpr int XB = CL == 2 ? 1 : 2;
     // FP8: the raw bytes of a tile land in one of NF staging buffers (one
     // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
     // values at [0, 320), its scale bytes at 320) and are widened to bf16
-    // into a kv stage by the gather warps
-    static constexpr int NF = F8 ? 2 : 0;
+    // into a kv stage by the gather warps; the copy warps run NF tiles ahead
+    static constexpr int NF = F8 ? 3 : 0;
     static constexpr int STG_ROW = 336;
     static constexpr int STG_SCALE = 320;
     static constexpr int STG_BYTES = kBN * STG_ROW;
