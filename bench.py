@@ -152,6 +152,41 @@ def _attn_kernel_sources():
     return [p for p in KERNEL_SOURCES if os.path.exists(os.path.join(ROOT, p))]
 
 
+def gather_ceiling(dev, flush):
+    """The GPU's random-row gather rate (sa_probe_row_gather): one CTA per SM
+    copies 24 tiles of 32 KB of rows picked at random from a 4 GB table of
+    1 KB rows; every run takes a fresh index set after a 256 MB L2 flush, so
+    the bytes come from HBM.  Median of 3 runs for whole 1 KB rows and for
+    512-byte half rows, in GB/s."""
+    from deepseek_top_sparse_gb300 import binding
+
+    row_bytes, rows, tiles = 1024, 1 << 22, 24
+    ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    table = torch.zeros(rows * row_bytes, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(20261203)
+    st = torch.cuda.current_stream()
+    res = {}
+    for part in (1024, 512):
+        n = ctas * tiles * (32768 // part)
+        idx = torch.randint(0, rows, (n,), generator=g, device=dev, dtype=torch.int32)
+        binding.probe_row_gather(table, row_bytes, part, idx, ctas, tiles)   # warm-up launch
+        ts = []
+        for _ in range(3):
+            idx = torch.randint(0, rows, (n,), generator=g, device=dev, dtype=torch.int32)
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            binding.probe_row_gather(table, row_bytes, part, idx, ctas, tiles)
+            b.record(st)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e-3)
+        res[part] = ctas * tiles * 32768 / statistics.median(ts) / 1e9
+    if binding.sa_device_error(True) != 0:
+        raise RuntimeError("the gather probe recorded a wait timeout")
+    del table
+    return res[1024], res[512]
+
+
 def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None, spread: bool = False):
     """Time the oracle (as it stands) on whole tokens of the workload until
     about budget_s of wall time; returns (tokens/s, tokens, seconds, threads).
@@ -582,6 +617,17 @@ def run_gpu(args):
 
     hbm, tf_burst, _, src = _peaks()
     sec = ms * 1e-3
+    ceiling_obj = None
+    if not args.no_extra:
+        whole, halves = gather_ceiling(dev, flush)
+        ceiling_obj = {"unit": "GB/s", "whole_rows_1kb": whole, "half_rows_512b": halves,
+                       "frac_of_copy_peak": whole / hbm,
+                       "decode_gathered": gathered / sec / 1e9,
+                       "decode_frac_of_ceiling": gathered / sec / 1e9 / whole,
+                       "probe": "sa_probe_row_gather: one CTA per SM, 24 tiles of 32 KB of random rows of a 4 GB "
+                                "table of 1 KB rows, fresh rows and a 256 MB L2 flush before each of 3 runs (median)",
+                       "note": "decode_frac_of_ceiling is the whole kernel (prologue and combine included) against the "
+                               "rate a random-row gather can reach on this GPU"}
     achieved_gbs = gathered / sec / 1e9
     tflops = flops / sec / 1e12
     roof_t = max(flops / (tf_burst * 1e12), gathered / (hbm * 1e9))
@@ -615,6 +661,7 @@ def run_gpu(args):
         "wall_s_timed_loop": wall,
         "mask_build": mask_obj,
         "hot_l2_graph": hot_obj,
+        "gather_ceiling": ceiling_obj,
         "other_configs": other,
     }
     print(json.dumps(line), flush=True)

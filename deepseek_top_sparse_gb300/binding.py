@@ -32,7 +32,8 @@ EXPORTS = ("sa_status_string", "sa_sparse_attn_num_splits", "sa_sparse_attn_work
            "sa_masked_dense_attn_fwd", "sa_masked_dense_attn_workspace_size", "sa_masked_dense_attn_launch_count",
            "sa_sparse_attn_fwd_fp8", "sa_sparse_attn_fp8_launch_count", "sa_build_topk_mask_window",
            "sa_masked_dense_attn_fwd_window", "sa_topk_mask_chunk_rows", "sa_topk_masked_attn_fwd",
-           "sa_topk_masked_attn_workspace_size", "sa_sparse_attn_fwd_extra", "sa_sparse_attn_fwd_fp8_extra")
+           "sa_topk_masked_attn_workspace_size", "sa_sparse_attn_fwd_extra", "sa_sparse_attn_fwd_fp8_extra",
+           "sa_probe_row_gather")
 
 _lock = threading.Lock()
 _lib = None
@@ -113,6 +114,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sa_selftest_wait_timeout.restype = i32
         lib.sa_selftest_wait_drain.argtypes = [i32, ctypes.c_longlong, ctypes.POINTER(ctypes.c_float)]
         lib.sa_selftest_wait_drain.restype = i32
+        lib.sa_probe_row_gather.argtypes = [p, i64, i64, i64, p, i64, i64, p]
+        lib.sa_probe_row_gather.restype = i32
         lib.sa_device_error.argtypes = [i32]
         lib.sa_device_error.restype = i32
         _lib = lib
@@ -249,6 +252,10 @@ def sa_selftest_wait_drain(ctas: int, first_cycles: int) -> tuple[int, float]:
     return code, float(ms.value)
 
 
+def sa_probe_row_gather(table, rows, row_bytes, part_bytes, idx, ctas, tiles, stream) -> int:
+    return int(load().sa_probe_row_gather(table, rows, row_bytes, part_bytes, idx, ctas, tiles, stream))
+
+
 def sa_device_error(clear: bool = True) -> int:
     return int(load().sa_device_error(int(bool(clear))))
 
@@ -268,6 +275,24 @@ def _dptr(t: torch.Tensor | None) -> int | None:
 def _check(fn: str, rc: int):
     if rc != SA_OK:
         raise SAError(fn, rc)
+
+
+def probe_row_gather(table: torch.Tensor, row_bytes: int, part_bytes: int, idx: torch.Tensor, ctas: int,
+                     tiles: int, stream=None) -> None:
+    """Enqueue the random-row gather probe (include/sa.h): `ctas` CTAs copy
+    `tiles` 32 KB tiles each of the first part_bytes of the rows of `table`
+    (a contiguous CUDA uint8 tensor of whole rows) that idx picks."""
+    if table.dtype != torch.uint8 or not table.is_cuda or not table.is_contiguous():
+        raise ValueError("table must be a contiguous CUDA uint8 tensor")
+    if idx.dtype != torch.int32 or not idx.is_cuda or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous CUDA int32 tensor")
+    if row_bytes <= 0 or table.numel() % row_bytes != 0 or part_bytes <= 0:
+        raise ValueError("table must hold whole rows of row_bytes bytes")
+    if idx.numel() != ctas * tiles * (32768 // part_bytes):
+        raise ValueError("idx must hold ctas * tiles * (32768 // part_bytes) rows")
+    _check("sa_probe_row_gather", load().sa_probe_row_gather(
+        _dptr(table), table.numel() // row_bytes, row_bytes, part_bytes, _dptr(idx), ctas, tiles,
+        _stream_ptr(stream)))
 
 
 def workspace_for(B, S, H, D, K, num_splits=0, device=None) -> torch.Tensor | None:

@@ -553,6 +553,27 @@ int sa_selftest_wait_drain(int ctas, long long first_cycles, float *elapsed_ms) 
     return code;
 }
 
+sa_status sa_probe_row_gather(const void *table, int64_t rows, int64_t row_bytes, int64_t part_bytes,
+                              const int32_t *idx, int64_t ctas, int64_t tiles, sa_stream_t stream) {
+    if (table == nullptr || idx == nullptr) return SA_ERR_INVALID_ARG;
+    if (rows < 1 || rows > INT32_MAX || ctas < 1 || ctas > 65535 || tiles < 1 || tiles > (1 << 20))
+        return SA_ERR_INVALID_ARG;
+    if (part_bytes < 16 || part_bytes > 32768 || (part_bytes & (part_bytes - 1)) != 0 || row_bytes < part_bytes ||
+        row_bytes % 16 != 0)
+        return SA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(table) % 16 != 0) return SA_ERR_ALIGNMENT;
+    if (rows > INT64_MAX / row_bytes) return SA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const sa_status st = current_device(&dev);
+    if (st != SA_OK) return st;
+    int shift = 4;
+    while ((int64_t(1) << shift) < part_bytes) ++shift;
+    if (sa::launch_row_gather_probe(table, rows, row_bytes, shift, idx, int(ctas), int(tiles),
+                                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return SA_OK;
+}
+
 int sa_device_error(int clear) {
     int v = 0;
     if (sa::read_device_error(&v, clear != 0) != cudaSuccess) return -1;

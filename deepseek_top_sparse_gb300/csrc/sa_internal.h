@@ -27,6 +27,10 @@ cudaError_t device_error_word(int **ptr);
 void *tensor_map_encode_fn();
 cudaError_t launch_wait_timeout_selftest(long long max_cycles, cudaStream_t stream);
 cudaError_t launch_wait_drain_selftest(int ctas, long long first_cycles, cudaStream_t stream);
+// The random-row gather probe (row_gather_probe.cu): `ctas` CTAs, each
+// copying `tiles` 32 KB tiles of 1 << part_shift bytes of the rows idx picks.
+cudaError_t launch_row_gather_probe(const void *table, int64_t rows, int64_t row_bytes, int part_shift,
+                                    const int32_t *idx, int ctas, int tiles, cudaStream_t stream);
 
 // ---- launchers (host side, enqueue only; arguments already validated) ----
 

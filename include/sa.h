@@ -399,6 +399,29 @@ int sa_selftest_wait_timeout(long long max_cycles);
  * have no counterpart of this call. */
 int sa_selftest_wait_drain(int ctas, long long first_cycles, float *elapsed_ms);
 
+/* Random-row gather probe: the rate at which the SMs can pull rows picked at
+ * random out of a table in device memory, which bounds the kv gather of
+ * sparse_attn ("第5章" §5.6: one kv row per valid slot, from anywhere in the
+ * cache).  The pages have no counterpart; the call measures the hardware.
+ *   table       device, `rows` rows of `row_bytes` bytes (16-byte aligned,
+ *               row_bytes a multiple of 16), 1 <= rows <= 2^31 - 1;
+ *   part_bytes  bytes copied from the start of each picked row: a power of
+ *               two in [16, 32768], at most row_bytes;
+ *   idx         device int32 [ctas * tiles * (32768 / part_bytes)]: the rows,
+ *               in the order CTA c copies them (c-major); a value outside
+ *               [0, rows) copies row 0;
+ *   ctas        1 .. 65535 CTAs of 256 threads, one per SM at most (197 KB of
+ *               shared memory each); CTA c copies `tiles` (1 .. 2^20) tiles of
+ *               32 KB into shared memory through a six-stage ring and
+ *               discards them.
+ * Enqueued on `stream`; the caller times it (the bytes moved are
+ * ctas * tiles * 32768) and flushes L2 first for an HBM figure.  Returns
+ * SA_ERR_INVALID_ARG / SA_ERR_ALIGNMENT on bad arguments before launching,
+ * SA_ERR_CUDA if the launch fails.  A wait that runs out sets the device
+ * error word (sa_device_error). */
+sa_status sa_probe_row_gather(const void *table, int64_t rows, int64_t row_bytes, int64_t part_bytes,
+                              const int32_t *idx, int64_t ctas, int64_t tiles, sa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

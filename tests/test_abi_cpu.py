@@ -250,3 +250,15 @@ def test_extra_source_arguments_are_checked_on_the_host():
     assert call(extra_kv=a16 + 4) == "SA_ERR_ALIGNMENT"
     assert call(extra_topk_idxs=a16 + 2) == "SA_ERR_ALIGNMENT"
     assert call(B=1 << 20, T=1 << 11, T2=1 << 11) == "SA_ERR_SHAPE"
+
+
+def test_gather_probe_validates_before_any_device_work():
+    f = binding.sa_probe_row_gather
+    ok = dict(table=4096, rows=1024, row_bytes=1024, part_bytes=512, idx=8192, ctas=4, tiles=2, stream=None)
+    bad = [dict(table=None), dict(idx=None), dict(rows=0), dict(rows=1 << 31), dict(ctas=0), dict(ctas=65536),
+           dict(tiles=0), dict(tiles=(1 << 20) + 1), dict(part_bytes=8), dict(part_bytes=768),
+           dict(part_bytes=65536), dict(row_bytes=256), dict(row_bytes=1032 - 1)]
+    for b in bad:
+        args = dict(ok, **b)
+        assert f(**args) == 1, b                              # SA_ERR_INVALID_ARG
+    assert f(**dict(ok, table=4096 + 8)) == 3                 # SA_ERR_ALIGNMENT
