@@ -316,6 +316,12 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+    // Launched with a programmatic dependency on the previous kernel of the
+    // stream: that kernel's writes are visible only after this wait, so every
+    // thread waits before its first global memory access; the next such
+    // launch may begin right away (it waits the same way for this grid).
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // A cluster is one token: its splits x the CL head-dim halves (CL alone
     // when the splits are combined by a separate kernel).  Rank = local split
@@ -1663,13 +1669,17 @@ cudaError_t launch_tc(const AttnArgs &a, cudaStream_t stream, bool *fused_out) {
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(fused ? cs_fused : CL);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+    // for the stream's previous kernel before it touches global memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     CUtensorMap qmap;
     e = encode_q_map(&qmap, a);
     if (e != cudaSuccess) return e;
