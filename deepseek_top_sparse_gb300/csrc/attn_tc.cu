@@ -1438,6 +1438,8 @@ __global__ void __launch_bounds__(128)
 attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse, const float *__restrict__ sink,
                     __nv_bfloat16 *__restrict__ o, int64_t rows, int64_t H, int ns, int64_t S, int64_t io_S,
                     int64_t io_s0) {
+    ptx::griddep_wait();               // the stream's previous kernel: complete and visible
+    ptx::griddep_launch_dependents();
     constexpr int E = D / 32;              // columns per lane
     constexpr int V = E >= 4 ? 4 : 2;      // columns per vector access
     constexpr int G = E / V;               // vectors per lane
@@ -1749,13 +1751,15 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t stream) {
     const int64_t io_S = a.io_S > 0 ? a.io_S : a.S;   // 0: o holds exactly the call's S rows per request
     if (rows == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+    cudaError_t e;
     switch (a.D) {
-        case 64: attn_combine_kernel<64><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
-        case 128: attn_combine_kernel<128><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
-        case 256: attn_combine_kernel<256><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
-        case 512: attn_combine_kernel<512><<<grid, 128, 0, stream>>>(a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 64: e = launch_pdl(attn_combine_kernel<64>, grid, dim3(128), 0, stream, a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 128: e = launch_pdl(attn_combine_kernel<128>, grid, dim3(128), 0, stream, a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 256: e = launch_pdl(attn_combine_kernel<256>, grid, dim3(128), 0, stream, a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
+        case 512: e = launch_pdl(attn_combine_kernel<512>, grid, dim3(128), 0, stream, a.ws_o, a.ws_lse, a.sink, static_cast<__nv_bfloat16 *>(a.o), rows, a.H, a.num_splits, a.S, io_S, a.io_s0); break;
         default: return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@
 //     load queues.
 //   * wider rows up to kSmemWordsMax words: one CTA per row.
 //   * wider still: global atomics straight into the output row.
+#include "ptx.cuh"
 #include "sa_internal.h"
 
 namespace sa {
@@ -67,6 +68,8 @@ __device__ __forceinline__ void scatter_row(const int32_t *__restrict__ row, int
 
 __global__ void __launch_bounds__(kMaskThreads)
 build_topk_mask_kernel(MaskArgs a, int smem_path) {
+    ptx::griddep_wait();               // the stream's previous kernel: complete and visible
+    ptx::griddep_launch_dependents();
     extern __shared__ __align__(16) uint32_t row_img[];
     const uint32_t max_key = static_cast<uint32_t>(a.max_key_len);
 
@@ -125,6 +128,8 @@ struct WarpMaskArgs {
 template <int kLoadsInFlight, int kMinBlocks>
 __global__ void __launch_bounds__(kMaskThreads, kMinBlocks)
 build_topk_mask_warp_kernel(WarpMaskArgs a) {
+    ptx::griddep_wait();               // the stream's previous kernel: complete and visible
+    ptx::griddep_launch_dependents();
     extern __shared__ __align__(16) uint32_t images[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int img_words = (a.live_words + 3) / 4 * 4;
@@ -203,7 +208,9 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
         if (live_words <= kSmallRowWords) {
-            build_topk_mask_warp_kernel<2, 8><<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(w);
+            const cudaError_t e = launch_pdl(build_topk_mask_warp_kernel<2, 8>, dim3(unsigned(grid)), dim3(kMaskThreads),
+                                             smem, stream, w);
+            if (e != cudaSuccess) return e;
         } else {
             auto kern = build_topk_mask_warp_kernel<8, 3>;
             if (smem > 48 * 1024) {
@@ -211,7 +218,8 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
                     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
                 if (e != cudaSuccess) return e;
             }
-            kern<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(w);
+            const cudaError_t e2 = launch_pdl(kern, dim3(unsigned(grid)), dim3(kMaskThreads), smem, stream, w);
+            if (e2 != cudaSuccess) return e2;
         }
         return cudaGetLastError();
     }
@@ -220,7 +228,9 @@ cudaError_t launch_build_topk_mask(const MaskArgs &a, int num_sms, cudaStream_t 
     int64_t grid = n_slots;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    build_topk_mask_kernel<<<static_cast<unsigned>(grid), kMaskThreads, smem, stream>>>(a, smem_path);
+    const cudaError_t e = launch_pdl(build_topk_mask_kernel, dim3(unsigned(grid)), dim3(kMaskThreads), smem, stream, a,
+                                     smem_path);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

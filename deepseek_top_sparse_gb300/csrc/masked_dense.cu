@@ -219,6 +219,8 @@ template <int D, bool POS>
 __global__ void __launch_bounds__(kThreads, Md<D>::CPS)
 masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kvmap) {
+    ptx::griddep_wait();               // the stream's previous kernel: complete and visible
+    ptx::griddep_launch_dependents();
     using C = Md<D>;
     constexpr int BN = C::BN;
     constexpr int NW = C::NW;
@@ -719,9 +721,10 @@ cudaError_t launch_md(const AttnArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t ctas = a.B * int64_t(p.groups) * p.ns;
     if (a.scale > 0.f)
-        masked_dense_kernel<D, true><<<unsigned(ctas), kThreads, C::SMEM, stream>>>(p, qmap, kvmap);
+        e = launch_pdl(masked_dense_kernel<D, true>, dim3(unsigned(ctas)), dim3(kThreads), C::SMEM, stream, p, qmap, kvmap);
     else
-        masked_dense_kernel<D, false><<<unsigned(ctas), kThreads, C::SMEM, stream>>>(p, qmap, kvmap);
+        e = launch_pdl(masked_dense_kernel<D, false>, dim3(unsigned(ctas)), dim3(kThreads), C::SMEM, stream, p, qmap, kvmap);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

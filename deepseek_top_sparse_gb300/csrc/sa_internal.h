@@ -9,6 +9,26 @@
 
 namespace sa {
 
+// Launches kern<<<grid, block, smem, stream>>>(args...) with a programmatic
+// dependency on the stream's previous kernel: the launch may proceed while
+// that kernel runs, so `kern` executes griddepcontrol.wait (ptx::griddep_wait)
+// in every thread before its first global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Codes written to the device error word (see sa_device_error in sa.h).
 enum DeviceError : int {
     kErrNone = 0,
