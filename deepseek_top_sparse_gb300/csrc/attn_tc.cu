@@ -247,12 +247,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float &sum) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Rows a split combines inside the cluster: [split * rp, split * rp + rp) with
-// rp = ceil(H / splits), clipped to H.
-__device__ __forceinline__ void combine_range(const TcParams &p, int split, int &cr0, int &cr1) {
-    const int rp = int((p.H + p.num_splits - 1) / p.num_splits);
-    cr0 = split * rp;
-    cr1 = cr0 + rp < p.H ? cr0 + rp : int(p.H);
+// (a, b) as a bf16 pair, and the two rounded values added to the packed pair
+// of partial sums `acc` (the rounded values are what the MMA accumulates).
+__device__ __forceinline__ uint32_t pack_bf16_acc(float a, float b, uint64_t &acc) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(&v);
+    acc = ptx::fadd2(acc, ptx::f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+    return u;
 }
 
 // E8M0 scale byte -> 2^(byte - 127) as a float (255 -> NaN; 0 -> 2^-127, a
@@ -975,11 +976,18 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                             for (int e = 0; e < 2; ++e)
                                 if (!((vq >> (8 * k + e)) & 1ull)) s[4 * k + e] = s[4 * k + 2 + e] = -INFINITY;
                     }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        mxA = fmaxf(mxA, fmaxf(s[4 * k], s[4 * k + 1]));
-                        mxB = fmaxf(mxB, fmaxf(s[4 * k + 2], s[4 * k + 3]));
-                    }
+                    // 3-input maxima over the 16 values of each row: row A holds
+                    // s[4k], s[4k + 1], row B s[4k + 2], s[4k + 3]
+                    auto row_max = [&](int o) {
+                        const float a0 = ptx::max3(s[o], s[o + 1], s[o + 4]);
+                        const float a1 = ptx::max3(s[o + 5], s[o + 8], s[o + 9]);
+                        const float a2 = ptx::max3(s[o + 12], s[o + 13], s[o + 16]);
+                        const float a3 = ptx::max3(s[o + 17], s[o + 20], s[o + 21]);
+                        const float a4 = ptx::max3(s[o + 24], s[o + 25], s[o + 28]);
+                        return ptx::max3(ptx::max3(a0, a1, a2), a3, fmaxf(a4, s[o + 29]));
+                    };
+                    mxA = row_max(0);
+                    mxB = row_max(2);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
@@ -1030,14 +1038,17 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 // P = 2^(scale*s - m) as bf16 pairs (invalid slots give exactly
                 // 0); l sums the rounded values the MMA accumulates
                 uint32_t pw[16];
-                float sumA = 0.f, sumB = 0.f;
-                const float nA = -mA, nB = -mB;
+                uint64_t accA = 0ull, accB = 0ull;   // packed pairs of partial sums
+                const uint64_t sl22 = ptx::f2(sl2, sl2), nA2 = ptx::f2(-mA, -mA), nB2 = ptx::f2(-mB, -mB);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    float p0 = ex2_approx(fmaf(s[4 * k], sl2, nA));
-                    float p1 = ex2_approx(fmaf(s[4 * k + 1], sl2, nA));
-                    float p2 = ex2_approx(fmaf(s[4 * k + 2], sl2, nB));
-                    float p3 = ex2_approx(fmaf(s[4 * k + 3], sl2, nB));
+                    float z0, z1, z2, z3;
+                    ptx::f2_split(ptx::ffma2(ptx::f2(s[4 * k], s[4 * k + 1]), sl22, nA2), z0, z1);
+                    ptx::f2_split(ptx::ffma2(ptx::f2(s[4 * k + 2], s[4 * k + 3]), sl22, nB2), z2, z3);
+                    float p0 = ex2_approx(z0);
+                    float p1 = ex2_approx(z1);
+                    float p2 = ex2_approx(z2);
+                    float p3 = ex2_approx(z3);
                     if constexpr (!kPosScale) {
                         if (!full) {
                             const bool v0 = (vq >> (8 * k)) & 1ull, v1 = (vq >> (8 * k + 1)) & 1ull;
@@ -1047,11 +1058,16 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                             p3 = v1 ? p3 : 0.f;
                         }
                     }
-                    pw[2 * k] = pack_bf16(p0, p1, sumA);
-                    pw[2 * k + 1] = pack_bf16(p2, p3, sumB);
+                    pw[2 * k] = pack_bf16_acc(p0, p1, accA);
+                    pw[2 * k + 1] = pack_bf16_acc(p2, p3, accB);
                 }
-                lA += sumA;
-                lB += sumB;
+                {
+                    float a0, a1, b0, b1;
+                    ptx::f2_split(accA, a0, a1);
+                    ptx::f2_split(accB, b0, b1);
+                    lA += a0 + a1;
+                    lB += b0 + b1;
+                }
                 // P of these rows into P buffer sb (free once the P.V of tile
                 // a-2 is done in both CTAs of the pair), and with a partner
                 // the same rows into its buffer sb, with their rescale factors

@@ -152,31 +152,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Packed fp32 pairs (f32x2 arithmetic issues one instruction for two values).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -507,10 +482,10 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
                 constexpr int L = BN / 8;                   // values a chain
                 float a = s[L * i];
 #pragma unroll
-                for (int e = 1; e + 1 < L; e += 2) a = max3(a, s[L * i + e], s[L * i + e + 1]);
+                for (int e = 1; e + 1 < L; e += 2) a = ptx::max3(a, s[L * i + e], s[L * i + e + 1]);
                 mc[i] = (L % 2 == 0) ? fmaxf(a, s[L * i + L - 1]) : a;
             }
-            const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+            const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
             const float mt = POS ? mx * sc : mx;       // -inf when the row admits nothing here
             // lazy rescale: a new reference maximum only when it grows by more than 2^8
             float f = 1.f;
@@ -536,7 +511,7 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
             }
             // P = 2^(x - m) (masked keys: 2^-inf = 0), bf16 pairs
             const float nm = m_run == -INFINITY ? 0.f : -m_run;
-            const uint64_t sc2 = f2(sc, sc), nm2 = f2(nm, nm);
+            const uint64_t sc2 = ptx::f2(sc, sc), nm2 = ptx::f2(nm, nm);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // packed partial sums
             // P buffer sb is free once the P.V of tile n - NB is done
             if (n >= C::NB && !wait_all(bar(C::B_PV_DONE + sb), ((n / C::NB) - 1) & 1, p.err)) { ok = false; break; }
@@ -548,18 +523,18 @@ masked_dense_kernel(const MdParams p, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                 for (int c2 = 0; c2 < 32; ++c2) {
                     const int c = 32 * k + c2;
-                    const uint64_t xy = f2(s[2 * c], s[2 * c + 1]);
+                    const uint64_t xy = ptx::f2(s[2 * c], s[2 * c + 1]);
                     float z0, z1;
-                    f2_split(POS ? ffma2(xy, sc2, nm2) : fadd2(xy, nm2), z0, z1);
+                    ptx::f2_split(POS ? ptx::ffma2(xy, sc2, nm2) : ptx::fadd2(xy, nm2), z0, z1);
                     const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-                    acc[c & 3] = fadd2(acc[c & 3], f2(p0, p1));
+                    acc[c & 3] = ptx::fadd2(acc[c & 3], ptx::f2(p0, p1));
                     q32[c2] = pack_bf16(p0, p1);
                 }
                 ptx::tmem_st32(lane_base + C::P_COL + sb * (BN / 2) + 32 * k, q32);
             }
             float l0, l1, l2, l3;
-            f2_split(fadd2(acc[0], acc[1]), l0, l1);
-            f2_split(fadd2(acc[2], acc[3]), l2, l3);
+            ptx::f2_split(ptx::fadd2(acc[0], acc[1]), l0, l1);
+            ptx::f2_split(ptx::fadd2(acc[2], acc[3]), l2, l3);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
