@@ -90,7 +90,7 @@ constexpr int kOtherRegs = 96;
 constexpr int kF8Row = 584;
 // FP8 gather roles: of the 7 gather warps, the first copy raw rows into the
 // staging ring and the others widen them into the kv stages
-constexpr int kF8CopyWarps = 3;
+constexpr int kF8CopyWarps = 2;
 constexpr int kF8WidenWarps = kGatherWarps - kF8CopyWarps;
 constexpr int kF8ScaleOff = 576;
 
@@ -540,65 +540,67 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 // 0..255) or [256, 576) (half 1: codes of dims 256..447, then the
                 // 64 RoPE dims in bf16), plus the scale bytes [576, 584).  A row
                 // starts 8 bytes past a 16-byte boundary when its index is odd, so
-                // the copies are the 16-byte-aligned windows covering those bytes
-                // (16-byte cp.async, L2 only): an odd row's first window starts 8
-                // bytes early, inside the previous row, and for half 1 its last
-                // window holds the scale bytes; otherwise one more window brings
-                // them.  In a staging row the wanted bytes then start at `shift`
-                // (0 for an even row, 8 for an odd one) and the scale bytes sit at
-                // STG_SCALE + shift.
-                //
-                // Copy warps: a tile is W copy items a row (windows, then the scale
-                // copy; W = 18 for half 0, 21 for half 1), 32 consecutive items per
-                // instruction, instructions dealt round-robin to the copy warps;
-                // every lane's copies arrive on stg_full when they land, so the
-                // copy warps run NF tiles ahead.  Widen warps: lane l turns 8 dims
-                // (8l.. of this half; lanes 24-31 of half 1 pass the RoPE dims
-                // through) of rows w, w + 3, ... into bf16 in the 128B-swizzled kv
+                // the copies start on the 16-byte boundary at or below the first
+                // wanted byte.  In a staging row the wanted bytes then start at
+                // `shift` (0 for an even row, 8 for an odd one) and the scale bytes
+                // sit at STG_SCALE + shift.  The copy warps run NF tiles ahead; the
+                // widen warps turn the staged rows into bf16 in the 128B-swizzled kv
                 // stage the MMA reads, then free the staging buffer.
                 const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
                 const uint8_t *kv8x = reinterpret_cast<const uint8_t *>(p.kv2);   // extra FP8 rows
                 const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
-                const int nwin = crank == 0 ? 16 : 20;            // windows of an even row
                 if (warp < kFirstGatherWarp + kF8CopyWarps) {
+                    // Copy warps: lane l of copy warp c takes the rows r = 32 (c + kF8CopyWarps i) + l
+                    // of every tile.  A valid row's wanted bytes come by one bulk copy (16-byte
+                    // aligned at both ends: [0, 256) or [-8, 264) for half 0, [256, 576) or
+                    // [248, 584) for half 1, the latter with the scale bytes), its scale bytes by
+                    // one more copy when they are not inside it: an even row's [576, 584) by a
+                    // cp.async that reads only those 8 bytes (a bulk copy of the 16-byte window
+                    // would read past the last row), half 0 of an odd row as the bulk copy of
+                    // [568, 584).  Each lane adds its bulk bytes to the staging barrier before
+                    // issuing them and arrives (noinc) once its cp.async has landed; invalid rows
+                    // are not copied (the widen warps write zeros for them).
                     const int cw = warp - kFirstGatherWarp;
-                    const int W = crank == 0 ? 18 : 21;           // copy items per row
-                    const int n_instr = (kBN * W + 31) / 32;
-                    bool ok = true;
-                    for (int a = 0; a < n_act && ok; ++a) {
+                    const uint32_t data_even = crank == 0 ? 256u : 320u;   // + 16 for an odd row
+                    int a = 0;
+                    for (; a < n_act; ++a) {
                         const int f = a % C::NF;
-                        if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) {
-                            ok = false;
-                            break;
-                        }
+                        if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) break;
                         const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
                         const int32_t *rc = rowc + act[a] * kBN;
-                        for (int j = cw; j < n_instr; j += kF8CopyWarps) {
-                            const int it = j * 32 + lane;
-                            const int r = it / W, w = it - r * W;
-                            if (r >= kBN) continue;
+                        uint32_t tx = 0;
+                        for (int r = cw * 32 + lane; r < kBN; r += 32 * kF8CopyWarps) {
                             const int32_t row = rc[r];
+                            if (row >= 0) {
+                                const int64_t rr = row >= p.BT ? int64_t(row) - p.BT : int64_t(row);
+                                tx += (rr & 1) ? data_even + 16u + (crank == 0 ? 16u : 0u) : data_even;
+                            }
+                        }
+                        if (tx != 0u) ptx::mbar_expect_tx(stg_full(f), tx);
+                        for (int r = cw * 32 + lane; r < kBN; r += 32 * kF8CopyWarps) {
+                            const int32_t row = rc[r];
+                            if (row < 0) continue;
                             // row in its own source (extra rows rebased past the even BT)
                             const bool xr = row >= p.BT;
-                            const int64_t rr = row < 0 ? 0 : xr ? int64_t(row) - p.BT : int64_t(row);
-                            const uint32_t n = row >= 0 ? 16u : 0u;
+                            const int64_t rr = xr ? int64_t(row) - p.BT : int64_t(row);
                             const int shift = int(rr & 1) * 8;
+                            const uint8_t *rowp = (xr ? kv8x : kv8) + rr * kF8Row;
                             const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
-                            const int nw = nwin + (shift >> 3);
-                            // one 16-byte copy per item, the same instruction for
-                            // every lane: a window, or the scale window (an even
-                            // row's [576, 592) reads only its 8 scale bytes, the
-                            // rest is zero-filled; half 0 of an odd row takes
-                            // [568, 584); half 1 of an odd row has it as its last
-                            // window), or nothing
-                            const bool win = w < nw;
-                            const bool scl = w == nw && (!shift || crank == 0);
-                            const uint8_t *src = (xr ? kv8x : kv8) + rr * kF8Row +
-                                                 (win ? base_x - shift + 16 * w : kF8ScaleOff - shift);
-                            const uint32_t dst = d + (win ? 16u * uint32_t(w) : uint32_t(C::STG_SCALE));
-                            if (win || scl) ptx::cp_async_16(dst, src, win || shift ? n : (n >> 1));
+                            ptx::bulk_load(d, rowp + (base_x - shift), data_even + uint32_t(2 * shift), stg_full(f));
+                            if (shift == 0)
+                                ptx::cp_async_16(d + uint32_t(C::STG_SCALE), rowp + kF8ScaleOff, 8u);
+                            else if (crank == 0)
+                                ptx::bulk_load(d + uint32_t(C::STG_SCALE), rowp + (kF8ScaleOff - 8), 16u, stg_full(f));
                         }
                         ptx::cp_async_arrive_noinc(stg_full(f));
+                    }
+                    // nothing of ours still lands after the CTA exits: the last fill of
+                    // every staging buffer this warp wrote has completed (bounded)
+                    for (int k = a > C::NF ? a - C::NF : 0; k < a; ++k) {
+                        const long long t0 = clock64();
+                        while (!ptx::mbar_try_wait(stg_full(k % C::NF), uint32_t(k / C::NF) & 1u) &&
+                               clock64() - t0 < kWaitCycles) {
+                        }
                     }
                 } else {
                     // widen warps: half-warp h of warp ww takes rows 2 (ww + W i) + h;
@@ -630,13 +632,15 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                             // every load of the batch before the first conversion
                             uint2 v[CB][2], w[CB][2];
                             uint32_t sb[CB];
+                            bool inval[CB];
 #pragma unroll
                             for (int k = 0; k < CB; ++k) {
                                 const int r = 2 * ((i0 + k) * kF8WidenWarps + ww) + h;
                                 if (i0 + k >= IT || r >= kBN) break;
                                 const int32_t row = rc[r];
-                                // as copied (an invalid row came as row 0)
+                                // as copied (an invalid row was not copied: zeros below)
                                 const int shift = row > 0 ? (row & 1) * 8 : 0;
+                                inval[k] = row < 0;
                                 const uint8_t *srow = stg + r * C::STG_ROW;
                                 const uint8_t *src = srow + shift + off;
                                 v[k][0] = *reinterpret_cast<const uint2 *>(src);
@@ -677,6 +681,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                                         o1.w = e4m3x2_scaled_bf16x2(v[k][1].y >> 16, sc);
                                     }
                                 }
+                                if (inval[k]) o0 = o1 = make_uint4(0u, 0u, 0u, 0u);   // an invalid slot's row is 0
                                 uint8_t *line = stage + blk * (kBN * 128) + uint32_t(r) * 128u;
                                 const uint32_t c0 = c_first, c1 = c_first ^ 1u;   // chunk of dims 0-7 is 2(u&3)
                                 const uint4 first = (c0 & 1u) ? o1 : o0, second = (c0 & 1u) ? o0 : o1;
