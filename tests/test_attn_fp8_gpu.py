@@ -121,3 +121,26 @@ def test_zero_and_subnormal_codes_at_the_fast_and_exact_paths(scale_byte):
     o = _run(inp, scale=0.02)
     want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, 0.02)
     assert_close(o, want, f"subnormal codes, scale byte {scale_byte}")
+
+
+def test_rows_no_valid_slot_points_at_are_never_read():
+    # every row that no valid slot points at, row 0 included, holds NaN codes
+    # and NaN scales; invalid slots (-1, past T) must contribute exact zeros,
+    # never a NaN through P.V (the copy path does not copy their rows)
+    inp = workloads.random_attn_fp8(2, 2, 16, 300, 130, p_invalid=0.3, seed=21)
+    idx = inp.topk_idxs.clone()
+    idx[0, 0, :5] = 300                       # past T: invalid
+    idx[idx == 0] = 1                         # no valid slot points at row 0
+    inp.topk_idxs = idx
+    used = torch.zeros(2, 300, dtype=torch.bool)
+    for b in range(2):
+        v = idx[b][(idx[b] >= 0) & (idx[b] < 300)]
+        used[b, v.long()] = True
+    kv8 = inp.kv8.clone()
+    kv8[~used] = 0xFF                         # E4M3 NaN codes, NaN bf16 RoPE values, E8M0 255 = NaN scales
+    inp.kv8 = kv8
+    assert not used[:, 0].any()
+    o = _run(inp)
+    assert torch.isfinite(o.float()).all()
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    assert_close(o, want, "NaN rows that no valid slot reads")
