@@ -220,11 +220,12 @@ def gather_ceiling(dev, flush):
     return res[1024], res[512]
 
 
-def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None, spread: bool = False):
+def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None, spread: bool = False, fp8: bool = False):
     """Time the oracle (as it stands) on whole tokens of the workload until
     about budget_s of wall time; returns (tokens/s, tokens, seconds, threads).
     spread: take the tokens in a scattered order over the whole batch (a
-    multiplicative hash of the position) instead of from its start."""
+    multiplicative hash of the position) instead of from its start.  fp8:
+    the workload's kv cache is in the FP8 row format (``inp.kv8``)."""
     import numpy as np
 
     import oracle
@@ -238,8 +239,12 @@ def cpu_oracle_time(inp, budget_s: float, max_tokens: int | None = None, spread:
         tok = np.arange(start_tok, start_tok + chunk, dtype=np.int64)
         tok = (tok * 2654435761) % ntok if spread else tok % ntok
         t0 = time.perf_counter()
-        oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, tokens=tok,
-                           nthreads=threads)
+        if fp8:
+            oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, tokens=tok,
+                                   nthreads=threads)
+        else:
+            oracle.sparse_attn(inp.q, inp.kv, inp.attn_sink, inp.topk_idxs, inp.softmax_scale, tokens=tok,
+                               nthreads=threads)
         elapsed += time.perf_counter() - t0
         done += chunk
         start_tok += chunk
@@ -593,6 +598,10 @@ def run_gpu(args):
                            "l2": l2_note}
             if eager_us is not None:
                 other[name]["eager_single_call_us"] = eager_us
+                cv, cn, csec, cth = cpu_oracle_time(wc, min(args.cpu_budget, 3.0), spread=True)
+                other[name]["cpu_baseline"] = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
+                                               "sample": f"{cn} query tokens x 128 heads scattered over the "
+                                                         f"batch, {csec:.1f} s"}
             assert binding.sa_device_error(True) == 0
             if name == "v4_prefill":
                 # the prefill's own CPU baseline (tokens scattered over the
@@ -688,6 +697,10 @@ def run_gpu(args):
             "roofline_frac": roof / (ms_f * 1e-3), "compute_frac": fl / (tf_o * 1e12) / (ms_f * 1e-3),
             "launches_per_call": binding.sa_sparse_attn_fp8_launch_count(Bf, Sf, Hf, Kf),
             "eager_single_call_us": eager_f,
+            "cpu_baseline": (lambda r: {"value": r[0], "unit": UNIT, "cores": r[3], "kind": "oracle",
+                                        "sample": f"{r[1]} query tokens x 128 heads scattered over the batch, "
+                                                  f"{r[2]:.1f} s"})(
+                cpu_oracle_time(fc, min(args.cpu_budget, 3.0), spread=True, fp8=True)),
             "l2": f"50 calls in one CUDA graph over {ROTATE_SETS} rotating input sets larger than L2 (as the headline); "
                   "eager_single_call_us: one call at a time after an L2 flush"}
         del fd, fc
@@ -735,6 +748,14 @@ def run_gpu(args):
                     "roofline": {"bound": "hbm", "achieved": m_gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": m_gbs / hbm, "peak_source": src,
                                  "traffic": _profile_traffic("mask_build", _source_hash(MASK_SOURCES))}}
+        # the oracle's build of the same workload (all 8192 rows), on the host
+        import oracle
+        mc = workloads.topk_mask()
+        t0 = time.perf_counter()
+        oracle.build_topk_mask(mc.topk, mc.cu_q_lens, mc.batch, mc.max_q_len, mc.max_key_len, mc.key_starts)
+        osec = time.perf_counter() - t0
+        mask_obj["cpu_baseline"] = {"value": m_bytes / osec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"the whole workload ({mc.batch} x {mc.max_q_len} rows), {osec:.2f} s"}
         del sets[1:]
 
         # ---- the mask's consumer: dense attention over the admitted keys of
