@@ -57,6 +57,9 @@ constexpr int kLaunchRegs = 128;
 constexpr int kSoftmaxRegs = 200;
 constexpr int kOtherRegs = 56;
 static_assert(128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
+// setmaxnreg acts on whole warpgroups: every warpgroup of the CTA must be
+// complete and execute the same setmaxnreg
+static_assert(kThreads % 128 == 0, "whole warpgroups");
 constexpr int kMaxTiles = 8192;          // key tiles per work unit (the host enforces it)
 constexpr int kBitmapWords = kMaxTiles / 32;
 constexpr long long kWaitCycles = 200000000ll;   // ~0.1 s at 2 GHz per wait
