@@ -16,7 +16,9 @@
 //   warps 9..15 (gather) copy the DC-column slice of each tile's 64 indexed
 //                        kv rows with 16-byte cp.async (invalid slots
 //                        zero-filled) into the 128B-swizzled K-major stage the
-//                        MMAs read;
+//                        MMAs read (an FP8 kv cache: warps 9-10 bulk-copy each
+//                        row's bytes into a staging ring, warps 11-15 widen
+//                        them to bf16 in the stage);
 //   warp 8 (MMA)         S = Q_c K_c^T with Q_c resident in TMEM, into one of
 //                        two S buffers (QK^T runs up to two tiles ahead of
 //                        the softmax); O_c += P V_c with P (bf16) in one of two
@@ -44,7 +46,9 @@
 // bounded by clock64 and gives up early once any wait of any kernel has
 // recorded an error, so a failing launch drains in about one wait bound.
 // The cluster barriers of the prologue and teardown are hardware barriers
-// that every CTA of the cluster reaches on every path.
+// that every CTA of the cluster reaches on every path.  The kernel launches with
+// a programmatic dependency on the stream's previous kernel: every thread
+// waits for it (griddepcontrol.wait) before its first global memory access.
 #include <cuda_bf16.h>
 
 #include <cudaTypedefs.h>
@@ -88,8 +92,8 @@ constexpr int kOtherRegs = 96;
 // dims as bf16, then one E8M0 scale byte per 64-dim tile of the codes (7 used,
 // 1 pad): 584 bytes, so a row starts on an 8-byte boundary only.
 constexpr int kF8Row = 584;
-// FP8 gather roles: of the 7 gather warps, the first copy raw rows into the
-// staging ring and the others widen them into the kv stages
+// FP8 gather roles: of the 7 gather warps, the first kF8CopyWarps copy raw
+// rows into the staging ring and the others widen them into the kv stages
 constexpr int kF8CopyWarps = 2;
 constexpr int kF8WidenWarps = kGatherWarps - kF8CopyWarps;
 constexpr int kF8ScaleOff = 576;
