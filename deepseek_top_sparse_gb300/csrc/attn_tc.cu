@@ -92,10 +92,9 @@ constexpr int kOtherRegs = 96;
 // dims as bf16, then one E8M0 scale byte per 64-dim tile of the codes (7 used,
 // 1 pad): 584 bytes, so a row starts on an 8-byte boundary only.
 constexpr int kF8Row = 584;
-// FP8 gather roles: of the 7 gather warps, the first kF8CopyWarps copy raw
-// rows into the staging ring and the others widen them into the kv stages
-constexpr int kF8CopyWarps = 2;
-constexpr int kF8WidenWarps = kGatherWarps - kF8CopyWarps;
+// FP8 gather: every gather warp bulk-copies raw rows into the staging ring
+// (three tiles ahead) and widens the same rows into the kv stages
+constexpr int kF8WidenWarps = kGatherWarps;
 constexpr int kF8ScaleOff = 576;
 
 template <int DC, int CL, bool F8 = false>
@@ -112,7 +111,7 @@ struct Cfg {
     // FP8: the raw bytes of a tile land in one of NF staging buffers (one
     // 336-byte row per kv row: this CTA's 256 or 320 bytes of codes / RoPE
     // values at [0, 320), its scale bytes at 320) and are widened to bf16
-    // into a kv stage by the gather warps; the copy warps run NF tiles ahead
+    // into a kv stage by the gather warps, which copy their own rows NF tiles ahead
     static constexpr int NF = F8 ? 3 : 0;
     static constexpr int STG_ROW = 336;
     static constexpr int STG_SCALE = 320;
@@ -454,7 +453,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
         ptx::mbar_init(q_smem, 1);
         ptx::mbar_init(q_free, kSoftmaxThreads);
         for (int f = 0; f < C::NF; ++f) {
-            ptx::mbar_init(stg_full(f), 32 * kF8CopyWarps);
+            ptx::mbar_init(stg_full(f), 32 * kF8WidenWarps);
             ptx::mbar_init(stg_empty(f), kF8WidenWarps);
         }
         ptx::mbar_init(rcv_bar, 1);   // thread 0's expect_tx + the bytes of every box
@@ -547,47 +546,53 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 // the copies start on the 16-byte boundary at or below the first
                 // wanted byte.  In a staging row the wanted bytes then start at
                 // `shift` (0 for an even row, 8 for an odd one) and the scale bytes
-                // sit at STG_SCALE + shift.  The copy warps run NF tiles ahead; the
-                // widen warps turn the staged rows into bf16 in the 128B-swizzled kv
-                // stage the MMA reads, then free the staging buffer.
+                // sit at STG_SCALE + shift.  Every gather warp copies the rows it will
+                // widen NF tiles ahead, turns the staged rows of the current tile into
+                // bf16 in the 128B-swizzled kv stage the MMA reads, and frees the
+                // staging buffer; a buffer is refilled once all gather warps freed it.
                 const uint8_t *kv8 = reinterpret_cast<const uint8_t *>(p.kv);
                 const uint8_t *kv8x = reinterpret_cast<const uint8_t *>(p.kv2);   // extra FP8 rows
                 const int base_x = crank == 0 ? 0 : 256;          // first wanted byte of a row
-                if (warp < kFirstGatherWarp + kF8CopyWarps) {
-                    // Copy warps: lane l of copy warp c takes the rows r = 32 (c + kF8CopyWarps i) + l
-                    // of every tile.  A valid row's wanted bytes come by one bulk copy (16-byte
-                    // aligned at both ends: [0, 256) or [-8, 264) for half 0, [256, 576) or
-                    // [248, 584) for half 1, the latter with the scale bytes), its scale bytes by
-                    // one more copy when they are not inside it: an even row's [576, 584) by a
-                    // cp.async that reads only those 8 bytes (a bulk copy of the 16-byte window
-                    // would read past the last row), half 0 of an odd row as the bulk copy of
-                    // [568, 584).  Each lane adds its bulk bytes to the staging barrier before
-                    // issuing them and arrives (noinc) once its cp.async has landed; invalid rows
-                    // are not copied (the widen warps write zeros for them).
-                    const int cw = warp - kFirstGatherWarp;
+                {
+                    // half-warp h of gather warp ww widens rows 2 (ww + W i) + h;
+                    // lane u of the half-warp owns 16 dims (16u.. of this half): 16
+                    // codes, or for u >= 12 of half 1 the RoPE dims 448 + 16 (u - 12)
+                    // as bf16, and stores them as two 16-byte chunks, odd chunk
+                    // first in every other 64-dim block so each 8-lane store phase
+                    // covers eight distinct bank groups
+                    const int ww = warp - kFirstGatherWarp;
+                    const int h = lane >> 4, u = lane & 15;
+                    constexpr int IT = kBN / (2 * kF8WidenWarps) + (kBN % (2 * kF8WidenWarps) ? 1 : 0);
+                    constexpr int CB = 4;                                            // row pairs per load batch
+                    const bool rope = crank == 1 && u >= 12;
+                    const int sc_idx = crank == 0 ? (u >> 2) : 4 + (u >> 2);         // scale byte of the lane's tile
+                    const int off = rope ? 192 + 32 * (u - 12) : 16 * u;             // lane's bytes in a staging row
+                    const uint32_t blk = uint32_t(u >> 2);                           // 64-dim block of the stage
+                    const uint32_t c_first = 2u * uint32_t(u & 3) + (blk & 1u);      // chunk stored first
+                    // the bulk copies of this warp's own rows of tile a into staging a % NF:
+                    // lane l < 2 IT copies row 2 (IT-index (l / 2) * kF8WidenWarps + ww) + l % 2,
+                    // the row that half-warp l % 2 widens in iteration l / 2.  A valid row's
+                    // wanted bytes come by one bulk copy, 16-byte aligned at both ends:
+                    // [0, 256) or [-8, 264) for half 0, [256, 576) or [248, 584) for half 1,
+                    // the latter with the scale bytes.  The scale bytes of an even row come
+                    // by a cp.async that reads only those 8 bytes (a bulk copy of their
+                    // 16-byte window would read past the last row); half 0 of an odd row
+                    // takes the bulk copy of [568, 584).  Each lane adds its bulk bytes to
+                    // the staging barrier before issuing them and arrives (noinc) once its
+                    // cp.async has landed; invalid rows are not copied (zeros below).
                     const uint32_t data_even = crank == 0 ? 256u : 320u;   // + 16 for an odd row
-                    int a = 0;
-                    for (; a < n_act; ++a) {
-                        const int f = a % C::NF;
-                        if (a >= C::NF && !wait_all(stg_empty(f), ((a / C::NF) - 1) & 1)) break;
+                    auto issue_copies = [&](int ta) {
+                        const int f = ta % C::NF;
                         const uint32_t stg = ptx::smem_u32(smem + C::OFF_STG + f * C::STG_BYTES);
-                        const int32_t *rc = rowc + act[a] * kBN;
-                        uint32_t tx = 0;
-                        for (int r = cw * 32 + lane; r < kBN; r += 32 * kF8CopyWarps) {
-                            const int32_t row = rc[r];
-                            if (row >= 0) {
-                                const int64_t rr = row >= p.BT ? int64_t(row) - p.BT : int64_t(row);
-                                tx += (rr & 1) ? data_even + 16u + (crank == 0 ? 16u : 0u) : data_even;
-                            }
-                        }
-                        if (tx != 0u) ptx::mbar_expect_tx(stg_full(f), tx);
-                        for (int r = cw * 32 + lane; r < kBN; r += 32 * kF8CopyWarps) {
-                            const int32_t row = rc[r];
-                            if (row < 0) continue;
+                        const int r = lane < 2 * IT ? 2 * ((lane >> 1) * kF8WidenWarps + ww) + (lane & 1) : kBN;
+                        const int32_t row = r < kBN ? rowc[act[ta] * kBN + r] : -1;
+                        if (row >= 0) {
                             // row in its own source (extra rows rebased past the even BT)
                             const bool xr = row >= p.BT;
                             const int64_t rr = xr ? int64_t(row) - p.BT : int64_t(row);
                             const int shift = int(rr & 1) * 8;
+                            const uint32_t tx = shift ? data_even + 16u + (crank == 0 ? 16u : 0u) : data_even;
+                            ptx::mbar_expect_tx(stg_full(f), tx);
                             const uint8_t *rowp = (xr ? kv8x : kv8) + rr * kF8Row;
                             const uint32_t d = stg + uint32_t(r) * C::STG_ROW;
                             ptx::bulk_load(d, rowp + (base_x - shift), data_even + uint32_t(2 * shift), stg_full(f));
@@ -597,32 +602,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                                 ptx::bulk_load(d + uint32_t(C::STG_SCALE), rowp + (kF8ScaleOff - 8), 16u, stg_full(f));
                         }
                         ptx::cp_async_arrive_noinc(stg_full(f));
-                    }
-                    // nothing of ours still lands after the CTA exits: the last fill of
-                    // every staging buffer this warp wrote has completed (bounded)
-                    for (int k = a > C::NF ? a - C::NF : 0; k < a; ++k) {
-                        const long long t0 = clock64();
-                        while (!ptx::mbar_try_wait(stg_full(k % C::NF), uint32_t(k / C::NF) & 1u) &&
-                               clock64() - t0 < kWaitCycles) {
-                        }
-                    }
-                } else {
-                    // widen warps: half-warp h of warp ww takes rows 2 (ww + W i) + h;
-                    // lane u of the half-warp owns 16 dims (16u.. of this half): 16
-                    // codes, or for u >= 12 of half 1 the RoPE dims 448 + 16 (u - 12)
-                    // as bf16, and stores them as two 16-byte chunks, odd chunk
-                    // first in every other 64-dim block so each 8-lane store phase
-                    // covers eight distinct bank groups
-                    const int ww = warp - kFirstGatherWarp - kF8CopyWarps;
-                    const int h = lane >> 4, u = lane & 15;
-                    constexpr int IT = kBN / (2 * kF8WidenWarps) + (kBN % (2 * kF8WidenWarps) ? 1 : 0);
-                    constexpr int CB = 4;                                            // row pairs per load batch
-                    const bool rope = crank == 1 && u >= 12;
-                    const int sc_idx = crank == 0 ? (u >> 2) : 4 + (u >> 2);         // scale byte of the lane's tile
-                    const int off = rope ? 192 + 32 * (u - 12) : 16 * u;             // lane's bytes in a staging row
-                    const uint32_t blk = uint32_t(u >> 2);                           // 64-dim block of the stage
-                    const uint32_t c_first = 2u * uint32_t(u & 3) + (blk & 1u);      // chunk stored first
-                    for (int a = 0; a < n_act; ++a) {
+                    };
+                    static_assert(2 * IT <= 32, "one copied row per lane");
+                    for (int ta = 0; ta < C::NF && ta < n_act; ++ta) issue_copies(ta);
+                    int a = 0;
+                    for (; a < n_act; ++a) {
                         const int s = a % C::NS, fs = a / C::NS, f = a % C::NF;
                         if (!wait_all(stg_full(f), (a / C::NF) & 1)) break;
                         if (fs >= 1 && !wait_all(kv_empty(s), (fs - 1) & 1)) break;
@@ -697,6 +681,20 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                         ptx::mbar_arrive(kv_full(s));
                         __syncwarp();                    // every lane done with the staging rows ...
                         if (lane == 0) ptx::mbar_arrive(stg_empty(f));   // ... before they are refilled
+                        // staging f takes tile a + NF once every gather warp has widened tile a
+                        if (a + C::NF < n_act) {
+                            if (!wait_all(stg_empty(f), uint32_t(a / C::NF) & 1u)) break;
+                            issue_copies(a + C::NF);
+                        }
+                    }
+                    // nothing of ours still lands after the CTA exits: the last fill of
+                    // every staging buffer has completed (bounded)
+                    const int issued = a + C::NF < n_act ? a + C::NF : n_act;
+                    for (int k = issued > C::NF ? issued - C::NF : 0; k < issued; ++k) {
+                        const long long t0 = clock64();
+                        while (!ptx::mbar_try_wait(stg_full(k % C::NF), uint32_t(k / C::NF) & 1u) &&
+                               clock64() - t0 < kWaitCycles) {
+                        }
                     }
                 }
                 ptx::cp_async_wait_all();   // nothing of ours still lands after the CTA exits
