@@ -105,3 +105,31 @@ def test_fp8_two_sources(ns):
     len1, len2 = _lens(2, 2, 400, 8), _lens(2, 2, 150, 9)
     o, want = _run(main, extra, len1, len2, ns, fp8=True)
     assert_close(o, want, f"fp8 two sources splits={ns}")
+
+
+@pytest.mark.parametrize("ns", [0, 2])
+def test_fp8_even_last_rows_of_both_sources(ns):
+    # both sources end on a row with an even index (B*T and B*T2 odd); the
+    # bytes after each hold NaN patterns, and several slots of every token of
+    # the last request pick each source's last row
+    B, S, H = 3, 2, 128
+    main = workloads.random_attn_fp8(B, S, H, 101, 96, p_invalid=0.1, seed=61 + ns)
+    extra = workloads.random_attn_fp8(B, S, H, 51, 40, p_invalid=0.1, seed=62 + ns)
+    i1, i2 = main.topk_idxs.clone(), extra.topk_idxs.clone()
+    i1[B - 1, :, :5] = 100
+    i2[B - 1, :, 3:9] = 50
+    main.topk_idxs, extra.topk_idxs = i1, i2
+
+    def poisoned(kv8):
+        n = kv8.shape[0] * kv8.shape[1]
+        big = torch.full((n + 2, 584), 0xFF, dtype=torch.uint8, device="cuda")
+        big[:n] = kv8.reshape(n, 584).cuda()
+        return big[:n].view(kv8.shape)
+
+    o = binding.sparse_attn_extra(main.q.cuda(), poisoned(main.kv8), main.attn_sink.cuda(), i1.cuda(),
+                                  poisoned(extra.kv8), i2.cuda(), main.softmax_scale, num_splits=ns)
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    want = oracle.sparse_attn_fp8(main.q, main.kv8, main.attn_sink, i1, main.softmax_scale,
+                                  extra_idxs=i2, extra_kv8=extra.kv8)
+    assert_close(o, want, f"fp8 even last rows splits={ns}")

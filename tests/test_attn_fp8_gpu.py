@@ -144,3 +144,24 @@ def test_rows_no_valid_slot_points_at_are_never_read():
     assert torch.isfinite(o.float()).all()
     want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
     assert_close(o, want, "NaN rows that no valid slot reads")
+
+
+def test_even_last_row_of_the_cache_with_poison_after_it():
+    # B*T odd: the cache's last row has an even index, and a 16-byte-aligned
+    # window over its scale bytes would reach 8 bytes past the cache.  The
+    # bytes after the cache hold NaN patterns; the last row is picked by
+    # several slots of every token of the last request.
+    B, S, H, T, K = 3, 2, 16, 101, 64
+    inp = workloads.random_attn_fp8(B, S, H, T, K, p_invalid=0.1, seed=77)
+    idx = inp.topk_idxs.clone()
+    idx[B - 1, :, :6] = T - 1
+    inp.topk_idxs = idx
+    big = torch.full((B * T + 2, 584), 0xFF, dtype=torch.uint8, device="cuda")
+    big[: B * T] = inp.kv8.reshape(B * T, 584).cuda()
+    kv = big[: B * T].view(B, T, 584)
+    d = inp.to("cuda")
+    o = binding.sparse_attn_fp8(d.q, kv, d.attn_sink, d.topk_idxs, inp.softmax_scale)
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    want = oracle.sparse_attn_fp8(inp.q, inp.kv8, inp.attn_sink, inp.topk_idxs, inp.softmax_scale)
+    assert_close(o, want, "even last row of the cache")
