@@ -1234,7 +1234,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
         const float2 st = stat[hr];
         const float sink2 = sink_tab[hr] * kLog2e;
         const int ns = p.num_splits;
-        const int32_t y_o = int32_t(iotok * p.H);                         // o rows of the token
         const int32_t y_ws = int32_t((tok * ns + split) * p.H);           // workspace rows of this split
         // chunk cc of the slice (fp32; 0 when the unit had no live tile); all
         // 32 lanes load (tcgen05.ld is warp-collective)
@@ -1281,6 +1280,26 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
             ptx::fence_proxy_async_smem();
             __syncthreads();
         };
+        // o from the staged bf16 boxes of granules [g0, g1) at `base` (box j:
+        // the token's rows by 64 columns, 128B-swizzled), once every thread
+        // has staged: 16-byte chunk c of row r goes to thread (r * cpr + c) mod
+        // 512, so a warp writes whole rows of this CTA's columns, contiguous in
+        // o.  Plain stores let the CTA finish without waiting for a copy engine
+        // to read its shared memory.
+        auto store_o = [&](int base, int g0, int g1) {
+            __syncthreads();
+            // (a split finishes 1, 2 or 4 granules: NG is 1, 2 or 4 and the
+            // splits share them out as floor(s NG / ns))
+            const int cs_shift = 3 + (31 - __clz(g1 - g0));   // log2 of the 16-byte chunks a row
+            const int nchunks = p.H << cs_shift;
+            __nv_bfloat16 *orow = p.o + int64_t(iotok * p.H) * p.D + int64_t(crank) * DC + 64 * g0;
+            for (int i = tid; i < nchunks; i += C::THREADS) {
+                const int r = i >> cs_shift, c = i & ((1 << cs_shift) - 1);
+                const uint4 v = *reinterpret_cast<const uint4 *>(smem + base + (g0 + (c >> 3)) * BOX + r * 128 +
+                                                                (((c & 7) ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4 *>(orow + int64_t(r) * p.D + 8 * c) = v;
+            }
+        };
         const uint32_t sbase = ptx::smem_u32(smem);
         if (ns == 1) {
             float f = 0.f;
@@ -1296,12 +1315,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                 load_chunk(cc, x);
                 if (rv) stage_bf16(0, c_slice + cc * CC, x, f);
             }
-            publish();
-            if (tid == 0) {
-                for (int j = 0; j < NG; ++j) ptx::tma_store_2d(&omap, sbase + j * BOX, int32_t(crank) * DC + 64 * j, y_o);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
-            }
+            store_o(0, 0, NG);
         } else if (!p.fused) {
             const float f = n_act > 0 ? 1.f / st.y : 0.f;
 #pragma unroll 1
@@ -1429,13 +1443,8 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap qmap, const
                     stage_bf16(hbase, c_slice + cc * CC, x, 1.f);
                 }
             }
-            publish();
-            if (tid == 0) {
-                for (int j = gs0; j < gs1; ++j)
-                    ptx::tma_store_2d(&omap, sbase + hbase + j * BOX, int32_t(crank) * DC + 64 * j, y_o);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
-            }
+            if (gs1 > gs0) store_o(hbase, gs0, gs1);
+            else __syncthreads();
         }
     }
     ptx::tc_fence_before();
