@@ -4,7 +4,8 @@ It serves callers that cannot hand the library device memory (a C host
 program without a device allocator, or a serving loop that forbids cudaMalloc
 on its hot path): the split-KV workspace is an array inside the library.  It
 must give what the regular entry point gives with a caller-supplied
-workspace, on consecutive calls that reuse the same array.  This file is
+workspace, on consecutive calls that reuse the same array, and match the
+oracle to the attention parity bar.  This file is
 collected last so that a run stopping at the first failure has already run
 every other test."""
 
@@ -12,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from deepseek_top_sparse_gb300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
@@ -59,6 +61,20 @@ def test_static_workspace_matches_regular_entry_on_consecutive_calls():
     got = _static(first, 0)
     torch.cuda.synchronize()
     _close(got, ref)
+
+
+@pytest.mark.parametrize("ns", [0, 5])
+def test_static_workspace_matches_the_oracle(ns):
+    # the same bar as every attention parity test, straight against the
+    # oracle: splits combined in the cluster (planner's choice) and by the
+    # separate combine kernel (5 splits)
+    c = workloads.random_attn(3, 2, 128, 512, 3000, 1152, p_invalid=0.2, seed=78 + ns)
+    got = _static(c.to("cuda"), ns)
+    torch.cuda.synchronize()
+    assert binding.sa_device_error(True) == 0
+    want = oracle.sparse_attn(c.q, c.kv, c.attn_sink, c.topk_idxs, c.softmax_scale)
+    g = got.double().cpu().numpy()
+    assert np.all(np.abs(g - want) <= ATOL + RTOL * np.abs(want))
 
 
 def test_static_workspace_rejects_plans_larger_than_the_array():
